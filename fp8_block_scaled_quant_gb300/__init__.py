@@ -1,0 +1,256 @@
+"""Python binding of libfp8blk (block-scaled FP8 linear algebra on GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libfp8blk.so`` behind its C ABI (``include/fp8blk.h``). PyTorch
+allocates device memory and supplies the current stream. There is no CPU or
+PyTorch fallback: if the library is missing every call raises.
+
+Names follow the DeepSeek-V3 inference kernels ("Administrator & Developer
+Guide", 8.5 The Triton kernels): act_quant, weight_dequant, fp8_gemm, plus
+the FP8 linear layer of 6.3 and the block weight quantisation of the README's
+weight_scale_inv section.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+__all__ = [
+    "SCALE_FP32", "SCALE_UE8M0", "BLOCK", "lib", "lib_path", "header_functions", "Fp8BlkError",
+    "act_quant", "weight_quant", "weight_dequant", "fp8_gemm", "linear", "linear_host",
+    "gemm_workspace_bytes", "linear_workspace_bytes", "linear_host_workspace_bytes", "last_device_error",
+]
+
+SCALE_FP32 = 0
+SCALE_UE8M0 = 1
+BLOCK = 128
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+HEADER = os.path.join(_ROOT, "include", "fp8blk.h")
+_LIB_PATH = os.path.join(_PKG, "libfp8blk.so")
+_lib = None
+_lib_lock = threading.Lock()
+
+
+class Fp8BlkError(RuntimeError):
+    pass
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def header_functions() -> list[str]:
+    """Names of the functions the public header declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"FP8BLK_API\s+[\w\s\*]*?\b(fp8blk_\w+)\s*\(", text)))
+
+
+def lib():
+    """The loaded libfp8blk (ctypes). Raises if it has not been built."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise Fp8BlkError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                  "or python fp8_block_scaled_quant_gb300/_build.py")
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+            L.fp8blk_status_string.argtypes = [i32]
+            L.fp8blk_status_string.restype = ctypes.c_char_p
+            L.fp8blk_version.argtypes = []
+            L.fp8blk_version.restype = i32
+            L.fp8blk_act_quant.argtypes = [vp, i64, i64, vp, vp, i32, vp]
+            L.fp8blk_weight_quant.argtypes = [vp, i64, i64, vp, vp, i32, vp]
+            L.fp8blk_weight_dequant.argtypes = [vp, vp, i64, i64, vp, vp]
+            L.fp8blk_gemm_workspace_bytes.argtypes = [i64, i64, i64]
+            L.fp8blk_gemm_workspace_bytes.restype = sz
+            L.fp8blk_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
+            L.fp8blk_linear_workspace_bytes.argtypes = [i64, i64, i64]
+            L.fp8blk_linear_workspace_bytes.restype = sz
+            L.fp8blk_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
+            L.fp8blk_linear_host_workspace_bytes.argtypes = [i64, i64, i64]
+            L.fp8blk_linear_host_workspace_bytes.restype = sz
+            L.fp8blk_linear_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
+            L.fp8blk_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+            for name in header_functions():
+                if getattr(L, name).restype is ctypes.c_int:
+                    getattr(L, name).restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = lib().fp8blk_status_string(status).decode()
+        raise Fp8BlkError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str, ndim: int = 2):
+    if not t.is_cuda:
+        raise Fp8BlkError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise Fp8BlkError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise Fp8BlkError(f"{name}: Input tensors must have {ndim} dimensions")
+    if not t.is_contiguous():
+        raise Fp8BlkError(f"{name}: Input tensor must be contiguous")
+
+
+# ---- workspaces: zero-filled device buffers cached per (device, stream) ------
+
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device: torch.device, key: str = "gemm") -> torch.Tensor:
+    """A zero-initialised uint8 device buffer of at least nbytes, reused by
+    every call on the same device, stream and key. The GEMM leaves its
+    counters at zero, so the buffer never needs clearing again."""
+    stream = torch.cuda.current_stream(device).cuda_stream
+    k = (device.index, stream, key)
+    buf = _ws_cache.get(k)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 256) + 256, dtype=torch.uint8, device=device)
+        _ws_cache[k] = buf
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + max(nbytes, 1)]
+
+
+# ---- operations --------------------------------------------------------------
+
+def act_quant(x: torch.Tensor, scale_fmt: int = SCALE_FP32, q: torch.Tensor | None = None,
+              s: torch.Tensor | None = None):
+    """x bf16 [M, K] -> (q float8_e4m3fn [M, K], s float32 [M, K/128])."""
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    if K % BLOCK:
+        raise Fp8BlkError(f"Last dimension size must be divisible by block_size (block_size={BLOCK})")
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=x.device)
+    if s is None:
+        s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=x.device)
+    _check(lib().fp8blk_act_quant(_ptr(x), M, K, _ptr(q), _ptr(s), scale_fmt, _stream(x.device)), "act_quant")
+    return q, s
+
+
+def weight_quant(w: torch.Tensor, scale_fmt: int = SCALE_FP32):
+    """w float32 [N, K] -> (q float8_e4m3fn [N, K], s float32 [ceil(N/128), ceil(K/128)])."""
+    _need(w, torch.float32, "w")
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.float8_e4m3fn, device=w.device)
+    s = torch.empty(((N + BLOCK - 1) // BLOCK, (K + BLOCK - 1) // BLOCK), dtype=torch.float32, device=w.device)
+    _check(lib().fp8blk_weight_quant(_ptr(w), N, K, _ptr(q), _ptr(s), scale_fmt, _stream(w.device)),
+           "weight_quant")
+    return q, s
+
+
+def weight_dequant(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """q float8_e4m3fn [N, K], s float32 [ceil(N/128), ceil(K/128)] -> bf16 [N, K]."""
+    _need(q, torch.float8_e4m3fn, "q")
+    _need(s, torch.float32, "s")
+    N, K = q.shape
+    if tuple(s.shape) != ((N + BLOCK - 1) // BLOCK, (K + BLOCK - 1) // BLOCK):
+        raise Fp8BlkError("scale must have shape (ceil(N/128), ceil(K/128))")
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=q.device)
+    _check(lib().fp8blk_weight_dequant(_ptr(q), _ptr(s), N, K, _ptr(out), _stream(q.device)), "weight_dequant")
+    return out
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().fp8blk_gemm_workspace_bytes(M, N, K))
+
+
+def linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().fp8blk_linear_workspace_bytes(M, N, K))
+
+
+def linear_host_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().fp8blk_linear_host_workspace_bytes(M, N, K))
+
+
+def fp8_gemm(a: torch.Tensor, a_s: torch.Tensor, w: torch.Tensor, w_s: torch.Tensor,
+             scale_fmt: int = SCALE_FP32, out: torch.Tensor | None = None,
+             ws: torch.Tensor | None = None) -> torch.Tensor:
+    """a e4m3 [M, K], a_s fp32 [M, K/128], w e4m3 [N, K], w_s fp32 [ceil(N/128), K/128] -> bf16 [M, N]."""
+    _need(a, torch.float8_e4m3fn, "a")
+    _need(w, torch.float8_e4m3fn, "w")
+    _need(a_s, torch.float32, "a_s")
+    _need(w_s, torch.float32, "w_s")
+    M, K = a.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise Fp8BlkError("a and w must share K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    nbytes = gemm_workspace_bytes(M, N, K)
+    if ws is None:
+        ws = workspace(nbytes, a.device)
+    _check(lib().fp8blk_gemm(_ptr(a), _ptr(a_s), _ptr(w), _ptr(w_s), _ptr(out), M, N, K, scale_fmt, _ptr(ws),
+                             ws.numel(), _stream(a.device)), "fp8_gemm")
+    return out
+
+
+def linear(x: torch.Tensor, w: torch.Tensor, w_s: torch.Tensor, scale_fmt: int = SCALE_FP32,
+           out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """FP8 linear layer: fp8_gemm(act_quant(x), w). x bf16 [M, K] -> bf16 [M, N]."""
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.float8_e4m3fn, "w")
+    _need(w_s, torch.float32, "w_s")
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(linear_workspace_bytes(M, N, K), x.device, "linear")
+    _check(lib().fp8blk_linear(_ptr(x), _ptr(w), _ptr(w_s), _ptr(out), M, N, K, scale_fmt, _ptr(ws), ws.numel(),
+                               _stream(x.device)), "linear")
+    return out
+
+
+def linear_host(x_host: torch.Tensor, w: torch.Tensor, w_s: torch.Tensor, y_host: torch.Tensor,
+                scale_fmt: int = SCALE_FP32, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """The FP8 linear layer on host (preferably pinned) bf16 buffers: enqueues the
+    copy in, the layer, and the copy out on the current stream of w's device.
+    y_host is valid after that stream is synchronised."""
+    if x_host.is_cuda or y_host.is_cuda:
+        raise Fp8BlkError("x_host and y_host must be host tensors")
+    if x_host.dtype != torch.bfloat16 or y_host.dtype != torch.bfloat16:
+        raise Fp8BlkError("x_host and y_host must be bf16")
+    if not (x_host.is_contiguous() and y_host.is_contiguous()):
+        raise Fp8BlkError("Input tensor must be contiguous")
+    _need(w, torch.float8_e4m3fn, "w")
+    M, K = x_host.shape
+    N = w.shape[0]
+    if tuple(y_host.shape) != (M, N):
+        raise Fp8BlkError("y_host must be [M, N]")
+    if ws is None:
+        ws = workspace(linear_host_workspace_bytes(M, N, K), w.device, "linear_host")
+    _check(lib().fp8blk_linear_host(_ptr(x_host), _ptr(w), _ptr(w_s), _ptr(y_host), M, N, K, scale_fmt, _ptr(ws),
+                                    ws.numel(), _stream(w.device)), "linear_host")
+    return y_host
+
+
+def last_device_error(device: torch.device | None = None) -> int:
+    """Synchronises the current stream and returns (and clears) the device
+    error bits: 0 when no kernel gave up waiting."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    bits = ctypes.c_uint(0)
+    st = lib().fp8blk_last_device_error(_stream(device), ctypes.byref(bits))
+    if st not in (0, 6):
+        _check(st, "last_device_error")
+    return int(bits.value)

@@ -1,0 +1,157 @@
+// Library-wide entry points: device checks, the device error word, status
+// names, and the FP8 linear layer ("Administrator & Developer Guide", 6.3:
+// with gemm_impl "fp8", linear() quantises its input with act_quant and calls
+// fp8_gemm) on device and on host buffers.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fp8blk.h"
+#include "host.cuh"
+
+namespace fp8blk {
+
+// Error word written by kernels that gave up waiting (one per device context).
+__device__ unsigned g_device_error_word;
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
+             int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DevInfo g_info[kMaxDevices];
+int g_status[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+void init_device(int dev) {
+  DevInfo& d = g_info[dev];
+  d.device = dev;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+    g_status[dev] = FP8BLK_ERR_CUDA;
+    return;
+  }
+  d.sm_count = prop.multiProcessorCount;
+  d.cc_major = prop.major;
+  d.cc_minor = prop.minor;
+  d.smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+  if (prop.major != 10 || prop.minor != 3) {
+    g_status[dev] = FP8BLK_ERR_ARCH;
+    return;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) {
+    g_status[dev] = FP8BLK_ERR_CUDA;
+    return;
+  }
+  d.err_word = static_cast<unsigned*>(p);
+  g_status[dev] = FP8BLK_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
+
+}  // namespace
+
+int current_device(const DevInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP8BLK_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FP8BLK_ERR_CUDA;
+  std::call_once(g_once[dev], init_device, dev);
+  *out = &g_info[dev];
+  return g_status[dev];
+}
+
+}  // namespace fp8blk
+
+using namespace fp8blk;
+
+extern "C" const char* fp8blk_status_string(int status) {
+  switch (status) {
+    case FP8BLK_OK: return "ok";
+    case FP8BLK_ERR_NULL: return "null pointer";
+    case FP8BLK_ERR_SHAPE: return "invalid shape (K must be a multiple of 128 where required)";
+    case FP8BLK_ERR_ALIGN: return "misaligned pointer";
+    case FP8BLK_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8BLK_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case FP8BLK_ERR_TIMEOUT: return "a kernel gave up waiting";
+    case FP8BLK_ERR_CUDA: return "CUDA runtime error";
+    case FP8BLK_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int fp8blk_version(void) { return 100; }
+
+extern "C" int fp8blk_last_device_error(fp8blk_stream_t stream, unsigned* bits) {
+  if (!bits) return FP8BLK_ERR_NULL;
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BLK_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, d->err_word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8BLK_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(d->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FP8BLK_ERR_CUDA;
+  }
+  *bits = v;
+  return v ? FP8BLK_ERR_TIMEOUT : FP8BLK_OK;
+}
+
+// Workspace of the linear layer: [x_q e4m3 M*K][x_s fp32 M*K/128][GEMM workspace],
+// each part 256-byte aligned.
+extern "C" size_t fp8blk_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  return align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / kBlock) * 4) +
+         gemm_workspace_bytes(M, N, K);
+}
+
+extern "C" int fp8blk_linear(const void* x_bf16, const void* w_e4m3, const float* w_s, void* y_bf16, int64_t M,
+                             int64_t N, int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes,
+                             fp8blk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8BLK_OK;
+  if (!workspace) return FP8BLK_ERR_WORKSPACE;
+  if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
+  const size_t need = fp8blk_linear_workspace_bytes(M, N, K);
+  if (workspace_bytes < need) return FP8BLK_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* xq = ws;
+  float* xs = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(M) * K));
+  uint8_t* gws = ws + align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / kBlock) * 4);
+  if (int st = fp8blk_act_quant(x_bf16, M, K, xq, xs, scale_fmt, stream)) return st;
+  return gemm_run(xq, xs, w_e4m3, w_s, y_bf16, M, N, K, scale_fmt, gws, workspace_bytes - (gws - ws),
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Host variant: [x bf16 M*K][y bf16 M*N][linear workspace].
+extern "C" size_t fp8blk_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * N * 2) +
+         fp8blk_linear_workspace_bytes(M, N, K);
+}
+
+extern "C" int fp8blk_linear_host(const void* x_host, const void* w_e4m3, const float* w_s, void* y_host,
+                                  int64_t M, int64_t N, int64_t K, int scale_fmt, void* workspace,
+                                  size_t workspace_bytes, fp8blk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
+  if (M == 0 || N == 0) return FP8BLK_OK;
+  if (!x_host || !y_host) return FP8BLK_ERR_NULL;
+  if (!workspace) return FP8BLK_ERR_WORKSPACE;
+  if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
+  if (workspace_bytes < fp8blk_linear_host_workspace_bytes(M, N, K)) return FP8BLK_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
+  uint8_t* xd = ws;
+  uint8_t* yd = ws + align256(xb);
+  uint8_t* lws = yd + align256(yb);
+  if (K > 0 && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
+  if (int st = fp8blk_linear(xd, w_e4m3, w_s, yd, M, N, K, scale_fmt, lws, workspace_bytes - (lws - ws), stream))
+    return st;
+  if (cudaMemcpyAsync(y_host, yd, yb, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
+  return FP8BLK_OK;
+}

@@ -1,0 +1,171 @@
+/*
+ * fp8blk -- block-scaled FP8 linear algebra for one NVIDIA GB300 (sm_103a).
+ *
+ * The operations are those of the DeepSeek-V3 inference kernels as the
+ * project's documentation pages describe them:
+ *   - act_quant: "Administrator & Developer Guide", 8.5.1 act_quant_kernel;
+ *   - weight_dequant: same guide, 8.5.2 weight_dequant_kernel, and the README
+ *     ("Algolia docsearch" page) section 3, weight_scale_inv and zero padding;
+ *   - fp8_gemm: same guide, 8.5.3 fp8_gemm_kernel, and 6.3 The FP8 path;
+ *   - the routed-expert FFN: same guide, 6.4 MoE expert routing and 8.4.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device pointers unless a name ends in _host. The caller
+ *     owns all memory; the library never allocates or frees. Scratch memory
+ *     is passed in as `workspace`.
+ *   - Matrices are dense and row-major: the last dimension is contiguous
+ *     (the pages' kernels assert contiguous 2-D tensors).
+ *   - bf16 is IEEE bfloat16 (uint16 storage); e4m3 is float8_e4m3fn (one
+ *     byte: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest
+ *     magnitude 448, codes 0x7F/0xFF NaN).
+ *   - Block size is 128: activation scales are one fp32 per (row, 128
+ *     columns), weight scales one fp32 per 128x128 block.
+ *   - scale_fmt is FP8BLK_SCALE_FP32 (0) or FP8BLK_SCALE_UE8M0 (1, scales
+ *     rounded up to a power of two and still stored as fp32).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; 0 = the legacy
+ *     default stream). Arguments are checked on the host before any launch;
+ *     a failed check launches nothing and returns a non-zero status.
+ *   - Sizes of 0 are valid and launch nothing (except where noted).
+ *   - Not thread-safe per workspace: calls that share a workspace must be
+ *     ordered on one stream.
+ */
+#ifndef FP8BLK_H
+#define FP8BLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8BLK_API __attribute__((visibility("default")))
+#else
+#define FP8BLK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *fp8blk_stream_t; /* identical to cudaStream_t */
+
+enum fp8blk_scale_fmt { FP8BLK_SCALE_FP32 = 0, FP8BLK_SCALE_UE8M0 = 1 };
+
+enum fp8blk_status {
+  FP8BLK_OK = 0,
+  FP8BLK_ERR_NULL = 1,        /* a required pointer is NULL */
+  FP8BLK_ERR_SHAPE = 2,       /* negative size, K % 128 != 0 where required, size limits */
+  FP8BLK_ERR_ALIGN = 3,       /* a pointer is not aligned as documented */
+  FP8BLK_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  FP8BLK_ERR_ARCH = 5,        /* the current device is not sm_103 */
+  FP8BLK_ERR_TIMEOUT = 6,     /* a kernel gave up waiting (see fp8blk_last_device_error) */
+  FP8BLK_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+  FP8BLK_ERR_ARG = 8          /* an enum argument is out of range */
+};
+
+/* Human-readable name of a status code (static string). */
+FP8BLK_API const char *fp8blk_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+FP8BLK_API int fp8blk_version(void);
+
+/*
+ * act_quant ("Administrator & Developer Guide", 8.5.1): for each row m and
+ * 128-column block b of x,
+ *     amax = max |x[m, b*128 + i]|                        (fp32)
+ *     s    = max(amax, 1e-4) / 448                        (fp32 division)
+ *     s    = 2^ceil(log2 s)          if scale_fmt == UE8M0 (exact, rounded up)
+ *     q[m, b*128 + i] = e4m3(x / s)  (fp32 division, round to nearest even,
+ *                                     saturating at +-448, sign of zero kept)
+ * x:  bf16 [M, K], 16-byte aligned.   q: e4m3 [M, K], 16-byte aligned.
+ * s:  fp32 [M, K/128], 4-byte aligned.
+ * K must be a multiple of 128 (FP8BLK_ERR_SHAPE otherwise, the pages' "Last
+ * dimension size must be divisible by block_size").
+ */
+FP8BLK_API int fp8blk_act_quant(const void *x_bf16, int64_t M, int64_t K, void *q_e4m3, float *s, int scale_fmt,
+                     fp8blk_stream_t stream);
+
+/*
+ * Block weight quantisation (README section 3: one fp32 scale per 128x128
+ * block; a block not aligned to 128 is zero-padded to 128 for the scale
+ * calculation and the padding is dropped after quantisation). Each block gets
+ * the act_quant rule above over its real elements:
+ *     s[bn, bk] = max(amax_block, 1e-4) / 448 (UE8M0: rounded up to 2^k),
+ *     q[n, k]   = e4m3(w[n, k] / s[n/128, k/128]).
+ * w: fp32 [N, K]; q: e4m3 [N, K]; s: fp32 [ceil(N/128), ceil(K/128)].
+ * Any N, K >= 0. Pointers 4-byte aligned (w, s), q unaligned allowed.
+ */
+FP8BLK_API int fp8blk_weight_quant(const float *w_f32, int64_t N, int64_t K, void *q_e4m3, float *s, int scale_fmt,
+                        fp8blk_stream_t stream);
+
+/*
+ * weight_dequant ("Administrator & Developer Guide", 8.5.2; README section 3):
+ *     out[n, k] = bf16( fp32(q[n, k]) * s[n/128, k/128] )
+ * one fp32 multiply, one round-to-nearest-even to bf16.
+ * q: e4m3 [N, K]; s: fp32 [ceil(N/128), ceil(K/128)]; out: bf16 [N, K].
+ * Any N, K >= 0; edge blocks are partial. No alignment beyond the element
+ * size is required (16-byte aligned rows take the vector path).
+ */
+FP8BLK_API int fp8blk_weight_dequant(const void *q_e4m3, const float *s, int64_t N, int64_t K, void *out_bf16,
+                          fp8blk_stream_t stream);
+
+/*
+ * fp8_gemm ("Administrator & Developer Guide", 8.5.3 and 6.3):
+ *     C[m, n] = sum over 128-wide K blocks kb of
+ *               a_s[m, kb] * w_s[n/128, kb] * sum_{k in kb} a[m, k] * w[n, k]
+ * accumulated in fp32 (each K block's tensor-core partial is scaled and added
+ * to the fp32 accumulator), stored as bf16 (round to nearest even).
+ * a:   e4m3 [M, K] (activations, quantised by fp8blk_act_quant), 16-byte aligned.
+ * a_s: fp32 [M, K/128].
+ * w:   e4m3 [N, K] (weights), 16-byte aligned.
+ * w_s: fp32 [ceil(N/128), K/128].
+ * c:   bf16 [M, N]. 16-byte alignment and N % 8 == 0 take the vector store path.
+ * K must be a multiple of 128; N need not be (the last weight block is
+ * partial: rows past N contribute nothing). K == 0 writes zeros.
+ * scale_fmt only states the scale format (both formats use the same math).
+ * workspace: device memory of at least fp8blk_gemm_workspace_bytes(M, N, K),
+ * 256-byte aligned, ZERO-FILLED before its first use; every call returns it
+ * to that state (its tile counters end at zero). One workspace serves one
+ * stream at a time.
+ */
+FP8BLK_API size_t fp8blk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+FP8BLK_API int fp8blk_gemm(const void *a_e4m3, const float *a_s, const void *w_e4m3, const float *w_s, void *c_bf16,
+                int64_t M, int64_t N, int64_t K, int scale_fmt, void *workspace, size_t workspace_bytes,
+                fp8blk_stream_t stream);
+
+/*
+ * FP8 linear layer ("Administrator & Developer Guide", 6.3, the gemm_impl
+ * "fp8" branch of linear()): y = fp8_gemm(act_quant(x), w) with x bf16 [M, K],
+ * w e4m3 [N, K] with scales w_s [ceil(N/128), K/128], y bf16 [M, N].
+ * The quantised activation lives in the workspace:
+ *     fp8blk_linear_workspace_bytes(M, N, K) bytes, 256-byte aligned, zero-filled
+ * before first use (as for fp8blk_gemm).
+ */
+FP8BLK_API size_t fp8blk_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+FP8BLK_API int fp8blk_linear(const void *x_bf16, const void *w_e4m3, const float *w_s, void *y_bf16, int64_t M, int64_t N,
+                  int64_t K, int scale_fmt, void *workspace, size_t workspace_bytes, fp8blk_stream_t stream);
+
+/*
+ * The same layer with the activation and the result in HOST memory: copies
+ * x_host (bf16 [M, K]) to the device workspace, runs fp8blk_linear, and copies
+ * y back to y_host (bf16 [M, N]), all enqueued on `stream`. Host buffers
+ * should be page-locked (cudaHostAlloc / pinned) for the copies to be
+ * asynchronous; y_host is valid once the stream has been synchronised. The
+ * weight stays on the device. Workspace: fp8blk_linear_host_workspace_bytes.
+ */
+FP8BLK_API size_t fp8blk_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
+FP8BLK_API int fp8blk_linear_host(const void *x_host_bf16, const void *w_e4m3, const float *w_s, void *y_host_bf16,
+                       int64_t M, int64_t N, int64_t K, int scale_fmt, void *workspace, size_t workspace_bytes,
+                       fp8blk_stream_t stream);
+
+/*
+ * Debug: synchronises `stream`, then returns and clears the device error
+ * word of the current device (0 when no kernel gave up waiting). A non-zero
+ * value means a kernel hit its wait limit and returned early: its outputs are
+ * undefined and the workspace must be zero-filled again before reuse.
+ */
+FP8BLK_API int fp8blk_last_device_error(fp8blk_stream_t stream, unsigned *device_error_bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BLK_H */

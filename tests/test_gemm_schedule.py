@@ -1,0 +1,113 @@
+"""Host-side check of the GEMM's work schedule (no GPU).
+
+The kernel's per-CTA work walk (data-parallel waves, then stream-K over the
+remaining tiles, fixed by the same integer formulas in the producer, MMA and
+epilogue roles) is mirrored here and checked for every workload shape:
+every (tile, K block) iteration is covered exactly once, every CTA's
+stream-K range is non-empty, the parts of each split tile are numbered
+0..nparts-1 by consecutive CTAs, and the partial slots they use are
+distinct. A mistake here would leave an output tile unwritten or let two
+CTAs race on one slot."""
+import pytest
+
+
+def make_plan(M, N, K, sms):
+    Kb = K // 128
+    if M <= 128:
+        swap = True
+        bn = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+        tl, tc = -(-N // 128), -(-M // bn)
+    else:
+        swap = False
+        bn = 128 if N <= 128 else 256
+        tl, tc = -(-M // 128), -(-N // bn)
+    tiles = tl * tc
+    if tiles >= 2 * sms:
+        grid = sms
+        dp = tiles // sms - 1
+        sk_tiles = tiles - dp * sms
+    else:
+        dp = 0
+        sk_tiles = tiles
+        grid = min(sms, tiles * Kb)
+    return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=grid, dp=dp, sk_tiles=sk_tiles,
+                sk_iters=sk_tiles * Kb, Kb=Kb, tiles=tiles)
+
+
+def units(p, c):
+    G, Kb, S = p["grid"], p["Kb"], p["sk_iters"]
+    for j in range(p["dp"]):
+        yield (c + j * G, 0, Kb, 0, 1)
+    it, it_end = c * S // G, (c + 1) * S // G
+
+    def cta_of(i):
+        return ((i + 1) * G - 1) // S
+
+    while it < it_end:
+        t = it // Kb
+        tb, te = t * Kb, t * Kb + Kb
+        seg = min(te, it_end)
+        first, last = cta_of(tb), cta_of(te - 1)
+        yield (p["dp"] * G + t, it - tb, seg - tb, c - first, last - first + 1)
+        it = seg
+
+
+SHAPES = [
+    (16, 320, 256), (1, 10944, 2048), (8, 10944, 2048), (64, 10944, 2048),
+    (4096, 18432, 7168), (4096, 7168, 18432),
+    (64, 1536, 7168), (64, 576, 7168), (64, 24576, 1536), (64, 32768, 512),
+    (2048, 1536, 7168), (2048, 576, 7168), (2048, 24576, 1536), (2048, 32768, 512),
+    (129, 130, 128), (300, 700, 384), (1, 1, 128), (128, 129, 2048), (33, 4000, 128),
+    (5000, 100, 256),
+]
+
+
+@pytest.mark.parametrize("sms", [152, 148, 7])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_schedule_covers_every_iteration_once(M, N, K, sms):
+    p = make_plan(M, N, K, sms)
+    G, Kb = p["grid"], p["Kb"]
+    assert G >= 1 and p["sk_iters"] >= G or p["sk_iters"] == 0
+    cover = {}
+    slots = {}
+    parts = {}
+    for c in range(G):
+        S = p["sk_iters"]
+        if S:
+            assert (c + 1) * S // G > c * S // G, "empty stream-K range"
+        for tile, kb0, kb1, part, nparts in units(p, c):
+            assert 0 <= tile < p["tiles"] and 0 <= kb0 < kb1 <= Kb
+            for kb in range(kb0, kb1):
+                assert (tile, kb) not in cover
+                cover[(tile, kb)] = c
+            if nparts > 1:
+                assert 0 <= part < nparts
+                slot = 2 * c + (1 if part == 0 else 0)
+                assert slot not in slots, "two partials in one slot"
+                slots[slot] = (tile, part)
+                parts.setdefault(tile, {})[part] = (c, kb0, kb1)
+            else:
+                assert kb0 == 0 and kb1 == Kb
+    assert len(cover) == p["tiles"] * Kb
+    for tile, ps in parts.items():
+        n = len(ps)
+        assert sorted(ps) == list(range(n))
+        cs = [ps[i][0] for i in range(n)]
+        assert cs == list(range(cs[0], cs[0] + n)), "parts come from consecutive CTAs"
+        # the parts tile the K range in order
+        assert ps[0][1] == 0 and ps[n - 1][2] == Kb
+        for i in range(n - 1):
+            assert ps[i][2] == ps[i + 1][1]
+        # the reducer finds each part's slot from (first CTA, part index)
+        for i in range(n):
+            assert slots[2 * (cs[0] + i) + (1 if i == 0 else 0)] == (tile, i)
+
+
+def test_decode_plan_uses_whole_machine():
+    p = make_plan(8, 10944, 2048, 152)
+    assert p["swap"] and p["bn"] == 16 and p["grid"] == 152 and p["dp"] == 0
+
+
+def test_prefill_plan_is_hybrid():
+    p = make_plan(4096, 18432, 7168, 152)
+    assert not p["swap"] and p["bn"] == 256 and p["dp"] == 14 and p["sk_tiles"] == 2304 - 14 * 152

@@ -1,0 +1,199 @@
+"""GPU parity of fp8_gemm (and the FP8 linear layer) against the CPU oracle.
+
+Small and medium shapes compare every output element; the full-size
+workloads compare sampled elements (all edge tiles plus random ones) that the
+oracle computes one by one. The oracle always quantises its inputs itself
+from the same seeded bf16 / fp32 data; the GPU codes are checked bit-exact
+against it on the way."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_quant_gb300 as fb
+import oracle
+import synthetic
+from helpers import assert_gemm_close, bits_to_dev_bf16, dev_to_bits, gemm_tol
+
+pytestmark = pytest.mark.gpu
+
+
+def host_problem(M, N, K, seed, frac=0.0, ue8m0=False):
+    x = synthetic.activations(M, K, seed, outlier_frac=frac)
+    w = synthetic.weights(N, K, seed)
+    xq, xs = oracle.act_quant(x, ue8m0)
+    wq, ws = oracle.weight_quant(w, ue8m0)
+    return x, w, xq, xs, wq, ws
+
+
+def gpu_quantised(x, w, fmt):
+    a, a_s = fb.act_quant(bits_to_dev_bf16(x), fmt)
+    q, s = fb.weight_quant(torch.from_numpy(w).cuda(), fmt)
+    return a, a_s, q, s
+
+
+SHAPES = [
+    (16, 320, 256, 0.0),      # the smallest workload: last weight block 64 rows
+    (1, 10944, 2048, 0.01),   # decode
+    (8, 10944, 2048, 0.01),
+    (64, 10944, 2048, 0.01),
+    (17, 576, 7168, 0.0),     # swapped, BN 32, N not 128-aligned
+    (100, 1536, 512, 0.0),    # swapped, BN 128
+    (128, 260, 384, 0.0),
+    (129, 320, 256, 0.0),     # first non-swapped size, ragged M tail
+    (300, 576, 1024, 0.02),   # N = 576: last block partial, BN 256
+    (257, 128, 2048, 0.0),    # BN 128 path
+    (1000, 1000, 128, 0.0),   # single K block, N % 8 == 0
+    (512, 2304, 1536, 0.0),   # several data-parallel waves
+]
+
+
+@pytest.mark.parametrize("M,N,K,frac", SHAPES)
+def test_gemm_full_compare(M, N, K, frac):
+    x, w, xq, xs, wq, ws = host_problem(M, N, K, 1000 + M + N, frac)
+    a, a_s, q, s = gpu_quantised(x, w, fb.SCALE_FP32)
+    assert np.array_equal(dev_to_bits(a), xq) and np.array_equal(dev_to_bits(q), wq)
+    c = fb.fp8_gemm(a, a_s, q, s)
+    ref = oracle.gemm(xq, xs, wq, ws)
+    assert_gemm_close(dev_to_bits(c), ref, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 1000, 1024), (300, 700, 512)])
+def test_gemm_ue8m0_scales(M, N, K):
+    x, w, xq, xs, wq, ws = host_problem(M, N, K, 77, 0.01, ue8m0=True)
+    a, a_s, q, s = gpu_quantised(x, w, fb.SCALE_UE8M0)
+    assert np.array_equal(dev_to_bits(a), xq) and np.array_equal(dev_to_bits(q), wq)
+    c = fb.fp8_gemm(a, a_s, q, s, scale_fmt=fb.SCALE_UE8M0)
+    assert_gemm_close(dev_to_bits(c), oracle.gemm(xq, xs, wq, ws))
+
+
+def test_gemm_pr1_golden():
+    """The 16x320x256 workload against the stored oracle output (bf16 of the
+    fp64 product), within the GEMM tolerance plus one bf16 step."""
+    import test_oracle_golden as g
+    x = synthetic.activations(16, 256, synthetic.SEED_PR1)
+    w = synthetic.weights(320, 256, synthetic.SEED_PR1)
+    a, a_s, q, s = gpu_quantised(x, w, fb.SCALE_FP32)
+    c = dev_to_bits(fb.fp8_gemm(a, a_s, q, s))
+    want = synthetic.bf16_bits_to_f32(g.load_pr1_out()).astype(np.float64)
+    got = synthetic.bf16_bits_to_f32(c).astype(np.float64)
+    assert np.all(np.abs(got - want) <= gemm_tol(want) + 2.0 ** -8 * np.abs(want))
+
+
+def test_gemm_deterministic_and_workspace_restored():
+    x, w, xq, xs, wq, ws = host_problem(8, 10944, 2048, 5, 0.01)
+    a, a_s, q, s = gpu_quantised(x, w, fb.SCALE_FP32)
+    nbytes = fb.gemm_workspace_bytes(8, 10944, 2048)
+    wsb = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    c1 = fb.fp8_gemm(a, a_s, q, s, ws=wsb)
+    tiles = (10944 + 127) // 128
+    assert torch.count_nonzero(wsb[: tiles * 4]) == 0      # counters back at zero
+    c2 = fb.fp8_gemm(a, a_s, q, s, ws=wsb)
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    assert fb.last_device_error() == 0
+
+
+def test_gemm_edge_cases():
+    L = fb.lib()
+    a = torch.zeros((4, 256), dtype=torch.float8_e4m3fn, device="cuda")
+    a_s = torch.ones((4, 2), device="cuda")
+    w = torch.zeros((8, 256), dtype=torch.float8_e4m3fn, device="cuda")
+    w_s = torch.ones((1, 2), device="cuda")
+    c = torch.full((4, 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    ws = fb.workspace(fb.gemm_workspace_bytes(4, 8, 256), torch.device("cuda"))
+    p = lambda t: t.data_ptr()
+    # K % 128 != 0
+    assert L.fp8blk_gemm(p(a), p(a_s), p(w), p(w_s), p(c), 4, 8, 200, 0, p(ws), ws.numel(), None) == 2
+    # misaligned operand
+    assert L.fp8blk_gemm(p(a) + 8, p(a_s), p(w), p(w_s), p(c), 4, 8, 128, 0, p(ws), ws.numel(), None) == 3
+    # workspace too small
+    assert L.fp8blk_gemm(p(a), p(a_s), p(w), p(w_s), p(c), 4, 8, 256, 0, p(ws), 16, None) == 4
+    # null operand
+    assert L.fp8blk_gemm(None, p(a_s), p(w), p(w_s), p(c), 4, 8, 256, 0, p(ws), ws.numel(), None) == 1
+    # bad scale format
+    assert L.fp8blk_gemm(p(a), p(a_s), p(w), p(w_s), p(c), 4, 8, 256, 5, p(ws), ws.numel(), None) == 8
+    # M == 0 and N == 0 are no-ops
+    assert L.fp8blk_gemm(None, None, None, None, p(c), 0, 8, 256, 0, None, 0, None) == 0
+    assert L.fp8blk_gemm(None, None, None, None, p(c), 4, 0, 256, 0, None, 0, None) == 0
+    # K == 0: an empty sum, zeros
+    assert L.fp8blk_gemm(None, None, None, None, p(c), 4, 8, 0, 0, None, 0, None) == 0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c.float()) == 0
+
+
+def test_gemm_unaligned_output_scalar_stores():
+    """N % 8 != 0 forces the scalar store path (non-swapped and swapped)."""
+    for M, N in ((200, 131), (5, 131)):
+        x, w, xq, xs, wq, ws = host_problem(M, N, 256, 9)
+        a, a_s, q, s = gpu_quantised(x, w, fb.SCALE_FP32)
+        c = fb.fp8_gemm(a, a_s, q, s)
+        assert_gemm_close(dev_to_bits(c), oracle.gemm(xq, xs, wq, ws))
+
+
+# ---- full-size workloads, sampled ------------------------------------------------
+
+def sampled_check(M, N, K, seed, frac=0.0, n_random=48):
+    """Device-generated inputs at full size; the oracle recomputes sampled
+    outputs from host copies of the same bf16 / fp32 inputs (quantising the
+    needed rows and weight blocks itself)."""
+    dev = torch.device("cuda")
+    x = synthetic.device_activations(M, K, seed, dev, outlier_frac=frac)
+    w = synthetic.device_normal((N, K), seed + 1, 0.02, dev)
+    a, a_s = fb.act_quant(x)
+    q, s = fb.weight_quant(w)
+    c = fb.fp8_gemm(a, a_s, q, s)
+    g = np.random.Generator(np.random.PCG64(seed))
+    ms = np.concatenate([[0, M - 1, min(127, M - 1), min(128, M - 1)], g.integers(0, M, n_random)])
+    ns = np.concatenate([[0, N - 1, min(127, N - 1), min(255, N - 1)], g.integers(0, N, n_random)])
+    ms, ns = np.meshgrid(np.unique(ms), np.unique(ns), indexing="ij")
+    ms, ns = ms.ravel(), ns.ravel()
+    rows = np.unique(ms)
+    xb = dev_to_bits(x[torch.from_numpy(rows).to(dev)])
+    xq, xs = oracle.act_quant(xb)
+    assert np.array_equal(dev_to_bits(a[torch.from_numpy(rows).to(dev)]), xq)
+    blocks = np.unique(ns // 128)
+    wq_parts, ws_parts = [], []
+    for b in blocks:
+        qo, so = oracle.weight_quant(w[b * 128:(b + 1) * 128].cpu().numpy())
+        assert np.array_equal(dev_to_bits(q[b * 128:(b + 1) * 128]), qo)
+        wq_parts.append(np.pad(qo, ((0, 128 - qo.shape[0]), (0, 0))))
+        ws_parts.append(so)
+    wq = np.concatenate(wq_parts)
+    wsc = np.concatenate(ws_parts)
+    row_of = {r: i for i, r in enumerate(rows)}
+    blk_of = {b: i for i, b in enumerate(blocks)}
+    mi = np.array([row_of[m] for m in ms])
+    ni = np.array([blk_of[n // 128] * 128 + n % 128 for n in ns])
+    ref = oracle.gemm_points(xq, xs, wq, wsc, mi, ni)
+    got = dev_to_bits(c)[ms, ns]
+    # rms of the whole output, from the GPU result (only sets the absolute floor)
+    rms = float(c.float().pow(2).mean().sqrt())
+    assert_gemm_close(got, ref, rms=rms, what=f"sampled {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 18432, 7168), (4096, 7168, 18432), (2048, 1536, 7168),
+                                   (2048, 576, 7168), (2048, 24576, 1536), (2048, 32768, 512),
+                                   (64, 24576, 1536), (64, 32768, 512), (64, 576, 7168)])
+def test_gemm_full_size_sampled(M, N, K):
+    sampled_check(M, N, K, 4000 + M % 97 + N % 89, frac=0.01)
+
+
+def test_linear_matches_quant_then_gemm():
+    x, w, xq, xs, wq, ws = host_problem(8, 10944, 2048, 21, 0.01)
+    xd = bits_to_dev_bf16(x)
+    q, s = fb.weight_quant(torch.from_numpy(w).cuda())
+    y = fb.linear(xd, q, s)
+    a, a_s = fb.act_quant(xd)
+    c = fb.fp8_gemm(a, a_s, q, s)
+    assert torch.equal(y.view(torch.int16), c.view(torch.int16))
+    assert_gemm_close(dev_to_bits(y), oracle.gemm(xq, xs, wq, ws))
+
+
+def test_linear_host_buffers():
+    x, w, xq, xs, wq, ws = host_problem(8, 10944, 2048, 22, 0.01)
+    q, s = fb.weight_quant(torch.from_numpy(w).cuda())
+    xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((8, 10944), dtype=torch.bfloat16).pin_memory()
+    fb.linear_host(xh, q, s, yh)
+    torch.cuda.current_stream().synchronize()
+    y = fb.linear(bits_to_dev_bf16(x), q, s)
+    assert torch.equal(yh.view(torch.int16), y.cpu().view(torch.int16))
