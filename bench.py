@@ -1,0 +1,593 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled FP8 hot path on one GB300 (or N replicas).
+
+Default workload: the decode-shaped FP8 linear layer, X bf16 [8, 2048] ~ N(0, 1)
+with 1% outlier channels x20, W e4m3 [10944, 2048] from N(0, 0.02) with
+per-128x128 fp32 scales. One step = act_quant(X) then fp8_gemm (the
+"Administrator & Developer Guide" 6.3 fp8 path of linear()), on inputs
+resident in HBM. The metric is HBM throughput in GB/s of algorithmic bytes
+(decode is HBM-bound); the GEMM-shaped workloads report TFLOP/s.
+
+Timing: steps are captured in CUDA graphs (chunks of up to 100 steps) and the
+timed region is the replay of exactly --steps steps between CUDA events on the
+launching stream, with a device synchronise and a barrier on both sides. The
+weights rotate over enough copies to exceed 3x the L2 size, so no step finds
+its weight in L2. nvidia-smi samples clocks during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With --impl reference the CPU oracle is timed on the host cores on a bounded
+sample of the same workload (there is no GPU reference implementation to run:
+the pages hold no code).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+# name -> (kind, shape dict). Shapes from the workload list: decode-shaped
+# linear (M in 1, 8, 64), the 16x320x256 case, the prefill FFN GEMMs, the
+# attention projections, weight_dequant of an [18432, 7168] weight.
+WORKLOADS = {
+    "decode_linear_m8": ("linear", dict(M=8, N=10944, K=2048, frac=0.01, seed=synthetic.SEED_DECODE)),
+    "decode_linear_m1": ("linear", dict(M=1, N=10944, K=2048, frac=0.01, seed=synthetic.SEED_DECODE)),
+    "decode_linear_m64": ("linear", dict(M=64, N=10944, K=2048, frac=0.01, seed=synthetic.SEED_DECODE)),
+    "pr1_linear_16x320x256": ("linear", dict(M=16, N=320, K=256, frac=0.0, seed=synthetic.SEED_PR1)),
+    "prefill_gemm_w1": ("linear", dict(M=4096, N=18432, K=7168, frac=0.0, seed=synthetic.SEED_PREFILL)),
+    "prefill_gemm_w2": ("linear", dict(M=4096, N=7168, K=18432, frac=0.0, seed=synthetic.SEED_PREFILL)),
+    "attn_wq_b_m2048": ("linear", dict(M=2048, N=24576, K=1536, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "attn_wkv_b_m2048": ("linear", dict(M=2048, N=32768, K=512, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "attn_wq_a_m2048": ("linear", dict(M=2048, N=1536, K=7168, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "attn_wkv_a_m2048": ("linear", dict(M=2048, N=576, K=7168, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "attn_wq_b_m64": ("linear", dict(M=64, N=24576, K=1536, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "attn_wkv_b_m64": ("linear", dict(M=64, N=32768, K=512, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "weight_dequant_18432x7168": ("dequant", dict(N=18432, K=7168, seed=synthetic.SEED_ATTN)),
+}
+DEFAULT = "decode_linear_m8"
+FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step from the host instead of replaying CUDA graphs (for profilers)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def linear_bytes(M, N, K):
+    """Bytes one FP8 linear step must move: act_quant (read x bf16, write q and
+    scales) and fp8_gemm (read q, scales, the weight and its scales, write C)."""
+    kb = K // 128
+    nb = -(-N // 128)
+    aq = M * K * 2 + M * K + M * kb * 4
+    gemm = M * K + M * kb * 4 + N * K + nb * kb * 4 + M * N * 2
+    return aq, gemm
+
+
+def linear_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def dequant_bytes(N, K):
+    return N * K + (-(-N // 128)) * (-(-K // 128)) * 4 + N * K * 2
+
+
+# ---------------------------------------------------------------------------
+# environment: peaks, clocks, ranks
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", f"-lms={period_ms}"]
+        self.lines = []
+        self.proc = None
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        rows = [ln for (t, ln) in self.lines if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+        if not rows:
+            rows = [ln for (_, ln) in self.lines]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in rows:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_over_ranks(elapsed_s: float, units: float, device=None):
+    """(max elapsed over ranks, sum of units over ranks). With one process it
+    returns its arguments; under torch.distributed it all-reduces."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# traffic figures recorded from ncu (profiles/), valid only for unchanged sources
+# ---------------------------------------------------------------------------
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_block_scaled_quant_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """dram bytes per launch recorded in profiles/*.md by an ncu capture of this
+    workload, if the kernel sources are unchanged since (else None)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    digest = kernel_source_digest()
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            text = f.read()
+        for m in re.finditer(r"^traffic: workload=(\S+) kernel=(\S+) bytes_per_launch=(\d+) sources=(\w+)",
+                             text, re.M):
+            if m.group(1) == workload and m.group(2) == kernel and m.group(4) == digest:
+                return int(m.group(3))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def graph_chunks(fn_step, n_steps, chunk, torch):
+    """CUDA graphs that run fn_step(i) for i in [0, n_steps), up to `chunk` per graph."""
+    graphs = []
+    i = 0
+    while i < n_steps:
+        n = min(chunk, n_steps - i)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(i, i + n):
+                fn_step(j)
+        graphs.append(g)
+        i += n
+    return graphs
+
+
+class Eager:
+    """Stands in for a captured graph: replay() runs the steps from the host."""
+
+    def __init__(self, fn_step, begin, n):
+        self.fn, self.begin, self.n = fn_step, begin, n
+
+    def replay(self):
+        for j in range(self.begin, self.begin + self.n):
+            self.fn(j)
+
+
+def make_runs(fn_step, n_steps, chunk, torch, eager):
+    if eager:
+        return [Eager(fn_step, i, min(chunk, n_steps - i)) for i in range(0, n_steps, chunk)]
+    return graph_chunks(fn_step, n_steps, chunk, torch)
+
+
+def timed_replay(graphs, stream, torch):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.time()
+    start.record(stream)
+    for g in graphs:
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    return start.elapsed_time(end) / 1e3, t0, t1
+
+
+def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
+    M, N, K, frac, seed = shape["M"], shape["N"], shape["K"], shape["frac"], shape["seed"]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
+    w_bytes = N * K
+    R = max(2, math.ceil(3 * l2 / w_bytes))
+    R = min(R, 64)
+    w = synthetic.device_normal((N, K), seed + 1, 0.02, dev)
+    q0, s0 = fb.weight_quant(w)
+    del w
+    qs = [q0] + [q0.clone() for _ in range(R - 1)]
+    ss = [s0] + [s0.clone() for _ in range(R - 1)]
+    xs = [synthetic.device_activations(M, K, seed + i, dev, outlier_frac=frac) for i in range(R)]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    aqs = [fb.act_quant(x) for x in xs]   # for the GEMM-only pass
+    ws = fb.workspace(fb.linear_workspace_bytes(M, N, K), dev, "bench")
+    gws = fb.workspace(fb.gemm_workspace_bytes(M, N, K), dev, "bench_gemm")
+    aq_buf = [(torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev),
+               torch.empty((M, K // 128), dtype=torch.float32, device=dev)) for _ in range(R)]
+
+    def step(i):
+        r = i % R
+        fb.linear(xs[r], qs[r], ss[r], out=ys[r], ws=ws)
+
+    def gemm_only(i):
+        r = i % R
+        fb.fp8_gemm(aqs[r][0], aqs[r][1], qs[r], ss[r], out=ys[r], ws=gws)
+
+    def aq_only(i):
+        r = i % R
+        fb.act_quant(xs[r], q=aq_buf[r][0], s=aq_buf[r][1])
+
+    for i in range(3):   # eager warm-up: sets kernel attributes, loads modules
+        step(i)
+        gemm_only(i)
+        aq_only(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    chunk = 100
+    g_warm = make_runs(step, warmup, chunk, torch, args.eager)
+    g_main = make_runs(step, steps, chunk, torch, args.eager)
+    g_gemm = make_runs(gemm_only, steps, chunk, torch, args.eager)
+    g_aq = make_runs(aq_only, steps, chunk, torch, args.eager)
+    for g in g_warm:
+        g.replay()
+    torch.cuda.synchronize()
+
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        el, t0, t1 = timed_replay(g_main, stream, torch)
+        el_gemm, _, _ = timed_replay(g_gemm, stream, torch)
+        el_aq, _, _ = timed_replay(g_aq, stream, torch)
+    clocks = clk.summary(t0, t1)
+    assert fb.last_device_error(dev) == 0, "a kernel reported a wait timeout"
+
+    aq_b, gemm_b = linear_bytes(M, N, K)
+    step_bytes = aq_b + gemm_b
+    flops = linear_flops(M, N, K)
+    el_max, units = reduce_over_ranks(el, steps * step_bytes, dev)
+    hbm_bound = flops / (aq_b + gemm_b) < 400
+    gemm_s = el_gemm / steps
+    if hbm_bound:
+        metric_val = units / el_max / 1e9
+        unit = "GB/s"
+        achieved = gemm_b / gemm_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm"], "peak_source": f"hbm_gbs ({peaks['src']})"}
+    else:
+        metric_val = steps * flops * world / el_max / 1e12
+        unit = "TFLOP/s"
+        peak = peaks["bf16"] * FP8_OVER_BF16
+        achieved = flops / gemm_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"bf16_tflops ({peaks['src']}) x {FP8_OVER_BF16} nominal fp8/bf16 ratio"}
+    roof["traffic"] = recorded_traffic(args.workload, "fp8_gemm")
+    roof["algorithmic_bytes_per_launch"] = gemm_b
+    roof["kernel_us"] = gemm_s * 1e6
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(shape, dev, torch, fb, qs[0], ss[0], min(steps, 20000), hbm_bound, step_bytes, flops)
+
+    out = {
+        "value": metric_val, "unit": unit, "ms_per_step": el_max / steps * 1e3,
+        "clocks": clocks, "roofline": roof, "e2e": e2e,
+        "gpu_launches": 2 * steps,
+        "kernels_us": {"act_quant": el_aq / steps * 1e6, "fp8_gemm": gemm_s * 1e6},
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "outlier_channels": frac,
+                   "x": "bf16 N(0,1)", "w": "e4m3 from N(0,0.02), fp32 128x128 block scales",
+                   "l2": f"weights rotate over {R} copies ({R * w_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
+                   "launch": "host loop" if args.eager else f"CUDA graphs of {chunk} steps"},
+        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
+    }
+    return out
+
+
+def run_e2e(shape, dev, torch, fb, q, s, n, hbm_bound, step_bytes, flops):
+    """End to end through fp8blk_linear_host: each step copies X from pinned
+    host memory, runs the layer, and copies Y back; timed on the stream."""
+    M, N, K = shape["M"], shape["N"], shape["K"]
+    xh = [synthetic.device_activations(M, K, shape["seed"] + 7 + i, dev, shape["frac"]).cpu().pin_memory()
+          for i in range(4)]
+    yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+    ws = fb.workspace(fb.linear_host_workspace_bytes(M, N, K), dev, "bench_e2e")
+    for i in range(3):
+        fb.linear_host(xh[i % 4], q, s, yh[i % 4], ws=ws)
+    stream = torch.cuda.current_stream(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(n):
+        fb.linear_host(xh[i % 4], q, s, yh[i % 4], ws=ws)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.time() - t0
+    el = max(start.elapsed_time(end) / 1e3, wall)
+    el, units = reduce_over_ranks(el, n * (step_bytes if hbm_bound else flops), dev)
+    val = units / el / (1e9 if hbm_bound else 1e12)
+    return {"value": val, "unit": "GB/s" if hbm_bound else "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
+            "d2h_bytes_per_step": M * N * 2, "steps": n, "ms_per_step": el / n * 1e3,
+            "api": "fp8blk_linear_host (pinned host buffers)"}
+
+
+def run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
+    N, K, seed = shape["N"], shape["K"], shape["seed"]
+    w = synthetic.device_normal((N, K), seed, 0.02, dev)
+    q, s = fb.weight_quant(w)
+    del w
+    outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    qs = [q, q.clone()]
+
+    def step(i):
+        fb.weight_dequant(qs[i % 2], s, out=outs[i % 2])
+
+    for i in range(3):
+        step(i)
+    stream = torch.cuda.current_stream(dev)
+    g_warm = make_runs(step, warmup, 20, torch, args.eager)
+    g_main = make_runs(step, steps, 20, torch, args.eager)
+    for g in g_warm:
+        g.replay()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        el, t0, t1 = timed_replay(g_main, stream, torch)
+    b = dequant_bytes(N, K)
+    el_max, units = reduce_over_ranks(el, steps * b, dev)
+    achieved = b / (el / steps) / 1e9
+    return {
+        "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
+        "clocks": clk.summary(t0, t1), "gpu_launches": steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm"], "traffic": recorded_traffic(args.workload, "weight_dequant"),
+                     "peak_source": f"hbm_gbs ({peaks['src']})", "algorithmic_bytes_per_launch": b},
+        "e2e": None,
+        "config": {"workload": args.workload, "N": N, "K": K,
+                   "l2": "two alternating inputs/outputs of 396 MB each (> L2)"},
+        "dtype": "e4m3 -> f32 multiply -> bf16",
+    }
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+_SAMPLE_CACHE = {}
+
+
+def oracle_linear_sample(shape, n_cols: int):
+    """One oracle step on a sample of the linear workload: act_quant of all
+    of X and the fp64 GEMM for n_cols weight rows. The sampled weight rows are
+    quantised once, outside the timed part (input preparation). Returns
+    (seconds, algorithmic bytes of the sampled work)."""
+    import oracle
+
+    M, N, K = shape["M"], shape["N"], shape["K"]
+    n_cols = max(1, min(n_cols, N))
+    key = (M, N, K, shape["seed"], n_cols)
+    if key not in _SAMPLE_CACHE:
+        x = synthetic.activations(M, K, shape["seed"], outlier_frac=shape["frac"])
+        w = synthetic.weights(-(-n_cols // 128) * 128, K, shape["seed"] + 1)
+        _SAMPLE_CACHE[key] = (x,) + oracle.weight_quant(w)
+    x, wq, ws = _SAMPLE_CACHE[key]
+    t0 = time.perf_counter()
+    xq, xs = oracle.act_quant(x)
+    oracle.gemm(xq, xs, wq[:n_cols], ws[: -(-n_cols // 128)])
+    dt = time.perf_counter() - t0
+    aq_b, _ = linear_bytes(M, N, K)
+    kb = K // 128
+    b = aq_b + M * K + M * kb * 4 + n_cols * K + (-(-n_cols // 128)) * kb * 4 + M * n_cols * 2
+    return dt, b
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(shape, kind, budget_s=10.0):
+    if kind != "linear":
+        return None
+    M, N, K = shape["M"], shape["N"], shape["K"]
+    # size one sample to about 1-2 s: the oracle runs ~2.5e7 multiply-adds/s
+    n_cols = max(1, min(N, int(2.5e7 * 1.5 / (M * K))))
+    total_t, total_b, reps = 0.0, 0, 0
+    while total_t < budget_s or reps == 0:
+        dt, b = oracle_linear_sample(shape, n_cols)
+        total_t += dt
+        total_b += b
+        reps += 1
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x (act_quant of X[{M},{K}] + fp64 GEMM over {n_cols} of {N} weight rows), "
+                      f"{total_t:.1f} s single-threaded C"}
+
+
+def run_reference(args, kind, shape, steps, warmup):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    if kind != "linear":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle leg covers the linear workloads only"}))
+        return 0
+    # size each step so that warm-up + steps take about a minute in all
+    M, N, K = shape["M"], shape["N"], shape["K"]
+    per_step_s = 60.0 / max(1, steps + warmup)
+    n_cols = max(1, min(N, int(2.5e7 * per_step_s / (M * K))))
+    for _ in range(min(warmup, 3)):
+        oracle_linear_sample(shape, n_cols)
+    tt, tb = 0.0, 0
+    for _ in range(steps):
+        dt, b = oracle_linear_sample(shape, n_cols)
+        tt += dt
+        tb += b
+    val = tb / tt / 1e9
+    line = {
+        "metric": "block-scaled FP8 GEMM TFLOP/s & decode GB/s, % of GB300 roofline, 1 GPU",
+        "value": val, "unit": "GB/s", "impl": "reference", "n_gpus": 1, "steps": steps, "warmup": warmup,
+        "ms_per_step": tt / steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "sample_cols": n_cols},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "kind": "oracle", "cores": 1,
+                         "sample": f"each step: act_quant of X[{M},{K}] + fp64 GEMM over {n_cols} of {N} rows"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    kind, shape = WORKLOADS[args.workload]
+    big = kind == "linear" and shape["M"] >= 2048 or kind == "dequant"
+    steps = args.steps if args.steps is not None else (200 if big else 100000)
+    warmup = args.warmup if args.warmup is not None else (10 if big else 1000)
+    if warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args, kind, shape, steps, warmup)
+
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    import fp8_block_scaled_quant_gb300 as fb
+
+    fb.lib()
+    peaks = load_peaks()
+    if kind == "linear":
+        res = run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
+    else:
+        res = run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(shape, kind)
+    if rank == 0:
+        line = {
+            "metric": "block-scaled FP8 GEMM TFLOP/s & decode GB/s, % of GB300 roofline, 1 GPU",
+            "value": res["value"], "unit": res["unit"], "n_gpus": world, "steps": steps, "warmup": warmup,
+            "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": res["dtype"], "data": "synthetic (seeded; no dataset on the pages)",
+            "config": dict(res["config"], parallelism=f"replicas x{world}"),
+            "clocks": res["clocks"], "roofline": res["roofline"], "e2e": res["e2e"],
+            "gpu_launches": res["gpu_launches"], "cpu_baseline": cpu,
+        }
+        if "kernels_us" in res:
+            line["kernels_us"] = res["kernels_us"]
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
