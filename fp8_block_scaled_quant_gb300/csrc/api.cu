@@ -79,6 +79,8 @@ extern "C" const char* fp8blk_status_string(int status) {
     case FP8BLK_ERR_TIMEOUT: return "a kernel gave up waiting";
     case FP8BLK_ERR_CUDA: return "CUDA runtime error";
     case FP8BLK_ERR_ARG: return "invalid argument";
+    case FP8BLK_ERR_TOO_LARGE:
+      return "problem needs more scratch than the built-in buffer of fp8blk_gemm_noalloc (use fp8blk_gemm)";
     default: return "unknown status";
   }
 }

@@ -612,6 +612,68 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
 
 }  // namespace fp8blk
 
+// ---------------------------------------------------------------------------
+// fp8blk_gemm_noalloc: the GEMM with library-held scratch, for callers that
+// cannot allocate device memory (see include/fp8blk.h). The scratch is a
+// file-scope device array: every GPU that loads the library holds it until
+// the process exits. Host code must not use the array's name as an address;
+// the device address comes from cudaGetSymbolAddress, once per device.
+// ---------------------------------------------------------------------------
+namespace fp8blk {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FP8BLK_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct NoAllocDevice {
+  std::once_flag once;
+  void* ptr;
+  int status;
+};
+NoAllocDevice g_noalloc_dev[64];
+
+// Device address of g_noalloc_scratch on device `dev` (which is current).
+int noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= 64) return FP8BLK_ERR_CUDA;
+  NoAllocDevice& nd = g_noalloc_dev[dev];
+  std::call_once(nd.once, [&nd] {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    nd.ptr = p;
+    nd.status = (e == cudaSuccess && p != nullptr) ? FP8BLK_OK : FP8BLK_ERR_CUDA;
+  });
+  *out = nd.ptr;
+  return nd.status;
+}
+
+// Bytes at the start of a plan's workspace that hold the tile counters.
+size_t plan_counter_bytes(const Plan& pl) {
+  return align256(static_cast<size_t>(pl.tiles_lane) * pl.tiles_col * sizeof(int));
+}
+
+}  // namespace
+}  // namespace fp8blk
+
+extern "C" int fp8blk_gemm_noalloc(const void* a_e4m3, const float* a_s, const void* w_e4m3, const float* w_s,
+                                   void* c_bf16, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                                   fp8blk_stream_t stream) {
+  using namespace fp8blk;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t lim = (int64_t{1} << 31) - 1;
+  if (M > 0 && N > 0 && K > 0 && K % kBlock == 0 && M <= lim && N <= lim && K <= lim) {
+    const DevInfo* d;
+    if (int st = current_device(&d)) return st;
+    const Plan pl = make_plan(M, N, K, d->sm_count);
+    if (plan_workspace(pl) > FP8BLK_NOALLOC_SCRATCH_BYTES) return FP8BLK_ERR_TOO_LARGE;
+    void* scratch = nullptr;
+    if (int st = noalloc_scratch(d->device, &scratch)) return st;
+    if (cudaMemsetAsync(scratch, 0, plan_counter_bytes(pl), cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
+    return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, scratch, FP8BLK_NOALLOC_SCRATCH_BYTES, cs);
+  }
+  // Empty, zero-K and invalid problems need no scratch: same answers as fp8blk_gemm.
+  return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, nullptr, 0, cs);
+}
+
 extern "C" size_t fp8blk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return fp8blk::gemm_workspace_bytes(M, N, K);
 }

@@ -58,7 +58,8 @@ enum fp8blk_status {
   FP8BLK_ERR_ARCH = 5,        /* the current device is not sm_103 */
   FP8BLK_ERR_TIMEOUT = 6,     /* a kernel gave up waiting (see fp8blk_last_device_error) */
   FP8BLK_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
-  FP8BLK_ERR_ARG = 8          /* an enum argument is out of range */
+  FP8BLK_ERR_ARG = 8,         /* an enum argument is out of range */
+  FP8BLK_ERR_TOO_LARGE = 9    /* needs more scratch than fp8blk_gemm_noalloc's built-in buffer */
 };
 
 /* Human-readable name of a status code (static string). */
@@ -155,6 +156,34 @@ FP8BLK_API size_t fp8blk_linear_host_workspace_bytes(int64_t M, int64_t N, int64
 FP8BLK_API int fp8blk_linear_host(const void *x_host_bf16, const void *w_e4m3, const float *w_s, void *y_host_bf16,
                        int64_t M, int64_t N, int64_t K, int scale_fmt, void *workspace, size_t workspace_bytes,
                        fp8blk_stream_t stream);
+
+/*
+ * fp8_gemm with no workspace argument and no device allocation: the same
+ * computation, result and argument rules as fp8blk_gemm, but its scratch
+ * (tile counters and stream-K partial sums) lives in a buffer of
+ * FP8BLK_NOALLOC_SCRATCH_BYTES that the library itself holds in device memory,
+ * on every GPU that loads the library, until the process exits.
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot allocate device memory themselves -- a plugin or custom layer
+ * inside a serving engine that plans all device memory up front and forbids
+ * allocation while it executes, a latency-critical loop that must never
+ * reach cudaMalloc/cudaFree (cudaFree synchronises the device), or a caller
+ * that is handed device pointers but has no allocator of its own.
+ * - Size limit: problems whose scratch need (fp8blk_gemm_workspace_bytes)
+ *   exceeds FP8BLK_NOALLOC_SCRATCH_BYTES return FP8BLK_ERR_TOO_LARGE and
+ *   launch nothing. On a 152-SM GB300 every M <= 32 fits, for any N and K.
+ * - The first call on a device looks up the buffer's device address; make that
+ *   first call before any stream capture begins.
+ * - Every call clears the tile counters in the buffer before its GEMM (a
+ *   memset on `stream`) and allocates nothing.
+ * - All calls on a device share the one buffer: calls that can overlap on the
+ *   GPU (unordered streams) race and corrupt each other's results. Order them
+ *   on one stream, or use fp8blk_gemm with a workspace per stream.
+ */
+#define FP8BLK_NOALLOC_SCRATCH_BYTES (8u << 20)
+FP8BLK_API int fp8blk_gemm_noalloc(const void *a_e4m3, const float *a_s, const void *w_e4m3, const float *w_s,
+                                   void *c_bf16, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                                   fp8blk_stream_t stream);
 
 /*
  * Debug: synchronises `stream`, then returns and clears the device error
