@@ -23,6 +23,7 @@ __all__ = [
     "SCALE_FP32", "SCALE_UE8M0", "BLOCK", "lib", "lib_path", "header_functions", "Fp8BlkError",
     "act_quant", "weight_quant", "weight_dequant", "fp8_gemm", "linear", "linear_host",
     "gemm_workspace_bytes", "linear_workspace_bytes", "linear_host_workspace_bytes", "last_device_error",
+    "swiglu_gemm", "ffn", "moe_permute", "moe_workspace_bytes", "moe_grouped_gemm",
 ]
 
 SCALE_FP32 = 0
@@ -254,3 +255,94 @@ def last_device_error(device: torch.device | None = None) -> int:
     if st not in (0, 6):
         _check(st, "last_device_error")
     return int(bits.value)
+
+
+# ---- SwiGLU FFN and routed experts -------------------------------------------
+
+def _set_types(name, argtypes, restype=ctypes.c_int):
+    f = getattr(lib(), name)
+    f.argtypes = argtypes
+    f.restype = restype
+    return f
+
+
+def swiglu_gemm(x: torch.Tensor, x_s: torch.Tensor, w1: torch.Tensor, w1_s: torch.Tensor, w3: torch.Tensor,
+                w3_s: torch.Tensor, scale_fmt: int = SCALE_FP32, ws: torch.Tensor | None = None):
+    """act_quant(bf16(silu(bf16(x w1^T))) * bf16(x w3^T)) -> (u float8_e4m3fn [M, inter], u_s float32 [M, inter/128])."""
+    for t, n, dt in ((x, "x", torch.float8_e4m3fn), (w1, "w1", torch.float8_e4m3fn), (w3, "w3", torch.float8_e4m3fn),
+                     (x_s, "x_s", torch.float32), (w1_s, "w1_s", torch.float32), (w3_s, "w3_s", torch.float32)):
+        _need(t, dt, n)
+    M, dim = x.shape
+    inter = w1.shape[0]
+    u = torch.empty((M, inter), dtype=torch.float8_e4m3fn, device=x.device)
+    us = torch.empty((M, inter // BLOCK), dtype=torch.float32, device=x.device)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    nb = _set_types("fp8blk_swiglu_workspace_bytes", [i64, i64, i64], sz)(M, inter, dim)
+    if ws is None:
+        ws = workspace(nb, x.device, "swiglu")
+    f = _set_types("fp8blk_swiglu_gemm", [vp] * 8 + [i64, i64, i64, i32, vp, sz, vp])
+    _check(f(_ptr(x), _ptr(x_s), _ptr(w1), _ptr(w1_s), _ptr(w3), _ptr(w3_s), _ptr(u), _ptr(us), M, inter, dim,
+             scale_fmt, _ptr(ws), ws.numel(), _stream(x.device)), "swiglu_gemm")
+    return u, us
+
+
+def ffn(x: torch.Tensor, w1, w1_s, w3, w3_s, w2, w2_s, scale_fmt: int = SCALE_FP32,
+        out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """Dense SwiGLU FFN with FP8 Linears: x bf16 [M, dim] -> bf16 [M, dim]."""
+    _need(x, torch.bfloat16, "x")
+    M, dim = x.shape
+    inter = w1.shape[0]
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    nb = _set_types("fp8blk_ffn_workspace_bytes", [i64, i64, i64], sz)(M, dim, inter)
+    if ws is None:
+        ws = workspace(nb, x.device, "ffn")
+    if out is None:
+        out = torch.empty((M, dim), dtype=torch.bfloat16, device=x.device)
+    f = _set_types("fp8blk_ffn", [vp] * 8 + [i64, i64, i64, i32, vp, sz, vp])
+    _check(f(_ptr(x), _ptr(w1), _ptr(w1_s), _ptr(w3), _ptr(w3_s), _ptr(w2), _ptr(w2_s), _ptr(out), M, dim, inter,
+             scale_fmt, _ptr(ws), ws.numel(), _stream(x.device)), "ffn")
+    return out
+
+
+def moe_permute(topk_idx: torch.Tensor, E: int):
+    """topk_idx int32 [T, topk] -> (counts int32 [E], offsets int32 [E+1], perm int32 [T*topk]);
+    perm past offsets[E] is unspecified."""
+    _need(topk_idx, torch.int32, "topk_idx")
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    f = _set_types("fp8blk_moe_permute", [vp, i64, i64, i64, vp, vp, vp, vp])
+    _check(f(_ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm), _stream(dev)), "moe_permute")
+    return counts, offsets, perm[: T * k]
+
+
+def moe_workspace_bytes(T: int, topk: int, E: int, dim: int, inter: int) -> int:
+    i64 = ctypes.c_int64
+    return int(_set_types("fp8blk_moe_workspace_bytes", [i64] * 5, ctypes.c_size_t)(T, topk, E, dim, inter))
+
+
+def moe_grouped_gemm(x: torch.Tensor, x_s: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                     w1, w1_s, w3, w3_s, w2, w2_s, E: int, scale_fmt: int = SCALE_FP32,
+                     out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """Routed-expert SwiGLU FFN over stacked block-FP8 experts.
+    x e4m3 [T, dim] (+ x_s), topk_idx int32 / topk_w fp32 [T, topk],
+    w1/w3 e4m3 [E*inter, dim], w2 e4m3 [E*dim, inter] (+ block scales) -> bf16 [T, dim]."""
+    _need(x, torch.float8_e4m3fn, "x")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(topk_w, torch.float32, "topk_w")
+    T, dim = x.shape
+    k = topk_idx.shape[1]
+    inter = w2.shape[1]
+    if ws is None:
+        ws = workspace(moe_workspace_bytes(T, k, E, dim, inter), x.device, "moe")
+    if out is None:
+        out = torch.empty((T, dim), dtype=torch.bfloat16, device=x.device)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    f = _set_types("fp8blk_moe_grouped_gemm", [vp] * 11 + [i64] * 5 + [i32, vp, sz, vp])
+    _check(f(_ptr(x), _ptr(x_s), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w1_s), _ptr(w3), _ptr(w3_s),
+             _ptr(w2), _ptr(w2_s), _ptr(out), T, k, E, dim, inter, scale_fmt, _ptr(ws), ws.numel(),
+             _stream(x.device)), "moe_grouped_gemm")
+    return out

@@ -33,6 +33,7 @@
 // frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,20 +45,41 @@
 
 namespace fp8blk {
 
+// Epilogue modes.
+enum : int {
+  kEpiBf16 = 0,     // C[row, col] = bf16(acc)
+  kEpiSwiGLU = 1,   // u = bf16(bf16(silu(bf16(h1))) * bf16(h3)), then act_quant of u -> e4m3 + scale
+  kEpiScatter = 2,  // C[perm[row], col] = bf16(acc)
+};
+
+// Most grouped-GEMM groups (experts) the kernels take.
+constexpr int kMaxGroups = 1024;
+
 struct GemmParams {
-  const float* a_s;    // [M, Kb]
-  const float* w_s;    // [n_wblocks, Kb]
-  __nv_bfloat16* c;    // [M, N]
+  const float* a_s;    // [rows, Kb]
+  const float* w_s;    // [weight blocks, Kb] (w1's scales in SwiGLU mode)
+  const float* w3_s;   // SwiGLU: w3's scales
+  __nv_bfloat16* c;    // bf16 output, row stride ldc
+  uint8_t* uq;         // SwiGLU: e4m3 output, row stride ldc
+  float* us;           // SwiGLU: scales of uq, row stride ldc / 128
+  const int* perm;     // scatter: output row of every input row
+  const int* grp_rows;    // grouped: first row of each group, [E + 1]
+  const int* grp_mtiles;  // grouped: cumulative 128-row tiles of the groups, [E + 1]
   float* slots;        // stream-K partial slots, 2 per CTA, BN * 128 floats each ([col][lane])
   int* counters;       // one arrival counter per tile (zero between calls)
   unsigned* err;       // device error word
-  int M, N, Kb, n_wblocks;
+  int M;               // rows of the activation operand
+  int N;               // output columns (grouped: per group)
+  int Kb, n_wblocks;   // K / 128; weight row blocks (dense)
+  int ldc;             // row stride of the output
+  int E;               // grouped: number of groups; 0 for a dense GEMM
   int tiles_lane, tiles_col;
   int grid;            // CTAs
   int dp_waves;        // tiles [0, dp_waves * grid) run whole, round-robin
   int sk_tiles;        // the remaining tiles run stream-K
   long long sk_iters;  // sk_tiles * Kb
   int vec_store;       // C rows 16-byte aligned and N % 8 == 0
+  int ue8m0;           // SwiGLU: power-of-two scales for the fused act_quant
 };
 
 namespace {
@@ -72,8 +94,10 @@ struct Sched {
   const GemmParams& p;
   int c, j;
   long long it, it_end;
+  int grouped_total;  // grouped GEMM: tile count read on the device (-1: dense)
 
-  __device__ Sched(const GemmParams& prm, int cta) : p(prm), c(cta), j(0) {
+  __device__ Sched(const GemmParams& prm, int cta, int grouped_tiles = -1)
+      : p(prm), c(cta), j(0), grouped_total(grouped_tiles) {
     it = static_cast<long long>(c) * p.sk_iters / p.grid;
     it_end = static_cast<long long>(c + 1) * p.sk_iters / p.grid;
   }
@@ -82,6 +106,17 @@ struct Sched {
   __device__ long long cta_of(long long i) const { return ((i + 1) * p.grid - 1) / p.sk_iters; }
 
   __device__ bool next(Unit& u) {
+    if (grouped_total >= 0) {  // grouped: whole tiles, round-robin
+      const long long t = c + static_cast<long long>(j) * p.grid;
+      if (t >= grouped_total) return false;
+      u.tile = static_cast<int>(t);
+      u.kb0 = 0;
+      u.kb1 = p.Kb;
+      u.part = 0;
+      u.nparts = 1;
+      ++j;
+      return true;
+    }
     if (j < p.dp_waves) {
       u.tile = c + j * p.grid;
       u.kb0 = 0;
@@ -112,13 +147,21 @@ constexpr int pow2_at_least(int v, int floor_) {
   return p;
 }
 
-template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_>
+template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_, int MODE_ = kEpiBf16, bool GROUPED_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr bool SWAP = SWAP_;
   static constexpr int STAGES = STAGES_;
   static constexpr int P = P_;
   static constexpr int EPI_WARPS = EPI_WARPS_;
+  static constexpr int MODE = MODE_;
+  static constexpr bool GROUPED = GROUPED_;
+  // Weight rows one tile covers (SwiGLU: 128 rows of w1 and the same 128 of w3).
+  static constexpr int kWRows = MODE == kEpiSwiGLU ? BN / 2 : BN;
+  // Extra shared memory: grouped tables (row offsets, cumulative tiles) and
+  // the SwiGLU amax exchange between the two column groups (double-buffered).
+  static constexpr int kGroupBytes = GROUPED ? 2 * (kMaxGroups + 4) * 4 : 0;
+  static constexpr int kXchgBytes = MODE == kEpiSwiGLU ? 2 * 2 * 128 * 4 : 0;
   static constexpr int kThreads = (2 + EPI_WARPS) * 32;
   static constexpr int kGroups = EPI_WARPS / 4;  // column groups in the epilogue
   static constexpr int kCpt = BN / kGroups;      // columns per epilogue thread
@@ -127,9 +170,12 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = pow2_at_least(P * BN, 32);
   static constexpr int kBarBytes = (2 * STAGES + 2 * P + 2) * 8 + 16;
-  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + kGroupBytes + kXchgBytes;
 
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+  static_assert(MODE == kEpiBf16 || !SWAP, "SwiGLU and scatter epilogues use activation rows as lanes");
+  static_assert(MODE != kEpiSwiGLU || (BN == 256 && EPI_WARPS == 8), "SwiGLU: w1|w3 128+128 columns");
+  static_assert(!GROUPED || !SWAP, "grouped GEMMs use activation rows as lanes");
   static_assert(EPI_WARPS % 4 == 0, "epilogue warps come in warpgroups");
   static_assert(kCpt == 16 || kCpt % 32 == 0, "TMEM loads of 16 or 32 columns");
   static_assert(SWAP || kCpt == 128, "non-swapped tiles: one weight block per column group");
@@ -138,19 +184,132 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-__device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& tl, int& tc) {
-  tl = tile % p.tiles_lane;
-  tc = tile / p.tiles_lane;
+// Where one output tile lives.
+struct TileInfo {
+  int lane_y;      // TMA row of the lane operand's 128-row tile
+  int col_y;       // TMA row of the column operand's tile (w1/w3 row in SwiGLU mode)
+  int lane_valid;  // lane rows of the tile that exist (activation rows, or weight rows when swapped)
+  int wblock;      // global 128-row weight block of the tile's first weight row
+  int col0;        // first output column (swapped: first token)
+};
+
+// Dense tiles run lane-tile fastest. Grouped tiles run (group, column tile,
+// 128-row tile) with the row tile fastest, so the row tiles of one group that
+// share a weight tile run side by side. rows/mtiles are the group tables in
+// shared memory.
+template <class C>
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, const int* rows, const int* mtiles) {
+  TileInfo t;
+  if constexpr (C::GROUPED) {
+    int lo = 0, hi = p.E - 1;  // last group whose first tile is <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (mtiles[mid] * p.tiles_col <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = lo;
+    const int mt_e = mtiles[e + 1] - mtiles[e];
+    const int local = tile - mtiles[e] * p.tiles_col;
+    const int nt = local / mt_e, mt = local - nt * mt_e;
+    t.lane_y = rows[e] + mt * 128;
+    t.lane_valid = min(128, rows[e + 1] - t.lane_y);
+    t.col_y = e * p.N + nt * C::kWRows;
+    t.wblock = t.col_y / 128;
+    t.col0 = nt * C::kWRows;
+  } else {
+    const int tl = tile % p.tiles_lane, tc = tile / p.tiles_lane;
+    t.lane_y = tl * 128;
+    if constexpr (C::SWAP) {
+      t.lane_valid = min(128, p.N - t.lane_y);
+      t.col_y = tc * C::BN;
+      t.wblock = tl;
+      t.col0 = tc * C::BN;
+    } else {
+      t.lane_valid = min(128, p.M - t.lane_y);
+      t.col_y = tc * C::kWRows;
+      t.wblock = t.col_y / 128;
+      t.col0 = tc * C::kWRows;
+    }
+  }
+  return t;
 }
 
-template <class C>
-__device__ __forceinline__ void store_tile(const GemmParams& p, const float (&acc)[C::kCpt], int tl, int tc, int group,
-                                           int row) {
-  if constexpr (!C::SWAP) {
-    const int m = tl * 128 + row;
-    const int n0 = tc * C::BN + group * 128;
-    if (m >= p.M) return;
-    __nv_bfloat16* crow = p.c + static_cast<size_t>(m) * p.N;
+// Scale of a 128-element block for the fused act_quant (the act_quant rule:
+// max(amax, 1e-4) / 448 as an IEEE division; ue8m0: rounded up to 2^k on the bits).
+__device__ __forceinline__ float quant_block_scale(float amax, bool ue8m0) {
+  float s = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+  if (ue8m0) {
+    uint32_t b = __float_as_uint(s);
+    if (b & 0x007FFFFFu) b = (b & 0x7F800000u) + 0x00800000u;
+    s = __uint_as_float(b);
+  }
+  return s;
+}
+
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+// Writes one thread's finished accumulators: row `row` of the tile, the
+// column group `group`. Returns false if an epilogue-wide wait gave up.
+template <class C, class Sync>
+__device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kCpt], const TileInfo& t, int group,
+                                         int row, float* xchg, uint32_t unit_parity, Sync&& epi_sync) {
+  if constexpr (C::SWAP) {
+    const int n = t.lane_y + row;
+    if (n >= p.N) return true;
+#pragma unroll
+    for (int j = 0; j < C::kCpt; ++j) {
+      const int m = t.col0 + j;
+      if (m < p.M) p.c[static_cast<size_t>(m) * p.ldc + n] = __float2bfloat16_rn(acc[j]);
+    }
+    return true;
+  } else if constexpr (C::MODE == kEpiSwiGLU) {
+    // acc[0, 64): h1 of output columns col0 + 64 group + i; acc[64, 128): h3 of the same columns.
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float h1 = bf16_round(acc[i]);
+      const float h3 = bf16_round(acc[64 + i]);
+      const float g = bf16_round(__fdiv_rn(h1, 1.0f + expf(-h1)));
+      const float u = bf16_round(g * h3);
+      acc[i] = u;
+      amax = fmaxf(amax, fabsf(u));
+    }
+    // The 128-column quantisation block is split over the two column groups:
+    // exchange the half-block maxima through shared memory.
+    float* x = xchg + unit_parity * 256;
+    x[group * 128 + row] = amax;
+    if (!epi_sync()) return false;
+    amax = fmaxf(x[row], x[128 + row]);
+    const float sc = quant_block_scale(amax, p.ue8m0 != 0);
+    if (row < t.lane_valid) {
+      const size_t r = static_cast<size_t>(t.lane_y + row);
+      uint4* dst = reinterpret_cast<uint4*>(p.uq + r * p.ldc + t.col0 + group * 64);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = v * 16 + e * 4;
+          w[e] = pack_e4m3x4(__fdiv_rn(acc[i], sc), __fdiv_rn(acc[i + 1], sc), __fdiv_rn(acc[i + 2], sc),
+                             __fdiv_rn(acc[i + 3], sc));
+        }
+        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      if (group == 0) p.us[r * (p.ldc / 128) + t.col0 / 128] = sc;
+    }
+    return true;
+  } else {
+    if (row >= t.lane_valid) return true;
+    const int r = t.lane_y + row;
+    const size_t out_row = C::MODE == kEpiScatter ? static_cast<size_t>(__ldg(p.perm + r)) : static_cast<size_t>(r);
+    const int n0 = t.col0 + group * 128;
+    __nv_bfloat16* crow = p.c + out_row * p.ldc;
 #pragma unroll
     for (int v = 0; v < C::kCpt / 8; ++v) {
       const int n = n0 + v * 8;
@@ -168,21 +327,14 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const float (&ac
           if (n + e < p.N) crow[n + e] = __float2bfloat16_rn(acc[v * 8 + e]);
       }
     }
-  } else {
-    const int n = tl * 128 + row;
-    if (n >= p.N) return;
-#pragma unroll
-    for (int j = 0; j < C::kCpt; ++j) {
-      const int m = tc * C::BN + j;
-      if (m < p.M) p.c[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(acc[j]);
-    }
+    return true;
   }
 }
 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_lane, const __grid_constant__ CUtensorMap tmap_col,
-                    const GemmParams prm) {
+                    const __grid_constant__ CUtensorMap tmap_col2, const GemmParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::kStageBytes);
@@ -190,10 +342,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + C::P;
   uint64_t* drain = tempty + C::P;
-  uint64_t* epi_bar = drain + 1;  // epilogue-only barrier for the stream-K fixup
+  uint64_t* epi_bar = drain + 1;  // epilogue-only barrier (stream-K fixup, SwiGLU amax exchange)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
+  int* grp_rows = reinterpret_cast<int*>(smem + C::STAGES * C::kStageBytes + C::kBarBytes);
+  int* grp_mtiles = grp_rows + (kMaxGroups + 4);
+  float* xchg = reinterpret_cast<float*>(smem + C::STAGES * C::kStageBytes + C::kBarBytes + C::kGroupBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -216,28 +371,36 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_lane);
     tma_prefetch_desc(&tmap_col);
+    if constexpr (C::MODE == kEpiSwiGLU) tma_prefetch_desc(&tmap_col2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  int grouped_tiles = -1;
+  if constexpr (C::GROUPED) {
+    for (int i = threadIdx.x; i <= prm.E; i += C::kThreads) {
+      grp_rows[i] = __ldg(prm.grp_rows + i);
+      grp_mtiles[i] = __ldg(prm.grp_mtiles + i);
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  if constexpr (C::GROUPED) grouped_tiles = grp_mtiles[prm.E] * prm.tiles_col;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      Sched sch(prm, blockIdx.x);
+      Sched sch(prm, blockIdx.x, grouped_tiles);
       Unit u;
       int st = 0;
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
       while (ok && sch.next(u)) {
-        int tl, tc;
-        tile_coords(prm, u.tile, tl, tc);
+        const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, prm.err, kDevErrTimeoutProducer)) {
             ok = false;
@@ -245,8 +408,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
           mbar_arrive_expect_tx(&full[st], C::kStageBytes);
           uint8_t* sa = smem + st * C::kStageBytes;
-          tma_load_2d(sa, &tmap_lane, &full[st], kb * 128, tl * 128);
-          tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, tc * C::BN);
+          tma_load_2d(sa, &tmap_lane, &full[st], kb * 128, t.lane_y);
+          if constexpr (C::MODE == kEpiSwiGLU) {
+            // Column rows [0,64) w1, [64,128) w3, [128,192) w1 + 64, [192,256) w3 + 64.
+            uint8_t* sb = sa + C::kABytes;
+            tma_load_2d(sb, &tmap_col, &full[st], kb * 128, t.col_y);
+            tma_load_2d(sb + 64 * 128, &tmap_col2, &full[st], kb * 128, t.col_y);
+            tma_load_2d(sb + 128 * 128, &tmap_col, &full[st], kb * 128, t.col_y + 64);
+            tma_load_2d(sb + 192 * 128, &tmap_col2, &full[st], kb * 128, t.col_y + 64);
+          } else {
+            tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, t.col_y);
+          }
           ++issued;
           if (++st == C::STAGES) {
             st = 0;
@@ -268,7 +440,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_e4m3_f32(128, C::BN);
-      Sched sch(prm, blockIdx.x);
+      Sched sch(prm, blockIdx.x, grouped_tiles);
       Unit u;
       int st = 0, pb = 0;
       uint32_t ph = 0, pph = 0;
@@ -324,34 +496,42 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       return r;
     };
 
-    Sched sch(prm, blockIdx.x);
+    Sched sch(prm, blockIdx.x, grouped_tiles);
     Unit u;
     int pb = 0;
     uint32_t pph = 0;
+    uint32_t unit_parity = 0;
     bool ok = true;
     while (ok && sch.next(u)) {
-      int tl, tc;
-      tile_coords(prm, u.tile, tl, tc);
+      const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles);
       float acc[C::kCpt];
 #pragma unroll
       for (int i = 0; i < C::kCpt; ++i) acc[i] = 0.0f;
 
       for (int kb = u.kb0; kb < u.kb1; ++kb) {
         // Scales of this K block, loaded before the wait to hide their latency.
-        float sc_row = 0.0f;
+        // sc_lo applies to the first half of the thread's columns, sc_hi to the
+        // second (they differ only in SwiGLU mode: w1 vs w3 scales).
+        float sc_lo = 0.0f, sc_hi = 0.0f;
         float sc_col[kAsRegs];
         if constexpr (!C::SWAP) {
-          const int m = tl * 128 + row;
-          const int nb = tc * C::kGroups + group;
-          const float as = (m < prm.M) ? __ldg(prm.a_s + static_cast<size_t>(m) * prm.Kb + kb) : 0.0f;
-          const float ws = (nb < prm.n_wblocks) ? __ldg(prm.w_s + static_cast<size_t>(nb) * prm.Kb + kb) : 0.0f;
-          sc_row = as * ws;
+          const float as =
+              (row < t.lane_valid) ? __ldg(prm.a_s + static_cast<size_t>(t.lane_y + row) * prm.Kb + kb) : 0.0f;
+          if constexpr (C::MODE == kEpiSwiGLU) {
+            sc_lo = as * __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
+            sc_hi = as * __ldg(prm.w3_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
+          } else {
+            const int nb = t.wblock + group;
+            const bool wv = C::GROUPED || nb < prm.n_wblocks;
+            sc_lo = wv ? as * __ldg(prm.w_s + static_cast<size_t>(nb) * prm.Kb + kb) : 0.0f;
+            sc_hi = sc_lo;
+          }
         } else {
-          const float ws = __ldg(prm.w_s + static_cast<size_t>(tl) * prm.Kb + kb);
+          const float ws = __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
 #pragma unroll
           for (int i = 0; i < kAsRegs; ++i) {
             const int j = lane + 32 * i;
-            const int m = tc * C::BN + j;
+            const int m = t.col0 + j;
             sc_col[i] = (j < C::kCpt && m < prm.M) ? __ldg(prm.a_s + static_cast<size_t>(m) * prm.Kb + kb) * ws
                                                    : 0.0f;
           }
@@ -362,22 +542,29 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t col0 = static_cast<uint32_t>(pb * C::BN + group * C::kCpt);
-        if constexpr (C::kCpt == 16) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(t_lane + col0, v);
+        if constexpr (C::kCpt == 16 || C::EPI_WARPS == 8) {
+          // 16-column loads: fewer live registers next to 128 accumulators
+          // (ten warps leave 168 registers per thread).
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float sc = C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[0], i) : sc_row;
-            acc[i] = fmaf(__uint_as_float(v[i]), sc, acc[i]);
+          for (int ch = 0; ch < C::kCpt / 16; ++ch) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(t_lane + col0 + ch * 16, v);
+            const float sc_h = (ch < C::kCpt / 32) ? sc_lo : sc_hi;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float sc = C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[(ch * 16 + i) / 32], (ch * 16 + i) % 32) : sc_h;
+              acc[ch * 16 + i] = fmaf(__uint_as_float(v[i]), sc, acc[ch * 16 + i]);
+            }
           }
         } else {
 #pragma unroll
           for (int ch = 0; ch < C::kCpt / 32; ++ch) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_lane + col0 + ch * 32, v);
+            const float sc_h = (ch < C::kCpt / 64) ? sc_lo : sc_hi;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float sc = C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[ch], i) : sc_row;
+              const float sc = C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[ch], i) : sc_h;
               acc[ch * 32 + i] = fmaf(__uint_as_float(v[i]), sc, acc[ch * 32 + i]);
             }
           }
@@ -393,7 +580,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (!ok) break;
 
       if (u.nparts == 1) {
-        store_tile<C>(prm, acc, tl, tc, group, row);
+        ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync);
       } else {
         // Stream-K fixup: publish this part, count arrivals, the last part sums.
         float* mine = prm.slots + static_cast<size_t>(2 * blockIdx.x + (u.part == 0 ? 1 : 0)) * (C::BN * 128);
@@ -417,10 +604,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < C::kCpt; ++i) acc[i] += __ldcg(src + (group * C::kCpt + i) * 128 + row);
           }
-          store_tile<C>(prm, acc, tl, tc, group, row);
+          ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync);
           if (ew == 0 && lane == 0) prm.counters[u.tile] = 0;
         }
       }
+      unit_parity ^= 1u;
     }
   }
 
@@ -477,6 +665,11 @@ using CfgS16 = Cfg<16, true, 8, 8, 4>;
 using CfgS32 = Cfg<32, true, 8, 8, 4>;
 using CfgS64 = Cfg<64, true, 6, 4, 4>;
 using CfgS128 = Cfg<128, true, 6, 4, 4>;
+// Fused w1/w3 GEMM with the SwiGLU + act_quant epilogue (dense and grouped),
+// and the grouped GEMM whose rows are scattered back to token order.
+using CfgSwiGLU = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false>;
+using CfgSwiGLUGrouped = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, true>;
+using CfgScatterGrouped = Cfg<256, false, 4, 2, 8, kEpiScatter, true>;
 
 struct Plan {
   int bn;
@@ -486,20 +679,8 @@ struct Plan {
   long long sk_iters;
 };
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
-  Plan pl{};
-  const int64_t Kb = K / kBlock;
-  if (M <= 128) {
-    pl.swap = true;
-    pl.bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-    pl.tiles_lane = static_cast<int>((N + 127) / 128);
-    pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
-  } else {
-    pl.swap = false;
-    pl.bn = N <= 128 ? 128 : 256;
-    pl.tiles_lane = static_cast<int>((M + 127) / 128);
-    pl.tiles_col = static_cast<int>((N + pl.bn - 1) / pl.bn);
-  }
+// Data-parallel waves while at least two full waves remain, stream-K for the rest.
+void plan_schedule(Plan& pl, int64_t Kb, int sm_count) {
   const long long tiles = static_cast<long long>(pl.tiles_lane) * pl.tiles_col;
   const int G = sm_count;
   if (tiles >= 2LL * G) {
@@ -513,6 +694,34 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
     pl.grid = static_cast<int>(iters < G ? iters : G);
   }
   pl.sk_iters = static_cast<long long>(pl.sk_tiles) * Kb;
+}
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
+  Plan pl{};
+  if (M <= 128) {
+    pl.swap = true;
+    pl.bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    pl.tiles_lane = static_cast<int>((N + 127) / 128);
+    pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
+  } else {
+    pl.swap = false;
+    pl.bn = N <= 128 ? 128 : 256;
+    pl.tiles_lane = static_cast<int>((M + 127) / 128);
+    pl.tiles_col = static_cast<int>((N + pl.bn - 1) / pl.bn);
+  }
+  plan_schedule(pl, K / kBlock, sm_count);
+  return pl;
+}
+
+// The fused w1/w3 GEMM: 128 activation rows x 128 output columns per tile
+// (MMA N = 256: 128 columns of w1 and the same 128 of w3).
+Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count) {
+  Plan pl{};
+  pl.swap = false;
+  pl.bn = 256;
+  pl.tiles_lane = static_cast<int>((M + 127) / 128);
+  pl.tiles_col = static_cast<int>(inter / 128);
+  plan_schedule(pl, K / kBlock, sm_count);
   return pl;
 }
 
@@ -529,8 +738,8 @@ int sm_count_or_default() {
 }
 
 template <class C>
-int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const GemmParams& prm,
-           cudaStream_t stream) {
+int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const CUtensorMap& mc2,
+           const GemmParams& prm, cudaStream_t stream) {
   static bool attr_done[64] = {};
   auto kern = fp8_gemm_kernel<C>;
   if (d->device >= 64 || !attr_done[d->device]) {
@@ -538,7 +747,7 @@ int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const
       return FP8BLK_ERR_CUDA;
     if (d->device < 64) attr_done[d->device] = true;
   }
-  kern<<<prm.grid, C::kThreads, C::kSmemBytes, stream>>>(ml, mc, prm);
+  kern<<<prm.grid, C::kThreads, C::kSmemBytes, stream>>>(ml, mc, mc2, prm);
   return launch_status();
 }
 
@@ -588,6 +797,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   prm.sk_tiles = pl.sk_tiles;
   prm.sk_iters = pl.sk_iters;
   prm.vec_store = (N % 8 == 0 && is_aligned(c, 16)) ? 1 : 0;
+  prm.ldc = static_cast<int>(N);
 
   CUtensorMap ml, mc;
   const void* lane_src = pl.swap ? w : a;
@@ -599,15 +809,137 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     return FP8BLK_ERR_CUDA;
 
   if (!pl.swap) {
-    if (pl.bn == 256) return launch<CfgN256>(d, ml, mc, prm, stream);
-    return launch<CfgN128>(d, ml, mc, prm, stream);
+    if (pl.bn == 256) return launch<CfgN256>(d, ml, mc, mc, prm, stream);
+    return launch<CfgN128>(d, ml, mc, mc, prm, stream);
   }
   switch (pl.bn) {
-    case 16: return launch<CfgS16>(d, ml, mc, prm, stream);
-    case 32: return launch<CfgS32>(d, ml, mc, prm, stream);
-    case 64: return launch<CfgS64>(d, ml, mc, prm, stream);
-    default: return launch<CfgS128>(d, ml, mc, prm, stream);
+    case 16: return launch<CfgS16>(d, ml, mc, mc, prm, stream);
+    case 32: return launch<CfgS32>(d, ml, mc, mc, prm, stream);
+    case 64: return launch<CfgS64>(d, ml, mc, mc, prm, stream);
+    default: return launch<CfgS128>(d, ml, mc, mc, prm, stream);
   }
+}
+
+namespace {
+
+bool scale_fmt_ok(int f) { return f == FP8BLK_SCALE_FP32 || f == FP8BLK_SCALE_UE8M0; }
+
+}  // namespace
+
+size_t swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t K) {
+  if (M <= 0 || inter <= 0 || K <= 0) return 256;
+  return plan_workspace(make_swiglu_plan(M, inter, K, sm_count_or_default()));
+}
+
+// u = act_quant(bf16(silu(bf16(x w1^T))) * bf16(x w3^T)) in one kernel.
+int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s, const void* w3, const float* w3s,
+               void* uq, float* us, int64_t M, int64_t inter, int64_t K, int scale_fmt, void* workspace,
+               size_t workspace_bytes, cudaStream_t stream) {
+  if (!scale_fmt_ok(scale_fmt)) return FP8BLK_ERR_ARG;
+  const int64_t lim = (int64_t{1} << 31) - 1;
+  if (M < 0 || inter < 0 || K <= 0 || K % kBlock || inter % kBlock || M > lim || inter > lim || K > lim)
+    return FP8BLK_ERR_SHAPE;
+  if (M == 0 || inter == 0) return FP8BLK_OK;
+  if (!xq || !xs || !w1 || !w1s || !w3 || !w3s || !uq || !us) return FP8BLK_ERR_NULL;
+  if (!is_aligned(xq, 16) || !is_aligned(w1, 16) || !is_aligned(w3, 16) || !is_aligned(uq, 16) ||
+      !is_aligned(xs, 4) || !is_aligned(w1s, 4) || !is_aligned(w3s, 4) || !is_aligned(us, 4))
+    return FP8BLK_ERR_ALIGN;
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  const Plan pl = make_swiglu_plan(M, inter, K, d->sm_count);
+  if (!workspace || workspace_bytes < plan_workspace(pl)) return FP8BLK_ERR_WORKSPACE;
+  if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
+  GemmParams prm{};
+  prm.a_s = xs;
+  prm.w_s = w1s;
+  prm.w3_s = w3s;
+  prm.uq = static_cast<uint8_t*>(uq);
+  prm.us = us;
+  const size_t tiles = static_cast<size_t>(pl.tiles_lane) * pl.tiles_col;
+  prm.counters = static_cast<int*>(workspace);
+  prm.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(tiles * sizeof(int)));
+  prm.err = d->err_word;
+  prm.M = static_cast<int>(M);
+  prm.N = static_cast<int>(inter);
+  prm.Kb = static_cast<int>(K / kBlock);
+  prm.n_wblocks = static_cast<int>(inter / kBlock);
+  prm.ldc = static_cast<int>(inter);
+  prm.tiles_lane = pl.tiles_lane;
+  prm.tiles_col = pl.tiles_col;
+  prm.grid = pl.grid;
+  prm.dp_waves = pl.dp_waves;
+  prm.sk_tiles = pl.sk_tiles;
+  prm.sk_iters = pl.sk_iters;
+  prm.ue8m0 = scale_fmt == FP8BLK_SCALE_UE8M0;
+  CUtensorMap ml, m1, m3;
+  if (!make_kmajor_map(&ml, xq, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128) ||
+      !make_kmajor_map(&m1, w1, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64) ||
+      !make_kmajor_map(&m3, w3, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64))
+    return FP8BLK_ERR_CUDA;
+  return launch<CfgSwiGLU>(d, ml, m1, m3, prm, stream);
+}
+
+// Grouped fused w1/w3 GEMM over rows sorted by group: group e owns rows
+// [grp_rows[e], grp_rows[e+1]) of xg and weight rows [e*inter, (e+1)*inter)
+// of w1 and w3. grp_rows / grp_mtiles are device arrays of E + 1 entries.
+int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const float* w1s, const void* w3,
+                       const float* w3s, void* uq, float* us, int64_t rows, int64_t E, int64_t inter, int64_t K,
+                       const int* grp_rows, const int* grp_mtiles, int scale_fmt, cudaStream_t stream) {
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  GemmParams prm{};
+  prm.a_s = xgs;
+  prm.w_s = w1s;
+  prm.w3_s = w3s;
+  prm.uq = static_cast<uint8_t*>(uq);
+  prm.us = us;
+  prm.grp_rows = grp_rows;
+  prm.grp_mtiles = grp_mtiles;
+  prm.err = d->err_word;
+  prm.M = static_cast<int>(rows);
+  prm.N = static_cast<int>(inter);
+  prm.Kb = static_cast<int>(K / kBlock);
+  prm.ldc = static_cast<int>(inter);
+  prm.E = static_cast<int>(E);
+  prm.tiles_col = static_cast<int>(inter / 128);
+  prm.grid = d->sm_count;
+  prm.ue8m0 = scale_fmt == FP8BLK_SCALE_UE8M0;
+  CUtensorMap ml, m1, m3;
+  if (!make_kmajor_map(&ml, xg, static_cast<uint64_t>(rows), static_cast<uint64_t>(K), 128) ||
+      !make_kmajor_map(&m1, w1, static_cast<uint64_t>(E * inter), static_cast<uint64_t>(K), 64) ||
+      !make_kmajor_map(&m3, w3, static_cast<uint64_t>(E * inter), static_cast<uint64_t>(K), 64))
+    return FP8BLK_ERR_CUDA;
+  return launch<CfgSwiGLUGrouped>(d, ml, m1, m3, prm, stream);
+}
+
+// Grouped GEMM (w2) whose output row r goes to out[perm[r]]: group e's rows
+// times weight rows [e*dim, (e+1)*dim) of w2 [E*dim, inter]; dim % 256 == 0.
+int grouped_scatter_run(const void* uq, const float* us, const void* w2, const float* w2s, void* out,
+                        const int* perm, int64_t rows, int64_t E, int64_t dim, int64_t inter, const int* grp_rows,
+                        const int* grp_mtiles, cudaStream_t stream) {
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  GemmParams prm{};
+  prm.a_s = us;
+  prm.w_s = w2s;
+  prm.c = static_cast<__nv_bfloat16*>(out);
+  prm.perm = perm;
+  prm.grp_rows = grp_rows;
+  prm.grp_mtiles = grp_mtiles;
+  prm.err = d->err_word;
+  prm.M = static_cast<int>(rows);
+  prm.N = static_cast<int>(dim);
+  prm.Kb = static_cast<int>(inter / kBlock);
+  prm.ldc = static_cast<int>(dim);
+  prm.E = static_cast<int>(E);
+  prm.tiles_col = static_cast<int>(dim / 256);
+  prm.grid = d->sm_count;
+  prm.vec_store = (dim % 8 == 0 && is_aligned(out, 16)) ? 1 : 0;
+  CUtensorMap ml, mc;
+  if (!make_kmajor_map(&ml, uq, static_cast<uint64_t>(rows), static_cast<uint64_t>(inter), 128) ||
+      !make_kmajor_map(&mc, w2, static_cast<uint64_t>(E * dim), static_cast<uint64_t>(inter), 256))
+    return FP8BLK_ERR_CUDA;
+  return launch<CfgScatterGrouped>(d, ml, mc, mc, prm, stream);
 }
 
 }  // namespace fp8blk

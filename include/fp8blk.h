@@ -158,6 +158,74 @@ FP8BLK_API int fp8blk_linear_host(const void *x_host_bf16, const void *w_e4m3, c
                        fp8blk_stream_t stream);
 
 /*
+ * Fused w1/w3 GEMM of the SwiGLU FFN ("Administrator & Developer Guide", 1.2
+ * module map: MLP / Expert compute w2(silu(w1 x) * w3 x); 6.3: every Linear
+ * quantises its input). With h1 = bf16(x w1^T) and h3 = bf16(x w3^T) (each an
+ * fp8_gemm as above):
+ *     u = bf16( bf16(silu(h1)) * h3 ),  silu(v) = v / (1 + e^-v) in fp32,
+ *     (u_q, u_s) = act_quant(u, scale_fmt)   -- the input of the w2 Linear.
+ * x: e4m3 [M, dim] + x_s [M, dim/128]; w1, w3: e4m3 [inter, dim] + scales
+ * [inter/128, dim/128]; u_q: e4m3 [M, inter] (16-byte aligned); u_s: fp32
+ * [M, inter/128]. dim % 128 == 0, inter % 128 == 0. The act_quant of u happens
+ * in the GEMM's epilogue (u never reaches memory in bf16).
+ * Workspace: fp8blk_swiglu_workspace_bytes(M, inter, dim), zero-filled before
+ * first use, left zero-filled.
+ */
+FP8BLK_API size_t fp8blk_swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t dim);
+FP8BLK_API int fp8blk_swiglu_gemm(const void *x_e4m3, const float *x_s, const void *w1_e4m3, const float *w1_s,
+                                  const void *w3_e4m3, const float *w3_s, void *u_e4m3, float *u_s, int64_t M,
+                                  int64_t inter, int64_t dim, int scale_fmt, void *workspace,
+                                  size_t workspace_bytes, fp8blk_stream_t stream);
+
+/*
+ * Dense SwiGLU FFN (the guide's MLP with FP8 Linears): y = w2(u) with
+ * u from fp8blk_swiglu_gemm on act_quant(x). x: bf16 [M, dim]; w2: e4m3
+ * [dim, inter] + scales [dim/128, inter/128]; y: bf16 [M, dim].
+ * Workspace: fp8blk_ffn_workspace_bytes(M, dim, inter), zero-filled before first use.
+ */
+FP8BLK_API size_t fp8blk_ffn_workspace_bytes(int64_t M, int64_t dim, int64_t inter);
+FP8BLK_API int fp8blk_ffn(const void *x_bf16, const void *w1_e4m3, const float *w1_s, const void *w3_e4m3,
+                          const float *w3_s, const void *w2_e4m3, const float *w2_s, void *y_bf16, int64_t M,
+                          int64_t dim, int64_t inter, int scale_fmt, void *workspace, size_t workspace_bytes,
+                          fp8blk_stream_t stream);
+
+/*
+ * MoE routing permutation ("Administrator & Developer Guide", 6.4: the
+ * per-expert bincount, then for each expert the (token, slot) pairs routed to
+ * it). topk_idx: int32 [T, topk] expert ids. Outputs (device):
+ *     counts[e]   = number of pairs routed to expert e, e < E,
+ *     offsets[e]  = exclusive prefix sum of counts, offsets[E] = valid pairs,
+ *     perm[offsets[e] + r] = t * topk + j of the r-th pair of expert e, in
+ *                   increasing pair order (a stable sort by expert id).
+ * Integer work, no host synchronisation. E <= 1024. Ids outside [0, E) join no
+ * expert and set a bit read by fp8blk_last_device_error.
+ */
+FP8BLK_API int fp8blk_moe_permute(const int32_t *topk_idx, int64_t T, int64_t topk, int64_t E, int32_t *counts,
+                                  int32_t *offsets, int32_t *perm, fp8blk_stream_t stream);
+
+/*
+ * Routed-expert FFN ("Administrator & Developer Guide", 6.4 and 8.4 steps
+ * 2-5): y[t] = bf16( sum over slots j (in order) of
+ *                    topk_w[t, j] * bf16(FFN_{topk_idx[t, j]}(x[t])) ),
+ * FFN_e(x) = w2_e(act_quant(bf16(silu(bf16(w1_e x))) * bf16(w3_e x))) with the
+ * rounding of fp8blk_swiglu_gemm, accumulation of the sum in fp32.
+ * x: e4m3 [T, dim] + x_s [T, dim/128] (x quantised once per token: act_quant
+ * is per row, so it commutes with routing). topk_idx int32 / topk_w fp32
+ * [T, topk]. Stacked expert weights: w1, w3 e4m3 [E*inter, dim] with scales
+ * [E*inter/128, dim/128]; w2 e4m3 [E*dim, inter] with scales [E*dim/128,
+ * inter/128]. y: bf16 [T, dim]. dim % 256 == 0, inter % 128 == 0, E <= 1024.
+ * Experts that receive no token read none of their weights.
+ * Workspace: fp8blk_moe_workspace_bytes(T, topk, E, dim, inter), 256-aligned.
+ */
+FP8BLK_API size_t fp8blk_moe_workspace_bytes(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t inter);
+FP8BLK_API int fp8blk_moe_grouped_gemm(const void *x_e4m3, const float *x_s, const int32_t *topk_idx,
+                                       const float *topk_w, const void *w1_e4m3, const float *w1_s,
+                                       const void *w3_e4m3, const float *w3_s, const void *w2_e4m3,
+                                       const float *w2_s, void *y_bf16, int64_t T, int64_t topk, int64_t E,
+                                       int64_t dim, int64_t inter, int scale_fmt, void *workspace,
+                                       size_t workspace_bytes, fp8blk_stream_t stream);
+
+/*
  * fp8_gemm with no workspace argument and no device allocation: the same
  * computation, result and argument rules as fp8blk_gemm, but its scratch
  * (tile counters and stream-K partial sums) lives in a buffer of

@@ -111,3 +111,87 @@ def test_decode_plan_uses_whole_machine():
 def test_prefill_plan_is_hybrid():
     p = make_plan(4096, 18432, 7168, 152)
     assert not p["swap"] and p["bn"] == 256 and p["dp"] == 14 and p["sk_tiles"] == 2304 - 14 * 152
+
+
+# ---- grouped (per-expert) tiles and the routing permutation -------------------
+
+def grouped_tile(tile, mtiles, tiles_col, E):
+    """Mirror of the kernel's tile -> (group, column tile, row tile) mapping."""
+    lo, hi = 0, E - 1
+    while lo < hi:
+        mid = (lo + hi + 1) >> 1
+        if mtiles[mid] * tiles_col <= tile:
+            lo = mid
+        else:
+            hi = mid - 1
+    e = lo
+    mt_e = mtiles[e + 1] - mtiles[e]
+    local = tile - mtiles[e] * tiles_col
+    return e, local // mt_e, local % mt_e
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_tiles_cover_every_group_tile_once(seed):
+    import numpy as np
+
+    g = np.random.Generator(np.random.PCG64(seed))
+    E = int(g.integers(1, 40))
+    counts = g.integers(0, 400, E) * (g.random(E) < 0.7)       # some empty experts
+    mt = -(-counts // 128)
+    mtiles = np.concatenate([[0], np.cumsum(mt)])
+    tiles_col = int(g.integers(1, 30))
+    want = {(e, nt, m) for e in range(E) for nt in range(tiles_col) for m in range(mt[e])}
+    got = [grouped_tile(t, mtiles, tiles_col, E) for t in range(int(mtiles[-1]) * tiles_col)]
+    assert len(got) == len(set(got)) and set(got) == want
+
+
+def permute_mirror(idx, E, chunk=1024):
+    """Mirror of the one-CTA permutation: per-chunk per-warp counts (match_any
+    ranks within a warp, prefix over earlier warps), running bases."""
+    import numpy as np
+
+    flat = idx.ravel()
+    n = flat.size
+    valid = (flat >= 0) & (flat < E)
+    counts = np.bincount(flat[valid], minlength=E)
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    base = offsets[:-1].copy()
+    perm = np.full(n, -1)
+    for c0 in range(0, n, chunk):
+        ids = np.arange(c0, min(c0 + chunk, n))
+        wtab = np.zeros((chunk // 32, E), np.int64)
+        rank = {}
+        for i in ids:
+            e = flat[i]
+            if not (0 <= e < E):
+                continue
+            w, lane = (i - c0) // 32, (i - c0) % 32
+            same = [j for j in range(c0 + w * 32, i) if flat[j] == e]
+            rank[i] = len(same)
+            wtab[w, e] += 1
+        for i in ids:
+            e = flat[i]
+            if not (0 <= e < E):
+                continue
+            w = (i - c0) // 32
+            perm[base[e] + wtab[:w, e].sum() + rank[i]] = i
+        base += wtab.sum(axis=0)
+    return counts, offsets, perm[: offsets[-1]]
+
+
+def test_permute_mirror_is_the_stable_sort():
+    import numpy as np
+
+    import oracle
+    import synthetic
+
+    idx, _ = synthetic.moe_routing(300, 16, 4, 91, zipf_s=1.2)
+    c, o, p = permute_mirror(idx, 16, chunk=256)
+    co, oo, po = oracle.moe_permute(idx, 16)
+    assert np.array_equal(c, co) and np.array_equal(o, oo) and np.array_equal(p, po)
+    bad = idx.copy()
+    bad[3, 1] = 99
+    bad[7, 0] = -1
+    c, o, p = permute_mirror(bad, 16, chunk=256)
+    keep = np.flatnonzero((bad.ravel() >= 0) & (bad.ravel() < 16))
+    assert np.array_equal(p, keep[np.argsort(bad.ravel()[keep], kind="stable")])

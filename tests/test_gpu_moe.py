@@ -1,0 +1,209 @@
+"""GPU parity of the SwiGLU FFN chain and the routed-expert (MoE) path
+against the CPU oracle ("Administrator & Developer Guide", 6.4 and 8.4; 1.2
+MLP / Expert).
+
+- The routing permutation is integer work: bit-exact.
+- The fused w1/w3 GEMM's e4m3 output is checked structurally against the
+  oracle chain. Its codes and scales match in all but a few elements: one
+  bf16 step of silu or of the fp32 accumulation can flip a code.
+- The chains (dense FFN, MoE) are graded on their final output with the GEMM
+  tolerance |diff| <= 2^-7 |ref| + 1e-3 rms(ref)."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_quant_gb300 as fb
+import oracle
+import synthetic
+from helpers import assert_gemm_close, bits_to_dev_bf16, dev_to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def to_dev_q(q):
+    return torch.from_numpy(q).cuda().view(torch.float8_e4m3fn)
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# ---- A5: permutation ------------------------------------------------------------
+
+@pytest.mark.parametrize("T,E,k,zipf", [(4096, 256, 8, 0.0), (4096, 256, 8, 1.2), (1, 4, 2, 0.0),
+                                        (3000, 1024, 6, 1.2), (700, 7, 3, 0.0)])
+def test_moe_permute_bit_exact(T, E, k, zipf):
+    idx, _ = synthetic.moe_routing(T, E, k, 500 + T + E, zipf_s=zipf)
+    counts, offsets, perm = fb.moe_permute(to_dev(idx), E)
+    co, oo, po = oracle.moe_permute(idx, E)
+    assert np.array_equal(counts.cpu().numpy(), co)
+    assert np.array_equal(offsets.cpu().numpy(), oo)
+    assert np.array_equal(perm.cpu().numpy(), po)
+
+
+def test_moe_permute_invalid_ids_reported_and_skipped():
+    idx, _ = synthetic.moe_routing(50, 8, 2, 7)
+    bad = idx.copy()
+    bad[4, 1] = 8
+    bad[9, 0] = -3
+    counts, offsets, perm = fb.moe_permute(to_dev(bad), 8)
+    assert fb.last_device_error() != 0          # reported ...
+    keep = np.flatnonzero((bad.ravel() >= 0) & (bad.ravel() < 8))
+    want = keep[np.argsort(bad.ravel()[keep], kind="stable")]
+    assert offsets[-1].item() == keep.size      # ... and left out
+    assert np.array_equal(perm[: keep.size].cpu().numpy(), want)
+    assert fb.last_device_error() == 0          # the bit was cleared
+
+
+# ---- A4: fused w1/w3 GEMM with SwiGLU + act_quant --------------------------------
+
+def oracle_u(xq, xs, w1q, w1s, w3q, w3s, ue8m0=False):
+    h1 = oracle.bf16_round(oracle.gemm(xq, xs, w1q, w1s))
+    h3 = oracle.bf16_round(oracle.gemm(xq, xs, w3q, w3s))
+    return oracle.act_quant(oracle.swiglu(h1, h3), ue8m0)
+
+
+@pytest.mark.parametrize("M,dim,inter", [(5, 256, 384), (130, 512, 256), (300, 256, 1024)])
+@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0])
+def test_swiglu_gemm_matches_oracle_chain(M, dim, inter, fmt):
+    ue = fmt == fb.SCALE_UE8M0
+    x = synthetic.activations(M, dim, 600 + M)
+    xq, xs = oracle.act_quant(x, ue)
+    w1q, w1s = oracle.weight_quant(synthetic.weights(inter, dim, 601 + M), ue)
+    w3q, w3s = oracle.weight_quant(synthetic.weights(inter, dim, 602 + M), ue)
+    u, us = fb.swiglu_gemm(to_dev_q(xq), to_dev(xs), to_dev_q(w1q), to_dev(w1s), to_dev_q(w3q), to_dev(w3s), fmt)
+    uo, uso = oracle_u(xq, xs, w1q, w1s, w3q, w3s, ue)
+    got_q, got_s = dev_to_bits(u), us.cpu().numpy()
+    assert (got_s == uso).mean() > 0.98
+    assert (got_q == uo).mean() > 0.995
+    # dequantised u agrees with the oracle's to a few e4m3 steps everywhere
+    dq = oracle.e4m3_decode_array(got_q) * np.repeat(got_s.astype(np.float64), 128, axis=1)
+    dqo = oracle.e4m3_decode_array(uo) * np.repeat(uso.astype(np.float64), 128, axis=1)
+    scale = np.repeat(uso.astype(np.float64), 128, axis=1)
+    assert np.all(np.abs(dq - dqo) <= 2.0 ** -2 * np.abs(dqo) + 2 * scale * 2.0 ** -6)
+
+
+# ---- A4 chain: dense FFN ---------------------------------------------------------
+
+@pytest.mark.parametrize("M,dim,inter", [(5, 256, 384), (300, 256, 384), (129, 512, 1024)])
+def test_ffn_full_compare(M, dim, inter):
+    x = synthetic.activations(M, dim, 700 + M, outlier_frac=0.02)
+    w1 = synthetic.weights(inter, dim, 701)
+    w3 = synthetic.weights(inter, dim, 702)
+    w2 = synthetic.weights(dim, inter, 703)
+    w1q, w1s = oracle.weight_quant(w1)
+    w3q, w3s = oracle.weight_quant(w3)
+    w2q, w2s = oracle.weight_quant(w2)
+    xq, xs = oracle.act_quant(x)
+    y = fb.ffn(bits_to_dev_bf16(x), to_dev_q(w1q), to_dev(w1s), to_dev_q(w3q), to_dev(w3s), to_dev_q(w2q),
+               to_dev(w2s))
+    ref = oracle.ffn_rows(xq, xs, w1q, w1s, w3q, w3s, w2q, w2s, range(M))
+    assert_gemm_close(dev_to_bits(y), ref, what=f"ffn {M}x{dim}x{inter}")
+    # repeated call: workspaces were left clean
+    y2 = fb.ffn(bits_to_dev_bf16(x), to_dev_q(w1q), to_dev(w1s), to_dev_q(w3q), to_dev(w3s), to_dev_q(w2q),
+                to_dev(w2s))
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_ffn_full_size_sampled_rows():
+    """The prefill FFN (x [4096, 7168], inter 18432) on the device; the oracle
+    recomputes two whole output rows (one per end of the row range)."""
+    M, dim, inter = 4096, 7168, 18432
+    dev = torch.device("cuda")
+    x = synthetic.device_activations(M, dim, synthetic.SEED_PREFILL, dev)
+    ws = [synthetic.device_normal(shape, synthetic.SEED_PREFILL + 10 + i, 0.02, dev)
+          for i, shape in enumerate([(inter, dim), (inter, dim), (dim, inter)])]
+    qs = [fb.weight_quant(w) for w in ws]
+    y = fb.ffn(x, qs[0][0], qs[0][1], qs[1][0], qs[1][1], qs[2][0], qs[2][1])
+    rows = np.array([1, M - 2])
+    xq, xs = oracle.act_quant(dev_to_bits(x[torch.from_numpy(rows).to(dev)]))
+    host_q = [oracle.weight_quant(w.cpu().numpy()) for w in ws]
+    for (q, s), (qo, so) in zip(qs, host_q):
+        assert np.array_equal(dev_to_bits(q), qo) and np.array_equal(s.cpu().numpy(), so)
+    ref = oracle.ffn_rows(xq, xs, *host_q[0], *host_q[1], *host_q[2], range(2))
+    rms = float(y.float().pow(2).mean().sqrt())
+    assert_gemm_close(dev_to_bits(y)[rows], ref, rms=rms, what="ffn sampled rows")
+
+
+# ---- A6/A7: routed experts ----------------------------------------------------------
+
+def moe_problem(T, E, dim, inter, k, seed, zipf=0.0, ue8m0=False):
+    x = synthetic.activations(T, dim, seed, outlier_frac=0.01)
+    xq, xs = oracle.act_quant(x, ue8m0)
+    w1q, w1s = oracle.weight_quant(synthetic.weights(E * inter, dim, seed + 1), ue8m0)
+    w3q, w3s = oracle.weight_quant(synthetic.weights(E * inter, dim, seed + 2), ue8m0)
+    w2q, w2s = oracle.weight_quant(synthetic.weights(E * dim, inter, seed + 3), ue8m0)
+    idx, wts = synthetic.moe_routing(T, E, k, seed + 4, zipf_s=zipf)
+    return xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s
+
+
+def run_moe(p, E, fmt=fb.SCALE_FP32):
+    xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s = p
+    return fb.moe_grouped_gemm(to_dev_q(xq), to_dev(xs), to_dev(idx), to_dev(wts), to_dev_q(w1q), to_dev(w1s),
+                               to_dev_q(w3q), to_dev(w3s), to_dev_q(w2q), to_dev(w2s), E, fmt)
+
+
+@pytest.mark.parametrize("T,E,dim,inter,k,zipf", [(64, 8, 256, 256, 2, 0.0), (96, 16, 512, 384, 4, 1.2),
+                                                  (33, 5, 256, 128, 3, 0.0), (300, 4, 256, 256, 1, 0.0)])
+@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0])
+def test_moe_full_compare(T, E, dim, inter, k, zipf, fmt):
+    p = moe_problem(T, E, dim, inter, k, 800 + T + E, zipf, fmt == fb.SCALE_UE8M0)
+    y = run_moe(p, E, fmt)
+    ref_bits = oracle.moe_tokens(*p, range(T), ue8m0=fmt == fb.SCALE_UE8M0)
+    ref = synthetic.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    # the oracle's bf16 output plus one bf16 step of slack for its own rounding
+    assert_gemm_close(dev_to_bits(y), ref, what=f"moe T={T} E={E}")
+    assert fb.last_device_error() == 0
+
+
+def test_moe_empty_experts_and_invalid_slots():
+    T, E, dim, inter = 40, 6, 256, 256
+    xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s = moe_problem(T, E, dim, inter, 2, 900)
+    idx[:, :] = np.where(idx >= 3, idx % 3, idx)     # experts 3..5 get no token
+    idx[:, 1] = np.where(idx[:, 1] == idx[:, 0], (idx[:, 0] + 1) % 3, idx[:, 1])
+    bad = idx.copy()
+    bad[5, 1] = 17                                   # invalid slot: contributes nothing
+    y = run_moe((xq, xs, bad, wts, w1q, w1s, w3q, w3s, w2q, w2s), E)
+    assert fb.last_device_error() != 0
+    idx_ref, wts_ref = bad.copy(), wts.copy()
+    idx_ref[5, 1], wts_ref[5, 1] = 0, 0.0
+    ref = oracle.moe_tokens(xq, xs, idx_ref, wts_ref, w1q, w1s, w3q, w3s, w2q, w2s, range(T))
+    assert_gemm_close(dev_to_bits(y), synthetic.bf16_bits_to_f32(ref).astype(np.float64))
+
+
+def test_moe_full_size_sampled_tokens():
+    """T=4096 tokens, 256 experts (dim 7168, inter 2048), top-8 Zipf(1.2)
+    routing on the device; the oracle recomputes two whole output rows from
+    its own quantisation of the experts those tokens use."""
+    T, E, dim, inter, k = 4096, 256, 7168, 2048, 8
+    dev = torch.device("cuda")
+    seed = synthetic.SEED_MOE
+    x = synthetic.device_activations(T, dim, seed, dev)
+    xq_d, xs_d = fb.act_quant(x)
+    idx, wts = synthetic.moe_routing(T, E, k, seed, zipf_s=1.2)
+
+    def expert_w(e, which):
+        shape = (inter, dim) if which < 2 else (dim, inter)
+        return synthetic.device_normal(shape, seed * 100000 + 3 * e + which, 0.02, dev)
+
+    stacks = []
+    for which in range(3):
+        qs, ss = zip(*[fb.weight_quant(expert_w(e, which)) for e in range(E)])
+        stacks.append((torch.cat(qs), torch.cat(ss)))
+    y = fb.moe_grouped_gemm(xq_d, xs_d, to_dev(idx), to_dev(wts), stacks[0][0], stacks[0][1], stacks[1][0],
+                            stacks[1][1], stacks[2][0], stacks[2][1], E)
+    tokens = [3, T - 1]
+    rows = torch.tensor(tokens, device=dev)
+    xq, xs = oracle.act_quant(dev_to_bits(x[rows]))
+    ref = []
+    for i, t in enumerate(tokens):
+        acc = np.zeros(dim)
+        for j in range(k):
+            e = idx[t, j]
+            wq = [oracle.weight_quant(expert_w(e, which).cpu().numpy()) for which in range(3)]
+            o = oracle.ffn_rows(xq[i:i + 1], xs[i:i + 1], *wq[0], *wq[1], *wq[2], [0])[0]
+            acc += np.float64(wts[t, j]) * synthetic.bf16_bits_to_f32(oracle.bf16_round(o))
+        ref.append(acc)
+    rms = float(y.float().pow(2).mean().sqrt())
+    assert_gemm_close(dev_to_bits(y)[tokens], np.array(ref), rms=rms, what="moe sampled tokens")
+    assert fb.last_device_error() == 0
