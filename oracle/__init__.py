@@ -77,6 +77,8 @@ def lib():
             L.orc_moe_permute.restype = i32
             L.orc_expert_ffn.argtypes = [vp] * 8 + [i64, i64, i32, vp]
             L.orc_expert_ffn.restype = i32
+            L.orc_expert_ffn_u.argtypes = [vp] * 8 + [i64, i64, i32, vp, vp, vp]
+            L.orc_expert_ffn_u.restype = i32
             L.orc_moe_token.argtypes = [vp, vp, vp, vp, i64, i64] + [vp] * 6 + [i64, i64, i32, vp]
             L.orc_moe_token.restype = i32
             L.orc_e4m3_encode_array.argtypes = [vp, i64, vp]
@@ -205,10 +207,11 @@ def swiglu(h1_bits, h3_bits) -> np.ndarray:
     return u
 
 
-def ffn_rows(xq, xs, w1q, w1s, w3q, w3s, w2q, w2s, rows, ue8m0=False):
+def ffn_rows(xq, xs, w1q, w1s, w3q, w3s, w2q, w2s, rows, ue8m0=False, return_u=False):
     """Dense SwiGLU FFN chain for the listed rows of an already-quantised x:
     h = bf16(w1 x), bf16(w3 x) -> swiglu -> act_quant -> fp64 product with w2.
-    Returns fp64 [len(rows), dim_out]."""
+    Returns fp64 [len(rows), dim_out]; with return_u also the quantised
+    intermediate (uq uint8 [len(rows), inter], us float32 [len(rows), inter/128])."""
     xq, xs = _c(xq, np.uint8), _c(xs, np.float32)
     w1q, w3q, w2q = _c(w1q, np.uint8), _c(w3q, np.uint8), _c(w2q, np.uint8)
     w1s, w3s, w2s = _c(w1s, np.float32), _c(w3s, np.float32), _c(w2s, np.float32)
@@ -216,7 +219,10 @@ def ffn_rows(xq, xs, w1q, w1s, w3q, w3s, w2q, w2s, rows, ue8m0=False):
     inter = w1q.shape[0]
     dout = w2q.shape[0]
     assert w2q.shape[1] == inter
+    rows = list(rows)
     out = np.empty((len(rows), dout), np.float64)
+    uq = np.empty((len(rows), inter), np.uint8)
+    us = np.empty((len(rows), inter // BLOCK), np.float32)
     L = lib()
     for i, r in enumerate(rows):
         o = np.empty(dout, np.float64)
@@ -224,12 +230,16 @@ def ffn_rows(xq, xs, w1q, w1s, w3q, w3s, w2q, w2s, rows, ue8m0=False):
         sr = np.ascontiguousarray(xs[r])
         if dout != dim:
             raise ValueError("the FFN maps dim -> dim")
-        rc = L.orc_expert_ffn(_ptr(xr), _ptr(sr), _ptr(w1q), _ptr(w1s), _ptr(w3q), _ptr(w3s),
-                              _ptr(w2q), _ptr(w2s), dim, inter, int(bool(ue8m0)), _ptr(o))
+        ur = np.empty(inter, np.uint8)
+        sr_u = np.empty(inter // BLOCK, np.float32)
+        rc = L.orc_expert_ffn_u(_ptr(xr), _ptr(sr), _ptr(w1q), _ptr(w1s), _ptr(w3q), _ptr(w3s),
+                                _ptr(w2q), _ptr(w2s), dim, inter, int(bool(ue8m0)), _ptr(o), _ptr(ur), _ptr(sr_u))
         if rc:
             raise MemoryError("oracle expert FFN failed")
         out[i] = o
-    return out
+        uq[i] = ur
+        us[i] = sr_u
+    return (out, uq, us) if return_u else out
 
 
 # ---- A5 MoE permutation --------------------------------------------------------

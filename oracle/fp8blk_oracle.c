@@ -309,11 +309,30 @@ int orc_moe_permute(const int32_t *idx, int64_t T, int64_t topk, int64_t E,
  * the w2 Linear, o [dim]. Scratch: 3*inter uint16 + inter bytes +
  * inter/128 floats, allocated here. Steps: h1 = bf16(w1 x), h3 = bf16(w3 x),
  * u = swiglu(h1, h3), (uq, us) = act_quant(u), o = fp64 product uq w2^T. */
+int orc_expert_ffn_u(const uint8_t *xq, const float *xs,
+                     const uint8_t *w1, const float *w1s,
+                     const uint8_t *w3, const float *w3s,
+                     const uint8_t *w2, const float *w2s,
+                     int64_t dim, int64_t inter, int ue8m0, double *o,
+                     uint8_t *uq_out, float *us_out);
+
 int orc_expert_ffn(const uint8_t *xq, const float *xs,
                    const uint8_t *w1, const float *w1s,
                    const uint8_t *w3, const float *w3s,
                    const uint8_t *w2, const float *w2s,
                    int64_t dim, int64_t inter, int ue8m0, double *o)
+{
+    return orc_expert_ffn_u(xq, xs, w1, w1s, w3, w3s, w2, w2s, dim, inter, ue8m0, o, NULL, NULL);
+}
+
+/* The same, also copying out the quantised intermediate u (uq_out: e4m3
+ * [inter], us_out: fp32 [inter/128]) when those pointers are not NULL. */
+int orc_expert_ffn_u(const uint8_t *xq, const float *xs,
+                     const uint8_t *w1, const float *w1s,
+                     const uint8_t *w3, const float *w3s,
+                     const uint8_t *w2, const float *w2s,
+                     int64_t dim, int64_t inter, int ue8m0, double *o,
+                     uint8_t *uq_out, float *us_out)
 {
     uint16_t *h1 = malloc(sizeof(uint16_t) * inter);
     uint16_t *h3 = malloc(sizeof(uint16_t) * inter);
@@ -332,6 +351,10 @@ int orc_expert_ffn(const uint8_t *xq, const float *xs,
     orc_act_quant(u, 1, inter, ue8m0, uq, us);
     for (int64_t c = 0; c < dim; ++c)
         o[c] = gemm_point(uq, us, w2, w2s, inter, 0, c);
+    if (uq_out)
+        memcpy(uq_out, uq, (size_t)inter);
+    if (us_out)
+        memcpy(us_out, us, sizeof(float) * (inter / ORC_BLOCK));
     free(h1); free(h3); free(u); free(uq); free(us);
     return 0;
 }

@@ -81,7 +81,7 @@ def device_normal(shape, seed: int, std: float, device, dtype=None):
     import torch
 
     g = torch.Generator(device=device)
-    g.manual_seed(seed)
+    g.manual_seed(int(seed))
     t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
     t.mul_(std)
     return t if dtype is None else t.to(dtype)
@@ -94,7 +94,7 @@ def device_activations(M: int, K: int, seed: int, device, outlier_frac: float = 
     import torch
 
     g = torch.Generator(device=device)
-    g.manual_seed(seed)
+    g.manual_seed(int(seed))
     x = torch.randn((M, K), generator=g, device=device, dtype=torch.float32)
     ch = outlier_channels(K, seed, outlier_frac)
     if ch.size:
