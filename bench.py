@@ -58,6 +58,9 @@ WORKLOADS = {
     "attn_wq_b_m64": ("linear", dict(M=64, N=24576, K=1536, frac=0.0, seed=synthetic.SEED_ATTN)),
     "attn_wkv_b_m64": ("linear", dict(M=64, N=32768, K=512, frac=0.0, seed=synthetic.SEED_ATTN)),
     "weight_dequant_18432x7168": ("dequant", dict(N=18432, K=7168, seed=synthetic.SEED_ATTN)),
+    "prefill_ffn_4096": ("ffn", dict(M=4096, dim=7168, inter=18432, seed=synthetic.SEED_PREFILL)),
+    "moe_t4096_uniform": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, seed=synthetic.SEED_MOE)),
+    "moe_t4096_zipf": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=1.2, seed=synthetic.SEED_MOE)),
 }
 DEFAULT = "decode_linear_m8"
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
@@ -82,13 +85,19 @@ def parse():
 # ---------------------------------------------------------------------------
 
 def linear_bytes(M, N, K):
-    """Bytes one FP8 linear step must move: act_quant (read x bf16, write q and
-    scales) and fp8_gemm (read q, scales, the weight and its scales, write C)."""
+    """Bytes the FP8 linear layer must move, whatever the kernels: read x
+    (bf16), the e4m3 weight and its 128x128 scales, write y (bf16)."""
     kb = K // 128
     nb = -(-N // 128)
-    aq = M * K * 2 + M * K + M * kb * 4
-    gemm = M * K + M * kb * 4 + N * K + nb * kb * 4 + M * N * 2
-    return aq, gemm
+    return M * K * 2 + N * K + nb * kb * 4 + M * N * 2
+
+
+def gemm_kernel_bytes(M, N, K):
+    """Bytes of the stand-alone fp8_gemm kernel: the quantised activation and
+    its scales, the weight and its scales, the bf16 output."""
+    kb = K // 128
+    nb = -(-N // 128)
+    return M * K + M * kb * 4 + N * K + nb * kb * 4 + M * N * 2
 
 
 def linear_flops(M, N, K):
@@ -339,29 +348,35 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     clocks = clk.summary(t0, t1)
     assert fb.last_device_error(dev) == 0, "a kernel reported a wait timeout"
 
-    aq_b, gemm_b = linear_bytes(M, N, K)
-    step_bytes = aq_b + gemm_b
+    # M <= 2: fp8blk_linear is one kernel (act_quant fused into the GEMM);
+    # otherwise act_quant then fp8_gemm.
+    fused = M <= 2
+    step_bytes = linear_bytes(M, N, K)
+    gemm_b = gemm_kernel_bytes(M, N, K)
     flops = linear_flops(M, N, K)
     el_max, units = reduce_over_ranks(el, steps * step_bytes, dev)
-    hbm_bound = flops / (aq_b + gemm_b) < 400
+    hbm_bound = flops / step_bytes < 400
     gemm_s = el_gemm / steps
+    kern_s, kern_b = (el / steps, step_bytes) if fused else (gemm_s, gemm_b)
+    kern_name = "fp8blk_linear (act_quant fused into the GEMM)" if fused else "fp8_gemm"
     if hbm_bound:
         metric_val = units / el_max / 1e9
         unit = "GB/s"
-        achieved = gemm_b / gemm_s / 1e9
+        achieved = kern_b / kern_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm"], "peak_source": f"hbm_gbs ({peaks['src']})"}
     else:
         metric_val = steps * flops * world / el_max / 1e12
         unit = "TFLOP/s"
         peak = peaks["bf16"] * FP8_OVER_BF16
-        achieved = flops / gemm_s / 1e12
+        achieved = flops / kern_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "peak_source": f"bf16_tflops ({peaks['src']}) x {FP8_OVER_BF16} nominal fp8/bf16 ratio"}
-    roof["traffic"] = recorded_traffic(args.workload, "fp8_gemm")
-    roof["algorithmic_bytes_per_launch"] = gemm_b
-    roof["kernel_us"] = gemm_s * 1e6
+    roof["kernel"] = kern_name
+    roof["traffic"] = recorded_traffic(args.workload, "linear_fused" if fused else "fp8_gemm")
+    roof["algorithmic_bytes_per_launch"] = kern_b
+    roof["kernel_us"] = kern_s * 1e6
 
     e2e = None
     if not args.no_e2e:
@@ -370,8 +385,9 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     out = {
         "value": metric_val, "unit": unit, "ms_per_step": el_max / steps * 1e3,
         "clocks": clocks, "roofline": roof, "e2e": e2e,
-        "gpu_launches": 2 * steps,
-        "kernels_us": {"act_quant": el_aq / steps * 1e6, "fp8_gemm": gemm_s * 1e6},
+        "gpu_launches": (1 if fused else 2) * steps,
+        "kernels_us": {"linear_step": el / steps * 1e6, "act_quant_alone": el_aq / steps * 1e6,
+                       "fp8_gemm_alone": gemm_s * 1e6},
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "outlier_channels": frac,
                    "x": "bf16 N(0,1)", "w": "e4m3 from N(0,0.02), fp32 128x128 block scales",
                    "l2": f"weights rotate over {R} copies ({R * w_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
@@ -408,6 +424,126 @@ def run_e2e(shape, dev, torch, fb, q, s, n, hbm_bound, step_bytes, flops):
     return {"value": val, "unit": "GB/s" if hbm_bound else "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
             "d2h_bytes_per_step": M * N * 2, "steps": n, "ms_per_step": el / n * 1e3,
             "api": "fp8blk_linear_host (pinned host buffers)"}
+
+
+def run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
+    """Dense SwiGLU FFN: act_quant(x), the fused w1/w3 GEMM (SwiGLU + act_quant
+    epilogue), the w2 GEMM. Tensor-bound: 3 * 2 * M * dim * inter flops."""
+    M, dim, inter, seed = shape["M"], shape["dim"], shape["inter"], shape["seed"]
+    x = synthetic.device_activations(M, dim, seed, dev)
+    sets = []
+    for c in range(2):   # two weight copies: 792 MB > 3x L2 between consecutive steps
+        ws_ = [synthetic.device_normal(sh, seed + 10 + i, 0.02, dev) for i, sh in
+               enumerate([(inter, dim), (inter, dim), (dim, inter)])]
+        sets.append([fb.weight_quant(w) for w in ws_])
+        del ws_
+    y = torch.empty((M, dim), dtype=torch.bfloat16, device=dev)
+    xq, xs = fb.act_quant(x)
+    wsp = fb.workspace(0, dev, "ffn")
+
+    def step(i):
+        (q1, s1), (q3, s3), (q2, s2) = sets[i % 2]
+        fb.ffn(x, q1, s1, q3, s3, q2, s2, out=y)
+
+    def swiglu_only(i):
+        (q1, s1), (q3, s3), _ = sets[i % 2]
+        fb.swiglu_gemm(xq, xs, q1, s1, q3, s3)
+
+    for i in range(3):
+        step(i)
+        swiglu_only(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    g_warm = make_runs(step, warmup, 10, torch, args.eager)
+    g_main = make_runs(step, steps, 10, torch, args.eager)
+    g_swi = make_runs(swiglu_only, steps, 10, torch, args.eager)
+    for g in g_warm:
+        g.replay()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        el, t0, t1 = timed_replay(g_main, stream, torch)
+        el_swi, _, _ = timed_replay(g_swi, stream, torch)
+    assert fb.last_device_error(dev) == 0
+    flops = 3 * 2.0 * M * dim * inter
+    el_max, units = reduce_over_ranks(el, steps * flops, dev)
+    peak = peaks["bf16"] * FP8_OVER_BF16
+    swi_flops = 2 * 2.0 * M * dim * inter
+    achieved = swi_flops / (el_swi / steps) / 1e12
+    del wsp
+    return {
+        "value": units / el_max / 1e12, "unit": "TFLOP/s", "ms_per_step": el_max / steps * 1e3,
+        "clocks": clk.summary(t0, t1), "gpu_launches": 3 * steps,
+        "roofline": {"bound": "tensor", "kernel": "fused w1/w3 GEMM + SwiGLU + act_quant", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic(args.workload, "swiglu_gemm"),
+                     "peak_source": f"bf16_tflops ({peaks['src']}) x {FP8_OVER_BF16} nominal fp8/bf16 ratio",
+                     "kernel_us": el_swi / steps * 1e6},
+        "e2e": None, "kernels_us": {"swiglu_gemm": el_swi / steps * 1e6},
+        "config": {"workload": args.workload, "M": M, "dim": dim, "inter": inter,
+                   "l2": "two weight sets (792 MB) alternate between steps"},
+        "dtype": "e4m3 x e4m3 -> f32 accumulate; SwiGLU in fp32/bf16; e4m3 re-quantisation",
+    }
+
+
+def moe_weight_bytes(E_touched, dim, inter):
+    kbd, kbi = dim // 128, inter // 128
+    return E_touched * (2 * inter * dim + dim * inter + 4 * (2 * (inter // 128) * kbd + (dim // 128) * kbi))
+
+
+def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
+    """Routed experts: permutation, gather, grouped w1/w3 GEMM with the SwiGLU
+    + act_quant epilogue, grouped w2 GEMM scattered to slots, weighted combine.
+    HBM-bound on the touched experts' weights at this token count."""
+    T, E, dim, inter, k, seed = (shape[n] for n in ("T", "E", "dim", "inter", "k", "seed"))
+    x = synthetic.device_activations(T, dim, seed, dev)
+    xq, xs = fb.act_quant(x)
+    idx_np, w_np = synthetic.moe_routing(T, E, k, seed, zipf_s=shape["zipf"])
+    idx = torch.from_numpy(idx_np).to(dev)
+    wts = torch.from_numpy(w_np).to(dev)
+    stacks = []
+    for which in range(3):
+        sh = (inter, dim) if which < 2 else (dim, inter)
+        qs, ss = zip(*[fb.weight_quant(synthetic.device_normal(sh, seed * 100000 + 3 * e + which, 0.02, dev))
+                       for e in range(E)])
+        stacks.append((torch.cat(qs), torch.cat(ss)))
+        del qs, ss
+    y = torch.empty((T, dim), dtype=torch.bfloat16, device=dev)
+    (q1, s1), (q3, s3), (q2, s2) = stacks
+
+    def step(i):
+        fb.moe_grouped_gemm(xq, xs, idx, wts, q1, s1, q3, s3, q2, s2, E, out=y)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    g_warm = make_runs(step, warmup, 10, torch, args.eager)
+    g_main = make_runs(step, steps, 10, torch, args.eager)
+    for g in g_warm:
+        g.replay()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        el, t0, t1 = timed_replay(g_main, stream, torch)
+    assert fb.last_device_error(dev) == 0
+    touched = int(np.unique(idx_np).size)
+    b = moe_weight_bytes(touched, dim, inter) + T * dim + T * (dim // 128) * 4 + T * dim * 2 + T * k * 8
+    flops = 3 * 2.0 * T * k * dim * inter
+    el_max, units = reduce_over_ranks(el, steps * b, dev)
+    achieved = b / (el / steps) / 1e9
+    return {
+        "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
+        "tflops": steps * flops / el / 1e12,
+        "clocks": clk.summary(t0, t1), "gpu_launches": 5 * steps,
+        "roofline": {"bound": "hbm", "kernel": "whole routed-expert step (5 kernels)", "achieved": achieved,
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
+                     "traffic": recorded_traffic(args.workload, "moe_step"),
+                     "peak_source": f"hbm_gbs ({peaks['src']})", "algorithmic_bytes_per_launch": b},
+        "e2e": None,
+        "config": {"workload": args.workload, "T": T, "E": E, "dim": dim, "inter": inter, "topk": k,
+                   "routing": "Zipf(1.2)" if shape["zipf"] else "uniform", "experts_touched": touched,
+                   "l2": f"{touched} experts' weights ({moe_weight_bytes(touched, dim, inter) / 1e9:.2f} GB) per step"},
+        "dtype": "e4m3 x e4m3 -> f32 accumulate; SwiGLU in fp32/bf16; e4m3 re-quantisation",
+    }
 
 
 def run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
@@ -473,9 +609,8 @@ def oracle_linear_sample(shape, n_cols: int):
     xq, xs = oracle.act_quant(x)
     oracle.gemm(xq, xs, wq[:n_cols], ws[: -(-n_cols // 128)])
     dt = time.perf_counter() - t0
-    aq_b, _ = linear_bytes(M, N, K)
     kb = K // 128
-    b = aq_b + M * K + M * kb * 4 + n_cols * K + (-(-n_cols // 128)) * kb * 4 + M * n_cols * 2
+    b = M * K * 2 + n_cols * K + (-(-n_cols // 128)) * kb * 4 + M * n_cols * 2
     return dt, b
 
 
@@ -541,7 +676,7 @@ def run_reference(args, kind, shape, steps, warmup):
 def main():
     args = parse()
     kind, shape = WORKLOADS[args.workload]
-    big = kind == "linear" and shape["M"] >= 2048 or kind == "dequant"
+    big = kind == "linear" and shape["M"] >= 2048 or kind in ("dequant", "ffn", "moe")
     steps = args.steps if args.steps is not None else (200 if big else 100000)
     warmup = args.warmup if args.warmup is not None else (10 if big else 1000)
     if warmup < 3:
@@ -565,6 +700,10 @@ def main():
     peaks = load_peaks()
     if kind == "linear":
         res = run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
+    elif kind == "ffn":
+        res = run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
+    elif kind == "moe":
+        res = run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     else:
         res = run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     cpu = None
@@ -580,8 +719,9 @@ def main():
             "clocks": res["clocks"], "roofline": res["roofline"], "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "cpu_baseline": cpu,
         }
-        if "kernels_us" in res:
-            line["kernels_us"] = res["kernels_us"]
+        for extra in ("kernels_us", "tflops"):
+            if extra in res:
+                line[extra] = res[extra]
         print(json.dumps(line))
     if world > 1:
         dist.barrier()

@@ -16,6 +16,10 @@ namespace fp8blk {
 __device__ unsigned g_device_error_word;
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int act_quant_launch(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* s, int scale_fmt,
+                     cudaStream_t stream, bool trigger);
+int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, int64_t M, int64_t N, int64_t K,
+                     int scale_fmt, cudaStream_t stream, bool* used);
 int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
              int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
@@ -52,6 +56,8 @@ void init_device(int dev) {
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
+
+constexpr int64_t kFusedLinearMaxM = 2;
 
 }  // namespace
 
@@ -116,6 +122,15 @@ extern "C" int fp8blk_linear(const void* x_bf16, const void* w_e4m3, const float
                              fp8blk_stream_t stream) {
   if (M < 0 || N < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
   if (M == 0 || N == 0) return FP8BLK_OK;
+  // M <= 2: act_quant runs inside the GEMM kernel (one launch). For larger M
+  // its in-kernel cost (every CTA quantises all of x) exceeds the launch it
+  // saves, so act_quant is a kernel of its own.
+  if (M <= kFusedLinearMaxM) {
+    bool used = false;
+    const int st = linear_fused_run(x_bf16, w_e4m3, w_s, y_bf16, M, N, K, scale_fmt,
+                                    reinterpret_cast<cudaStream_t>(stream), &used);
+    if (st || used) return st;
+  }
   if (!workspace) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   const size_t need = fp8blk_linear_workspace_bytes(M, N, K);
@@ -124,7 +139,8 @@ extern "C" int fp8blk_linear(const void* x_bf16, const void* w_e4m3, const float
   uint8_t* xq = ws;
   float* xs = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(M) * K));
   uint8_t* gws = ws + align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / kBlock) * 4);
-  if (int st = fp8blk_act_quant(x_bf16, M, K, xq, xs, scale_fmt, stream)) return st;
+  if (int st = act_quant_launch(x_bf16, M, K, xq, xs, scale_fmt, reinterpret_cast<cudaStream_t>(stream), true))
+    return st;
   return gemm_run(xq, xs, w_e4m3, w_s, y_bf16, M, N, K, scale_fmt, gws, workspace_bytes - (gws - ws),
                   reinterpret_cast<cudaStream_t>(stream));
 }

@@ -79,7 +79,10 @@ struct GemmParams {
   int sk_tiles;        // the remaining tiles run stream-K
   long long sk_iters;  // sk_tiles * Kb
   int vec_store;       // C rows 16-byte aligned and N % 8 == 0
-  int ue8m0;           // SwiGLU: power-of-two scales for the fused act_quant
+  int ue8m0;           // power-of-two scales for a fused act_quant (SwiGLU output, decode input)
+  int whole_tiles;     // > 0: that many whole tiles, round-robin over the CTAs (no stream-K)
+  const __nv_bfloat16* x;  // fused decode linear: the bf16 activation [M, Kb * 128]
+  int trace_id;        // phase-trace builds only: which of 8 trace slots this launch fills
 };
 
 namespace {
@@ -97,7 +100,8 @@ struct Sched {
   int grouped_total;  // grouped GEMM: tile count read on the device (-1: dense)
 
   __device__ Sched(const GemmParams& prm, int cta, int grouped_tiles = -1)
-      : p(prm), c(cta), j(0), grouped_total(grouped_tiles) {
+      : p(prm), c(cta), j(0), grouped_total(grouped_tiles >= 0 ? grouped_tiles
+                                                               : (prm.whole_tiles > 0 ? prm.whole_tiles : -1)) {
     it = static_cast<long long>(c) * p.sk_iters / p.grid;
     it_end = static_cast<long long>(c + 1) * p.sk_iters / p.grid;
   }
@@ -147,8 +151,17 @@ constexpr int pow2_at_least(int v, int floor_) {
   return p;
 }
 
-template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_, int MODE_ = kEpiBf16, bool GROUPED_ = false>
+#ifndef FP8BLK_DECODE_L2_AHEAD
+#define FP8BLK_DECODE_L2_AHEAD 0
+#endif
+
+template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_, int MODE_ = kEpiBf16, bool GROUPED_ = false,
+          bool FUSED_ = false>
 struct Cfg {
+  // FUSED: decode linear with act_quant inside -- the CTA quantises the bf16
+  // activation itself into a resident shared-memory operand (all K blocks),
+  // and only the weights stream through the stage ring.
+  static constexpr bool FUSED = FUSED_;
   static constexpr int BN = BN_;
   static constexpr bool SWAP = SWAP_;
   static constexpr int STAGES = STAGES_;
@@ -167,15 +180,20 @@ struct Cfg {
   static constexpr int kCpt = BN / kGroups;      // columns per epilogue thread
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStageBytes = FUSED ? kABytes : kABytes + kBBytes;
+  // Decode tiles: weight chunks beyond the stage ring that are prefetched into
+  // L2 before the dependency wait, so the whole weight tile streams from DRAM
+  // while the previous kernel finishes.
+  static constexpr int kL2Ahead = SWAP ? FP8BLK_DECODE_L2_AHEAD : 0;
   static constexpr int kTmemCols = pow2_at_least(P * BN, 32);
-  static constexpr int kBarBytes = (2 * STAGES + 2 * P + 2) * 8 + 16;
+  static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16;
   static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + kGroupBytes + kXchgBytes;
 
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(MODE == kEpiBf16 || !SWAP, "SwiGLU and scatter epilogues use activation rows as lanes");
   static_assert(MODE != kEpiSwiGLU || (BN == 256 && EPI_WARPS == 8), "SwiGLU: w1|w3 128+128 columns");
   static_assert(!GROUPED || !SWAP, "grouped GEMMs use activation rows as lanes");
+  static_assert(!FUSED || (SWAP && BN <= 32 && MODE == kEpiBf16 && !GROUPED), "fused act_quant: decode tiles");
   static_assert(EPI_WARPS % 4 == 0, "epilogue warps come in warpgroups");
   static_assert(kCpt == 16 || kCpt % 32 == 0, "TMEM loads of 16 or 32 columns");
   static_assert(SWAP || kCpt == 128, "non-swapped tiles: one weight block per column group");
@@ -331,26 +349,57 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
   }
 }
 
+// Optional phase trace (compile with -DFP8BLK_TRACE): %globaltimer stamps per
+// CTA at fixed points of each role, read back with fp8trace_read(). Not part
+// of the library's interface; default builds contain none of it.
+#ifdef FP8BLK_TRACE
+constexpr int kTraceSlots = 16;
+__device__ unsigned long long g_trace[8 * 4096 * kTraceSlots];
+#define FP8BLK_STAMP(slot)                                                                               \
+  do {                                                                                                   \
+    if (blockIdx.x < 4096)                                                                               \
+      g_trace[((prm.trace_id & 7) * 4096 + blockIdx.x) * kTraceSlots + (slot)] = global_timer_ns();       \
+  } while (0)
+#else
+#define FP8BLK_STAMP(slot) do { } while (0)
+#endif
+
+// Shared memory of the fused decode operand: Kb blocks of BN rows x 128
+// e4m3, then Kb x BN fp32 scales.
+__host__ __device__ constexpr size_t fused_extra_bytes(int Kb, int BN) {
+  return static_cast<size_t>(Kb) * BN * 128 + ((static_cast<size_t>(Kb) * BN * 4 + 15) & ~size_t{15});
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_lane, const __grid_constant__ CUtensorMap tmap_col,
                     const __grid_constant__ CUtensorMap tmap_col2, const GemmParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::kStageBytes);
+  // Fused decode: the quantised activation (all K blocks, BN token rows each,
+  // 128-byte swizzled like a TMA tile) and its scales follow the stage ring.
+  uint8_t* act_smem = smem + C::STAGES * C::kStageBytes;
+  float* act_scale = reinterpret_cast<float*>(act_smem + static_cast<size_t>(prm.Kb) * C::BN * 128);
+  uint8_t* tail = act_smem + (C::FUSED ? fused_extra_bytes(prm.Kb, C::BN) : 0);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tail);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + C::P;
   uint64_t* drain = tempty + C::P;
-  uint64_t* epi_bar = drain + 1;  // epilogue-only barrier (stream-K fixup, SwiGLU amax exchange)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
+  uint64_t* epi_bar = drain + 1;    // epilogue-only barrier (stream-K fixup, SwiGLU amax exchange)
+  uint64_t* act_ready = epi_bar + 1;  // fused decode: activation operand written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(act_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
-  int* grp_rows = reinterpret_cast<int*>(smem + C::STAGES * C::kStageBytes + C::kBarBytes);
+  int* grp_rows = reinterpret_cast<int*>(tail + C::kBarBytes);
   int* grp_mtiles = grp_rows + (kMaxGroups + 4);
-  float* xchg = reinterpret_cast<float*>(smem + C::STAGES * C::kStageBytes + C::kBarBytes + C::kGroupBytes);
+  float* xchg = reinterpret_cast<float*>(tail + C::kBarBytes + C::kGroupBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) FP8BLK_STAMP(0);
+  // The next kernel on the stream may begin its prologue (and its weight
+  // loads) now; it waits for this one before touching anything we write.
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -363,6 +412,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(epi_bar, C::EPI_WARPS);
+    mbar_init(act_ready, C::EPI_WARPS);
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -379,6 +429,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   }
   int grouped_tiles = -1;
   if constexpr (C::GROUPED) {
+    griddep_wait();  // the group tables come from the previous kernel
     for (int i = threadIdx.x; i <= prm.E; i += C::kThreads) {
       grp_rows[i] = __ldg(prm.grp_rows + i);
       grp_mtiles[i] = __ldg(prm.grp_mtiles + i);
@@ -388,11 +439,60 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) FP8BLK_STAMP(1);
   if constexpr (C::GROUPED) grouped_tiles = grp_mtiles[prm.E] * prm.tiles_col;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      // The weight operand is the lane operand when swapped, else the column one.
+      auto load_weights = [&](int st, const TileInfo& t, int kb) {
+        uint8_t* sa = smem + st * C::kStageBytes;
+        if constexpr (C::SWAP) {
+          tma_load_2d(sa, &tmap_lane, &full[st], kb * 128, t.lane_y);
+        } else if constexpr (C::MODE == kEpiSwiGLU) {
+          // Column rows [0,64) w1, [64,128) w3, [128,192) w1 + 64, [192,256) w3 + 64.
+          uint8_t* sb = sa + C::kABytes;
+          tma_load_2d(sb, &tmap_col, &full[st], kb * 128, t.col_y);
+          tma_load_2d(sb + 64 * 128, &tmap_col2, &full[st], kb * 128, t.col_y);
+          tma_load_2d(sb + 128 * 128, &tmap_col, &full[st], kb * 128, t.col_y + 64);
+          tma_load_2d(sb + 192 * 128, &tmap_col2, &full[st], kb * 128, t.col_y + 64);
+        } else {
+          tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, t.col_y);
+        }
+      };
+      auto load_acts = [&](int st, const TileInfo& t, int kb) {
+        if constexpr (C::FUSED) return;  // the epilogue warps build the activation operand
+        uint8_t* sa = smem + st * C::kStageBytes;
+        if constexpr (C::SWAP) tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, t.col_y);
+        else tma_load_2d(sa, &tmap_lane, &full[st], kb * 128, t.lane_y);
+      };
+      // Weights do not depend on the previous kernel on the stream: the first
+      // STAGES stages start loading them before the dependency wait; the
+      // activations follow once the previous kernel has completed.
+      int npre = 0;
+      if constexpr (!C::GROUPED) {
+        Sched pre(prm, blockIdx.x);
+        Unit u;
+        int nl2 = 0;
+        while ((npre < C::STAGES || nl2 < C::kL2Ahead) && pre.next(u)) {
+          const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles);
+          for (int kb = u.kb0; kb < u.kb1; ++kb) {
+            if (npre < C::STAGES) {
+              mbar_arrive_expect_tx(&full[npre], C::kStageBytes);
+              load_weights(npre, t, kb);
+              ++npre;
+            } else if (nl2 < C::kL2Ahead) {
+              if constexpr (C::SWAP) tma_prefetch_l2_2d(&tmap_lane, kb * 128, t.lane_y);
+              ++nl2;
+            } else {
+              break;
+            }
+          }
+        }
+      }
+      griddep_wait();
+      FP8BLK_STAMP(2);
       Sched sch(prm, blockIdx.x, grouped_tiles);
       Unit u;
       int st = 0;
@@ -402,22 +502,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       while (ok && sch.next(u)) {
         const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, prm.err, kDevErrTimeoutProducer)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-          uint8_t* sa = smem + st * C::kStageBytes;
-          tma_load_2d(sa, &tmap_lane, &full[st], kb * 128, t.lane_y);
-          if constexpr (C::MODE == kEpiSwiGLU) {
-            // Column rows [0,64) w1, [64,128) w3, [128,192) w1 + 64, [192,256) w3 + 64.
-            uint8_t* sb = sa + C::kABytes;
-            tma_load_2d(sb, &tmap_col, &full[st], kb * 128, t.col_y);
-            tma_load_2d(sb + 64 * 128, &tmap_col2, &full[st], kb * 128, t.col_y);
-            tma_load_2d(sb + 128 * 128, &tmap_col, &full[st], kb * 128, t.col_y + 64);
-            tma_load_2d(sb + 192 * 128, &tmap_col2, &full[st], kb * 128, t.col_y + 64);
+          if (issued < npre) {
+            load_acts(st, t, kb);  // stage st == issued: weights already on their way
           } else {
-            tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, t.col_y);
+            if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, prm.err, kDevErrTimeoutProducer)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+            load_weights(st, t, kb);
+            load_acts(st, t, kb);
+#ifdef FP8BLK_TRACE
+            if (issued == C::STAGES) FP8BLK_STAMP(10);
+            FP8BLK_STAMP(11);
+#endif
           }
           ++issued;
           if (++st == C::STAGES) {
@@ -445,6 +543,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       int st = 0, pb = 0;
       uint32_t ph = 0, pph = 0;
       bool ok = true;
+      if constexpr (C::FUSED) ok = mbar_wait(act_ready, 0, abort_flag, prm.err, kDevErrTimeoutMma);
       while (ok && sch.next(u)) {
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(&full[st], ph, abort_flag, prm.err, kDevErrTimeoutMma) ||
@@ -453,9 +552,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             break;
           }
           tc_fence_after_sync();
+#ifdef FP8BLK_TRACE
+          if (st == 0 && ph == 0 && pb == 0) FP8BLK_STAMP(3);
+          if (st == 0 && ph == 1) FP8BLK_STAMP(12);
+#endif
           const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
           const uint64_t ad = sdesc_kmajor_sw128(a_addr);
-          const uint64_t bd = sdesc_kmajor_sw128(a_addr + C::kABytes);
+          const uint64_t bd = C::FUSED ? sdesc_kmajor_sw128(smem_u32(act_smem + kb * (C::BN * 128)))
+                                       : sdesc_kmajor_sw128(a_addr + C::kABytes);
           const uint32_t d = tmem_base + static_cast<uint32_t>(pb * C::BN);
 #pragma unroll
           for (int k = 0; k < 4; ++k)  // 32-byte K slices: start address advances by 32 B (2 x 16 B)
@@ -472,6 +576,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
       }
+      FP8BLK_STAMP(4);
       // Wait for every MMA this thread issued before TMEM is released.
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr, prm.err, kDevErrTimeoutDrain);
@@ -496,6 +601,115 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       return r;
     };
 
+    griddep_wait();  // activation scales and every output are the previous kernel's business
+    if (threadIdx.x == 64) FP8BLK_STAMP(5);
+    if constexpr (C::FUSED) {
+      // act_quant of x [M, K] into the resident MMA operand: the act_quant rule
+      // per (row, 128 columns) -- amax, max(amax, 1e-4) / 448 (ue8m0: rounded
+      // up to 2^k), codes e4m3(x / s) -- one 128-element block per 16 lanes.
+      // Rows M..BN-1 of the operand are zero. Layout: block kb at kb*BN*128,
+      // row m at (m / 8) * 1024 + (m % 8) * 128, its 16-byte chunk c stored at
+      // chunk c ^ (m % 8) (the 128-byte swizzle the descriptors name).
+      const int et = threadIdx.x - 64;  // 0 .. 127
+      const int sub = et & 15, hw = et >> 4;
+      const int total = prm.M * prm.Kb;
+      const int K = prm.Kb * 128;
+      // Up to kQb blocks per half-warp are loaded before any is used, so their
+      // L2/DRAM round trips overlap.
+      constexpr int kQb = 16;
+      constexpr int kPass = C::EPI_WARPS * 2;  // half-warps
+      for (int base = 0; base < total; base += kPass * kQb) {
+        uint4 v[kQb];
+#pragma unroll
+        for (int q = 0; q < kQb; ++q) {
+          const int b = base + q * kPass + hw;
+          const int m = b / prm.Kb, kb = b - m * prm.Kb;
+          v[q] = b < total ? __ldg(reinterpret_cast<const uint4*>(prm.x + static_cast<size_t>(m) * K + kb * 128) +
+                                   sub)
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < kQb; ++q) {
+          const int b = base + q * kPass + hw;
+          if (base + q * kPass >= total) break;  // uniform over the warp: no block of this pass exists
+          const bool valid = b < total;
+          const int m = valid ? b / prm.Kb : 0, kb = valid ? b - m * prm.Kb : 0;
+          const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+          float f[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+          }
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+          for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off, 16));
+          const float sc = quant_block_scale(amax, prm.ue8m0 != 0);
+          const uint32_t lo = pack_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc),
+                                          __fdiv_rn(f[3], sc));
+          const uint32_t hi = pack_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc),
+                                          __fdiv_rn(f[7], sc));
+          if (valid) {
+            uint8_t* rowp = act_smem + kb * (C::BN * 128) + (m >> 3) * 1024 + (m & 7) * 128;
+            *reinterpret_cast<uint2*>(rowp + (((sub >> 1) ^ (m & 7)) << 4) + (sub & 1) * 8) = make_uint2(lo, hi);
+            if (sub == 0) act_scale[kb * C::BN + m] = sc;
+          }
+        }
+      }
+      // zero rows M..BN-1 (16 bytes per thread per step) and their scales
+      const int pad_rows = C::BN - prm.M;
+      for (int i = et; i < pad_rows * prm.Kb * 8; i += C::EPI_WARPS * 32) {
+        const int r = prm.M + i / (prm.Kb * 8), rem = i % (prm.Kb * 8);
+        const int kb = rem >> 3, chunk = rem & 7;
+        *reinterpret_cast<uint4*>(act_smem + kb * (C::BN * 128) + (r >> 3) * 1024 + (r & 7) * 128 + chunk * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int i = et; i < pad_rows * prm.Kb; i += C::EPI_WARPS * 32)
+        act_scale[(i % prm.Kb) * C::BN + prm.M + i / prm.Kb] = 0.0f;
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+      named_barrier_sync(1, C::EPI_WARPS * 32);
+      if (lane == 0) mbar_arrive(act_ready);
+      if (threadIdx.x == 64) FP8BLK_STAMP(6);
+    }
+    // Raw scale loads of one K block, issued kAhead blocks before their use so
+    // that their L2 round trips overlap the MMAs of the blocks in between.
+    constexpr int kColRegs = (C::SWAP && !C::FUSED) ? kAsRegs : 1;
+    struct ScaleRaw {
+      float a, w, w3;
+      float col[kColRegs];
+    };
+    constexpr int kAhead = C::EPI_WARPS == 8 ? 3 : 4;
+    auto load_scales = [&](const TileInfo& t, int kb, int kb_end) -> ScaleRaw {
+      ScaleRaw r;
+      r.a = r.w = r.w3 = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kColRegs; ++i) r.col[i] = 0.0f;
+      if (kb >= kb_end) return r;
+      if constexpr (!C::SWAP) {
+        if (row < t.lane_valid) r.a = __ldg(prm.a_s + static_cast<size_t>(t.lane_y + row) * prm.Kb + kb);
+        if constexpr (C::MODE == kEpiSwiGLU) {
+          r.w = __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
+          r.w3 = __ldg(prm.w3_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
+        } else {
+          const int nb = t.wblock + group;
+          if (C::GROUPED || nb < prm.n_wblocks) r.w = __ldg(prm.w_s + static_cast<size_t>(nb) * prm.Kb + kb);
+        }
+      } else {
+        r.w = __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
+        if constexpr (!C::FUSED) {
+#pragma unroll
+          for (int i = 0; i < kColRegs; ++i) {
+            const int j = lane + 32 * i;
+            const int m = t.col0 + j;
+            if (j < C::kCpt && m < prm.M) r.col[i] = __ldg(prm.a_s + static_cast<size_t>(m) * prm.Kb + kb);
+          }
+        }
+      }
+      return r;
+    };
+
     Sched sch(prm, blockIdx.x, grouped_tiles);
     Unit u;
     int pb = 0;
@@ -507,39 +721,42 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       float acc[C::kCpt];
 #pragma unroll
       for (int i = 0; i < C::kCpt; ++i) acc[i] = 0.0f;
+      ScaleRaw pipe[kAhead];
+#pragma unroll
+      for (int d = 0; d < kAhead; ++d) pipe[d] = load_scales(t, u.kb0 + d, u.kb1);
 
       for (int kb = u.kb0; kb < u.kb1; ++kb) {
-        // Scales of this K block, loaded before the wait to hide their latency.
-        // sc_lo applies to the first half of the thread's columns, sc_hi to the
-        // second (they differ only in SwiGLU mode: w1 vs w3 scales).
+        // Scales of this K block: loaded kAhead blocks earlier (the shifting
+        // window `pipe`), multiplied here. sc_lo applies to the first half of
+        // the thread's columns, sc_hi to the second (they differ only in
+        // SwiGLU mode: w1 vs w3 scales).
+        const ScaleRaw cur = pipe[0];
+#pragma unroll
+        for (int d = 0; d + 1 < kAhead; ++d) pipe[d] = pipe[d + 1];
+        pipe[kAhead - 1] = load_scales(t, kb + kAhead, u.kb1);
         float sc_lo = 0.0f, sc_hi = 0.0f;
         float sc_col[kAsRegs];
         if constexpr (!C::SWAP) {
-          const float as =
-              (row < t.lane_valid) ? __ldg(prm.a_s + static_cast<size_t>(t.lane_y + row) * prm.Kb + kb) : 0.0f;
-          if constexpr (C::MODE == kEpiSwiGLU) {
-            sc_lo = as * __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
-            sc_hi = as * __ldg(prm.w3_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
-          } else {
-            const int nb = t.wblock + group;
-            const bool wv = C::GROUPED || nb < prm.n_wblocks;
-            sc_lo = wv ? as * __ldg(prm.w_s + static_cast<size_t>(nb) * prm.Kb + kb) : 0.0f;
-            sc_hi = sc_lo;
-          }
+          sc_lo = cur.a * cur.w;
+          sc_hi = C::MODE == kEpiSwiGLU ? cur.a * cur.w3 : sc_lo;
         } else {
-          const float ws = __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
 #pragma unroll
           for (int i = 0; i < kAsRegs; ++i) {
             const int j = lane + 32 * i;
-            const int m = t.col0 + j;
-            sc_col[i] = (j < C::kCpt && m < prm.M) ? __ldg(prm.a_s + static_cast<size_t>(m) * prm.Kb + kb) * ws
-                                                   : 0.0f;
+            if constexpr (C::FUSED)
+              sc_col[i] = (j < C::kCpt) ? act_scale[kb * C::BN + j] * cur.w : 0.0f;
+            else
+              sc_col[i] = cur.col[i < kColRegs ? i : 0] * cur.w;
           }
         }
         if (!mbar_wait(&tfull[pb], pph, abort_flag, prm.err, kDevErrTimeoutEpilogue)) {
           ok = false;
           break;
         }
+#ifdef FP8BLK_TRACE
+        if (threadIdx.x == 64 && pb == 0 && pph == 0) FP8BLK_STAMP(7);
+        if (threadIdx.x == 64 && kb == u.kb0 + C::STAGES) FP8BLK_STAMP(13);
+#endif
         tc_fence_after_sync();
         const uint32_t col0 = static_cast<uint32_t>(pb * C::BN + group * C::kCpt);
         if constexpr (C::kCpt == 16 || C::EPI_WARPS == 8) {
@@ -612,12 +829,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   }
 
+  if (threadIdx.x == 64) FP8BLK_STAMP(8);
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  if (threadIdx.x == 0) FP8BLK_STAMP(9);
 }
 
 // ---------------------------------------------------------------------------
@@ -661,8 +880,20 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 // Swapped (decode-sized M): BN = 16..128 token columns.
 using CfgN256 = Cfg<256, false, 4, 2, 8>;
 using CfgN128 = Cfg<128, false, 6, 4, 4>;
-using CfgS16 = Cfg<16, true, 8, 8, 4>;
-using CfgS32 = Cfg<32, true, 8, 8, 4>;
+#ifndef FP8BLK_DECODE_STAGES
+#define FP8BLK_DECODE_STAGES 8
+#endif
+#ifndef FP8BLK_DECODE_P
+#define FP8BLK_DECODE_P 8
+#endif
+#ifndef FP8BLK_SWAP_WHOLE_TILES
+#define FP8BLK_SWAP_WHOLE_TILES 1
+#endif
+#ifndef FP8BLK_DECODE_OCC
+#define FP8BLK_DECODE_OCC 1
+#endif
+using CfgS16 = Cfg<16, true, FP8BLK_DECODE_STAGES, FP8BLK_DECODE_P, 4>;
+using CfgS32 = Cfg<32, true, (FP8BLK_DECODE_STAGES > 10 ? 10 : FP8BLK_DECODE_STAGES), 8, 4>;
 using CfgS64 = Cfg<64, true, 6, 4, 4>;
 using CfgS128 = Cfg<128, true, 6, 4, 4>;
 // Fused w1/w3 GEMM with the SwiGLU + act_quant epilogue (dense and grouped),
@@ -670,6 +901,10 @@ using CfgS128 = Cfg<128, true, 6, 4, 4>;
 using CfgSwiGLU = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false>;
 using CfgSwiGLUGrouped = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, true>;
 using CfgScatterGrouped = Cfg<256, false, 4, 2, 8, kEpiScatter, true>;
+// Decode linear with the act_quant fused in (M <= 16): weights-only stages.
+using CfgF16S8 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, true>;
+using CfgF16S4 = Cfg<16, true, 4, 8, 4, kEpiBf16, false, true>;
+constexpr int kMaxDynSmem = 232448;
 
 struct Plan {
   int bn;
@@ -703,6 +938,19 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
     pl.bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
     pl.tiles_lane = static_cast<int>((N + 127) / 128);
     pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
+    const long long tiles = static_cast<long long>(pl.tiles_lane) * pl.tiles_col;
+    if (FP8BLK_SWAP_WHOLE_TILES && pl.bn <= 32 && tiles <= sm_count) {
+      // One CTA streams each whole weight tile: no stream-K fixup.
+      pl.grid = static_cast<int>(tiles);
+      pl.dp_waves = 1;
+      pl.sk_tiles = 0;
+      pl.sk_iters = 0;
+      return pl;
+    }
+    if (pl.bn <= 32) {
+      plan_schedule(pl, K / kBlock, sm_count * FP8BLK_DECODE_OCC);
+      return pl;
+    }
   } else {
     pl.swap = false;
     pl.bn = N <= 128 ? 128 : 256;
@@ -739,16 +987,30 @@ int sm_count_or_default() {
 
 template <class C>
 int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const CUtensorMap& mc2,
-           const GemmParams& prm, cudaStream_t stream) {
+           const GemmParams& prm, cudaStream_t stream, size_t extra_smem = 0) {
   static bool attr_done[64] = {};
   auto kern = fp8_gemm_kernel<C>;
+  const int smem_attr = C::FUSED ? kMaxDynSmem : C::kSmemBytes;
   if (d->device >= 64 || !attr_done[d->device]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_attr) != cudaSuccess)
       return FP8BLK_ERR_CUDA;
     if (d->device < 64) attr_done[d->device] = true;
   }
-  kern<<<prm.grid, C::kThreads, C::kSmemBytes, stream>>>(ml, mc, mc2, prm);
-  return launch_status();
+#ifdef FP8BLK_TRACE
+  static int trace_counter = 0;
+  const_cast<GemmParams&>(prm).trace_id = trace_counter++ & 7;
+#endif
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(prm.grid));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes + extra_smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, ml, mc, mc2, prm));
 }
 
 }  // namespace
@@ -825,6 +1087,48 @@ namespace {
 bool scale_fmt_ok(int f) { return f == FP8BLK_SCALE_FP32 || f == FP8BLK_SCALE_UE8M0; }
 
 }  // namespace
+
+// Decode FP8 linear (M <= 16) in one kernel: act_quant of x inside the GEMM
+// CTAs, whole 128-row weight tiles per CTA. Sets *used = false (and launches
+// nothing) when the shape does not fit the fused kernel's shared memory; the
+// caller then runs act_quant + fp8_gemm.
+int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, int64_t M, int64_t N, int64_t K,
+                     int scale_fmt, cudaStream_t stream, bool* used) {
+  *used = false;
+  if (!scale_fmt_ok(scale_fmt)) return FP8BLK_ERR_ARG;
+  if (M < 1 || M > 16 || N < 1 || K < kBlock || K % kBlock || N > (int64_t{1} << 31) - 1 || K > (int64_t{1} << 24))
+    return FP8BLK_OK;
+  if (!x || !w || !w_s || !y) return FP8BLK_ERR_NULL;
+  if (!is_aligned(x, 16) || !is_aligned(w, 16) || !is_aligned(w_s, 4) || !is_aligned(y, 2)) return FP8BLK_ERR_ALIGN;
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  const int Kb = static_cast<int>(K / kBlock);
+  const size_t extra = fused_extra_bytes(Kb, 16);
+  const int variant = CfgF16S8::kSmemBytes + extra <= kMaxDynSmem   ? 0   // 8 weight stages
+                      : CfgF16S4::kSmemBytes + extra <= kMaxDynSmem ? 1   // 4 weight stages
+                                                                    : -1;
+  if (variant < 0) return FP8BLK_OK;
+  GemmParams prm{};
+  prm.w_s = w_s;
+  prm.c = static_cast<__nv_bfloat16*>(y);
+  prm.x = static_cast<const __nv_bfloat16*>(x);
+  prm.err = d->err_word;
+  prm.M = static_cast<int>(M);
+  prm.N = static_cast<int>(N);
+  prm.Kb = Kb;
+  prm.n_wblocks = static_cast<int>((N + 127) / 128);
+  prm.ldc = static_cast<int>(N);
+  prm.tiles_lane = prm.n_wblocks;
+  prm.tiles_col = 1;
+  prm.whole_tiles = prm.n_wblocks;
+  prm.grid = prm.n_wblocks < d->sm_count ? prm.n_wblocks : d->sm_count;
+  prm.ue8m0 = scale_fmt == FP8BLK_SCALE_UE8M0;
+  CUtensorMap ml;
+  if (!make_kmajor_map(&ml, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128)) return FP8BLK_ERR_CUDA;
+  *used = true;
+  return variant == 0 ? launch<CfgF16S8>(d, ml, ml, ml, prm, stream, extra)
+                      : launch<CfgF16S4>(d, ml, ml, ml, prm, stream, extra);
+}
 
 size_t swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t K) {
   if (M <= 0 || inter <= 0 || K <= 0) return 256;
@@ -1016,3 +1320,14 @@ extern "C" int fp8blk_gemm(const void* a_e4m3, const float* a_s, const void* w_e
   return fp8blk::gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, workspace, workspace_bytes,
                           reinterpret_cast<cudaStream_t>(stream));
 }
+
+#ifdef FP8BLK_TRACE
+// Phase-trace reader (trace builds only): copies n stamps (16 per CTA) to host.
+extern "C" __attribute__((visibility("default"))) int fp8trace_read(unsigned long long* host, int n) {
+  return cudaMemcpyFromSymbol(host, fp8blk::g_trace, sizeof(unsigned long long) * n) == cudaSuccess ? 0 : 1;
+}
+extern "C" __attribute__((visibility("default"))) int fp8trace_clear(void) {
+  static unsigned long long zeros[8 * 4096 * 16];
+  return cudaMemcpyToSymbol(fp8blk::g_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 1;
+}
+#endif

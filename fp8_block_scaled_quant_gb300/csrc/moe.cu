@@ -26,6 +26,8 @@
 namespace fp8blk {
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int act_quant_launch(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* s, int scale_fmt,
+                     cudaStream_t stream, bool trigger);
 int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
              int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t K);
@@ -277,7 +279,7 @@ extern "C" int fp8blk_ffn(const void* x_bf16, const void* w1_e4m3, const float* 
   const size_t g1 = align256(swiglu_workspace_bytes(M, inter, dim));
   uint8_t* g2p = p + g1;
   const size_t rest = workspace_bytes - (g2p - static_cast<uint8_t*>(workspace));
-  if (int st = fp8blk_act_quant(x_bf16, M, dim, xq, xs, scale_fmt, stream)) return st;
+  if (int st = act_quant_launch(x_bf16, M, dim, xq, xs, scale_fmt, cs, true)) return st;
   if (int st = swiglu_run(xq, xs, w1_e4m3, w1_s, w3_e4m3, w3_s, uq, us, M, inter, dim, scale_fmt, p, g1, cs))
     return st;
   return gemm_run(uq, us, w2_e4m3, w2_s, y_bf16, M, dim, inter, scale_fmt, g2p, rest, cs);

@@ -14,6 +14,7 @@
 
 #include "fp8blk.h"
 #include "host.cuh"
+#include "ptx.cuh"
 
 namespace fp8blk {
 namespace {
@@ -54,7 +55,11 @@ constexpr int kAqUnroll = 2;
 
 __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint4* __restrict__ x, uint2* __restrict__ q,
                                                                float* __restrict__ s, int64_t nblocks,
-                                                               bool ue8m0) {
+                                                               bool ue8m0, bool trigger) {
+  // Launched programmatically, this kernel may start before the previous one
+  // on the stream ends: x is read only after that kernel has completed.
+  griddep_wait();
+  if (trigger) griddep_launch_dependents();
   const int sub = threadIdx.x & 15;
   const int half = (threadIdx.x >> 4) & 1;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kAqThreads + threadIdx.x) >> 5;
@@ -208,8 +213,13 @@ int grid_for(const DevInfo* d, int64_t work_items, int threads, int per_sm) {
 
 using namespace fp8blk;
 
-extern "C" int fp8blk_act_quant(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* s, int scale_fmt,
-                                fp8blk_stream_t stream) {
+namespace fp8blk {
+
+// act_quant launch; `trigger` lets the next kernel on the stream start early
+// (used inside the linear / FFN entry points, whose next kernel is a GEMM that
+// reads only its weights before it waits for this one).
+int act_quant_launch(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* s, int scale_fmt,
+                     cudaStream_t stream, bool trigger) {
   if (scale_fmt != FP8BLK_SCALE_FP32 && scale_fmt != FP8BLK_SCALE_UE8M0) return FP8BLK_ERR_ARG;
   if (M < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
   if (M == 0 || K == 0) return FP8BLK_OK;
@@ -220,10 +230,25 @@ extern "C" int fp8blk_act_quant(const void* x_bf16, int64_t M, int64_t K, void* 
   const int64_t nblocks = M * (K / kBlock);
   // A warp per pair of blocks, kAqUnroll pairs per pass, up to 8 CTAs per SM.
   const int grid = grid_for(d, (nblocks + 1) / 2 * 32 / kAqUnroll, kAqThreads, 8);
-  act_quant_kernel<<<grid, kAqThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(x_bf16), static_cast<uint2*>(q_e4m3), s, nblocks,
-      scale_fmt == FP8BLK_SCALE_UE8M0);
-  return launch_status();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kAqThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, act_quant_kernel, static_cast<const uint4*>(x_bf16),
+                                        static_cast<uint2*>(q_e4m3), s, nblocks, scale_fmt == FP8BLK_SCALE_UE8M0,
+                                        trigger));
+}
+
+}  // namespace fp8blk
+
+extern "C" int fp8blk_act_quant(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* s, int scale_fmt,
+                                fp8blk_stream_t stream) {
+  return act_quant_launch(x_bf16, M, K, q_e4m3, s, scale_fmt, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" int fp8blk_weight_quant(const float* w, int64_t N, int64_t K, void* q_e4m3, float* s, int scale_fmt,

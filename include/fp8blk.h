@@ -28,6 +28,14 @@
  *   - Sizes of 0 are valid and launch nothing (except where noted).
  *   - Not thread-safe per workspace: calls that share a workspace must be
  *     ordered on one stream.
+ *   - Overlap on a stream: the GEMM kernels (and act_quant inside
+ *     fp8blk_linear / fp8blk_ffn) let the next kernel of this library on the
+ *     same stream start early (programmatic dependent launch). That kernel
+ *     may begin loading its WEIGHT operands (w, w1, w3, w2) before the
+ *     previous one has finished; it reads activations and scales, and writes
+ *     anything, only after. So a weight operand must not be the output of the
+ *     library call issued just before it on the same stream. Kernels of other
+ *     libraries are ordered as usual.
  */
 #ifndef FP8BLK_H
 #define FP8BLK_H

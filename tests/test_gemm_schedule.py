@@ -17,6 +17,9 @@ def make_plan(M, N, K, sms):
         swap = True
         bn = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
         tl, tc = -(-N // 128), -(-M // bn)
+        if bn <= 32 and tl * tc <= sms:   # decode: one CTA per whole weight tile
+            return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tl * tc, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
+                        tiles=tl * tc)
     else:
         swap = False
         bn = 128 if N <= 128 else 256
@@ -103,9 +106,11 @@ def test_schedule_covers_every_iteration_once(M, N, K, sms):
             assert slots[2 * (cs[0] + i) + (1 if i == 0 else 0)] == (tile, i)
 
 
-def test_decode_plan_uses_whole_machine():
+def test_decode_plan_uses_whole_tiles():
     p = make_plan(8, 10944, 2048, 152)
-    assert p["swap"] and p["bn"] == 16 and p["grid"] == 152 and p["dp"] == 0
+    assert p["swap"] and p["bn"] == 16 and p["grid"] == 86 and p["dp"] == 1 and p["sk_iters"] == 0
+    p = make_plan(64, 10944, 2048, 152)      # BN 64: stream-K over the whole machine
+    assert p["grid"] == 152 and p["dp"] == 0
 
 
 def test_prefill_plan_is_hybrid():

@@ -197,3 +197,26 @@ def test_linear_host_buffers():
     torch.cuda.current_stream().synchronize()
     y = fb.linear(bits_to_dev_bf16(x), q, s)
     assert torch.equal(yh.view(torch.int16), y.cpu().view(torch.int16))
+
+
+# ---- decode linear with act_quant fused into the GEMM (M <= 32) ----------------
+
+@pytest.mark.parametrize("M,N,K", [(1, 10944, 2048), (2, 320, 256), (1, 1000, 7168), (2, 576, 9984),
+                                   (2, 32768, 512), (1, 129, 4096), (8, 10944, 2048), (32, 4096, 1024)])
+@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0])
+def test_fused_decode_linear(M, N, K, fmt):
+    """fp8blk_linear (for M <= 2 act_quant runs inside the GEMM kernel, with
+    8 weight stages up to K = 5888 and 4 beyond): same bits as act_quant +
+    fp8_gemm on the same whole-tile schedule (N <= 128 * SMs), and within the
+    GEMM tolerance of the oracle."""
+    ue = fmt == fb.SCALE_UE8M0
+    x, w, xq, xs, wq, ws = host_problem(M, N, K, 3000 + M + N, 0.01, ue8m0=ue)
+    xd = bits_to_dev_bf16(x)
+    q, s = fb.weight_quant(torch.from_numpy(w).cuda(), fmt)
+    y = fb.linear(xd, q, s, scale_fmt=fmt)
+    a, a_s = fb.act_quant(xd, fmt)
+    c = fb.fp8_gemm(a, a_s, q, s, scale_fmt=fmt)
+    if -(-N // 128) <= torch.cuda.get_device_properties(0).multi_processor_count:
+        assert torch.equal(y.view(torch.int16), c.view(torch.int16))
+    assert_gemm_close(dev_to_bits(y), oracle.gemm(xq, xs, wq, ws), what=f"fused linear {M}x{N}x{K}")
+    assert fb.last_device_error() == 0
