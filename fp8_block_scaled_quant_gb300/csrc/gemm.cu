@@ -155,9 +155,19 @@ constexpr int pow2_at_least(int v, int floor_) {
 #define FP8BLK_DECODE_L2_AHEAD 0
 #endif
 
+// TMEM columns per load (and per wait) in the register-split epilogue.
+#ifndef FP8BLK_SPLIT_LD
+#define FP8BLK_SPLIT_LD 64
+#endif
+
 template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_, int MODE_ = kEpiBf16, bool GROUPED_ = false,
-          bool FUSED_ = false>
+          bool FUSED_ = false, int CLUSTER_ = 1>
 struct Cfg {
+  // CLUSTER = 2: two CTAs with adjacent 128-row lane tiles and the same column
+  // tile form a cluster. Each loads its own lane tile and one half of the
+  // shared column tile, multicast into both, so every CTA reads 2/3 of the
+  // operand bytes per K block from L2 that a lone CTA would.
+  static constexpr int CLUSTER = CLUSTER_;
   // FUSED: decode linear with act_quant inside -- the CTA quantises the bf16
   // activation itself into a resident shared-memory operand (all K blocks),
   // and only the weights stream through the stage ring.
@@ -175,9 +185,18 @@ struct Cfg {
   // the SwiGLU amax exchange between the two column groups (double-buffered).
   static constexpr int kGroupBytes = GROUPED ? 2 * (kMaxGroups + 4) * 4 : 0;
   static constexpr int kXchgBytes = MODE == kEpiSwiGLU ? 2 * 2 * 128 * 4 : 0;
-  static constexpr int kThreads = (2 + EPI_WARPS) * 32;
   static constexpr int kGroups = EPI_WARPS / 4;  // column groups in the epilogue
   static constexpr int kCpt = BN / kGroups;      // columns per epilogue thread
+  // Register split for large-M tiles (two column groups of 128): 12 warps, and
+  // setmaxnreg moves registers from the first warpgroup (TMA producer, MMA
+  // issuer, two idle warps) to the two epilogue warpgroups, whose threads hold
+  // 128 accumulators next to 64 freshly loaded TMEM columns. The launch holds
+  // kThreads x 168 registers; the split hands out exactly that many.
+  static constexpr bool kSplitRegs = !SWAP && !FUSED && EPI_WARPS == 8 && kCpt == 128;
+  static constexpr int kEpiWarp0 = kSplitRegs ? 4 : 2;  // first epilogue warp
+  static constexpr int kThreads = (kEpiWarp0 + EPI_WARPS) * 32;
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kRegsLow = 56, kRegsHigh = 224;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = FUSED ? kABytes : kABytes + kBBytes;
@@ -196,9 +215,15 @@ struct Cfg {
   static_assert(!FUSED || (SWAP && BN <= 32 && MODE == kEpiBf16 && !GROUPED), "fused act_quant: decode tiles");
   static_assert(EPI_WARPS % 4 == 0, "epilogue warps come in warpgroups");
   static_assert(kCpt == 16 || kCpt % 32 == 0, "TMEM loads of 16 or 32 columns");
-  static_assert(SWAP || kCpt == 128, "non-swapped tiles: one weight block per column group");
+  static_assert(SWAP || kCpt == 128 || (kCpt == 64 && MODE != kEpiSwiGLU),
+                "non-swapped tiles: a column group lies inside one weight block");
   static_assert(!SWAP || kGroups == 1, "swapped tiles: one column group");
   static_assert(P * BN <= 512, "TMEM has 512 columns");
+  static_assert(!kSplitRegs || (128 * kRegsLow + EPI_WARPS * 32 * kRegsHigh <= kThreads * kLaunchRegs &&
+                                kThreads * kLaunchRegs <= 65536),
+                "the register split must fit the registers the CTA is launched with");
+  static_assert(CLUSTER == 1 || (CLUSTER == 2 && !SWAP && !GROUPED && !FUSED && BN == 256),
+                "clusters pair the 128-row lane tiles of dense large-M GEMMs");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -216,7 +241,8 @@ struct TileInfo {
 // share a weight tile run side by side. rows/mtiles are the group tables in
 // shared memory.
 template <class C>
-__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, const int* rows, const int* mtiles) {
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, const int* rows, const int* mtiles,
+                                              int rank) {
   TileInfo t;
   if constexpr (C::GROUPED) {
     int lo = 0, hi = p.E - 1;  // last group whose first tile is <= tile
@@ -235,7 +261,8 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
     t.wblock = t.col_y / 128;
     t.col0 = nt * C::kWRows;
   } else {
-    const int tl = tile % p.tiles_lane, tc = tile / p.tiles_lane;
+    // Clusters: the schedule's lane index counts CTA pairs; `rank` picks the half.
+    const int tl = (tile % p.tiles_lane) * C::CLUSTER + rank, tc = tile / p.tiles_lane;
     t.lane_y = tl * 128;
     if constexpr (C::SWAP) {
       t.lane_valid = min(128, p.N - t.lane_y);
@@ -326,7 +353,7 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
     if (row >= t.lane_valid) return true;
     const int r = t.lane_y + row;
     const size_t out_row = C::MODE == kEpiScatter ? static_cast<size_t>(__ldg(p.perm + r)) : static_cast<size_t>(r);
-    const int n0 = t.col0 + group * 128;
+    const int n0 = t.col0 + group * C::kCpt;
     __nv_bfloat16* crow = p.c + out_row * p.ldc;
 #pragma unroll
     for (int v = 0; v < C::kCpt / 8; ++v) {
@@ -352,16 +379,31 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
 // Optional phase trace (compile with -DFP8BLK_TRACE): %globaltimer stamps per
 // CTA at fixed points of each role, read back with fp8trace_read(). Not part
 // of the library's interface; default builds contain none of it.
+// Slots 16.. hold per-role sums of SM cycles (FP8BLK_PUT), e.g. time spent in
+// one kind of wait.
 #ifdef FP8BLK_TRACE
-constexpr int kTraceSlots = 16;
+constexpr int kTraceSlots = 32;
 __device__ unsigned long long g_trace[8 * 4096 * kTraceSlots];
-#define FP8BLK_STAMP(slot)                                                                               \
+#define FP8BLK_PUT(slot, value)                                                                          \
   do {                                                                                                   \
-    if (blockIdx.x < 4096)                                                                               \
-      g_trace[((prm.trace_id & 7) * 4096 + blockIdx.x) * kTraceSlots + (slot)] = global_timer_ns();       \
+    if (blockIdx.x < 4096) g_trace[((prm.trace_id & 7) * 4096 + blockIdx.x) * kTraceSlots + (slot)] = (value); \
   } while (0)
+#define FP8BLK_STAMP(slot) FP8BLK_PUT(slot, global_timer_ns())
+// Per-K-block event timeline of CTA 0 in SM cycles: g_timeline[event][k-block].
+constexpr int kTimelineLen = 1024;
+__device__ long long g_timeline[16 * kTimelineLen];
+#define FP8BLK_TL(ev, j)                                                                 \
+  do {                                                                                   \
+    if (blockIdx.x == 0 && (j) < kTimelineLen) g_timeline[(ev) * kTimelineLen + (j)] = clock64(); \
+  } while (0)
+#define FP8BLK_TIC(v) const long long v = clock64()
+#define FP8BLK_TOC(sum, v) (sum) += clock64() - (v)
 #else
+#define FP8BLK_PUT(slot, value) do { } while (0)
+#define FP8BLK_TL(ev, j) do { } while (0)
 #define FP8BLK_STAMP(slot) do { } while (0)
+#define FP8BLK_TIC(v) do { } while (0)
+#define FP8BLK_TOC(sum, v) do { } while (0)
 #endif
 
 // Shared memory of the fused decode operand: Kb blocks of BN rows x 128
@@ -396,6 +438,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   float* xchg = reinterpret_cast<float*>(tail + C::kBarBytes + C::kGroupBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Cluster rank, and the index of the schedule this CTA (pair) walks.
+  const int rank = C::CLUSTER > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int worker = static_cast<int>(blockIdx.x) / C::CLUSTER;
   if (threadIdx.x == 0) FP8BLK_STAMP(0);
   // The next kernel on the stream may begin its prologue (and its weight
   // loads) now; it waits for this one before touching anything we write.
@@ -404,7 +449,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], C::CLUSTER);  // freed by the MMAs of every CTA that shares the stage
     }
     for (int q = 0; q < C::P; ++q) {
       mbar_init(&tfull[q], 1);
@@ -436,12 +481,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  // Clusters: no CTA multicasts into its peer before the peer's barriers exist.
+  if constexpr (C::CLUSTER > 1) cluster_sync();
+  else __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   if (threadIdx.x == 0) FP8BLK_STAMP(1);
   if constexpr (C::GROUPED) grouped_tiles = grp_mtiles[prm.E] * prm.tiles_col;
 
+  // Roles: warp 0 TMA producer, warp 1 MMA issuer, warps kEpiWarp0.. promotion
+  // and epilogue. With the register split, each warpgroup sets its budget at
+  // the head of its own branch, so the code it runs is compiled for it.
+  if (warp < C::kEpiWarp0) {
+  if constexpr (C::kSplitRegs) setmaxnreg_dec<C::kRegsLow>();
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -453,10 +505,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         } else if constexpr (C::MODE == kEpiSwiGLU) {
           // Column rows [0,64) w1, [64,128) w3, [128,192) w1 + 64, [192,256) w3 + 64.
           uint8_t* sb = sa + C::kABytes;
-          tma_load_2d(sb, &tmap_col, &full[st], kb * 128, t.col_y);
-          tma_load_2d(sb + 64 * 128, &tmap_col2, &full[st], kb * 128, t.col_y);
-          tma_load_2d(sb + 128 * 128, &tmap_col, &full[st], kb * 128, t.col_y + 64);
-          tma_load_2d(sb + 192 * 128, &tmap_col2, &full[st], kb * 128, t.col_y + 64);
+          if constexpr (C::CLUSTER > 1) {  // rank r loads rows [128 r, 128 r + 128) into both CTAs
+            const int off = rank * 64;
+            tma_load_2d_multicast(sb + 2 * off * 128, &tmap_col, &full[st], kb * 128, t.col_y + off, 0x3);
+            tma_load_2d_multicast(sb + (2 * off + 64) * 128, &tmap_col2, &full[st], kb * 128, t.col_y + off, 0x3);
+          } else {
+            tma_load_2d(sb, &tmap_col, &full[st], kb * 128, t.col_y);
+            tma_load_2d(sb + 64 * 128, &tmap_col2, &full[st], kb * 128, t.col_y);
+            tma_load_2d(sb + 128 * 128, &tmap_col, &full[st], kb * 128, t.col_y + 64);
+            tma_load_2d(sb + 192 * 128, &tmap_col2, &full[st], kb * 128, t.col_y + 64);
+          }
+        } else if constexpr (C::CLUSTER > 1) {
+          tma_load_2d_multicast(sa + C::kABytes + rank * 128 * 128, &tmap_col, &full[st], kb * 128,
+                                t.col_y + rank * 128, 0x3);
         } else {
           tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, t.col_y);
         }
@@ -472,11 +533,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // activations follow once the previous kernel has completed.
       int npre = 0;
       if constexpr (!C::GROUPED) {
-        Sched pre(prm, blockIdx.x);
+        Sched pre(prm, worker);
         Unit u;
         int nl2 = 0;
         while ((npre < C::STAGES || nl2 < C::kL2Ahead) && pre.next(u)) {
-          const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles);
+          const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
           for (int kb = u.kb0; kb < u.kb1; ++kb) {
             if (npre < C::STAGES) {
               mbar_arrive_expect_tx(&full[npre], C::kStageBytes);
@@ -493,22 +554,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       griddep_wait();
       FP8BLK_STAMP(2);
-      Sched sch(prm, blockIdx.x, grouped_tiles);
+      Sched sch(prm, worker, grouped_tiles);
       Unit u;
       int st = 0;
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
+#ifdef FP8BLK_TRACE
+      long long tw_empty = 0;
+#endif
       while (ok && sch.next(u)) {
-        const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles);
+        const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (issued < npre) {
             load_acts(st, t, kb);  // stage st == issued: weights already on their way
           } else {
+            FP8BLK_TIC(t0);
             if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, prm.err, kDevErrTimeoutProducer)) {
               ok = false;
               break;
             }
+            FP8BLK_TOC(tw_empty, t0);
             mbar_arrive_expect_tx(&full[st], C::kStageBytes);
             load_weights(st, t, kb);
             load_acts(st, t, kb);
@@ -517,7 +583,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             FP8BLK_STAMP(11);
 #endif
           }
+          FP8BLK_TL(0, issued);
           ++issued;
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+#ifdef FP8BLK_TRACE
+      FP8BLK_PUT(20, tw_empty);
+#endif
+      if constexpr (C::CLUSTER > 1) {
+        // Wait until both CTAs' MMAs have released the last stages: their
+        // multicast arrivals on this CTA's barriers have then all landed.
+        const long long n = issued < C::STAGES ? issued : C::STAGES;
+        for (long long i = 0; ok && i < n; ++i) {
+          if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, prm.err, kDevErrTimeoutProducer)) ok = false;
           if (++st == C::STAGES) {
             st = 0;
             ph ^= 1u;
@@ -536,54 +618,91 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_e4m3_f32(128, C::BN);
-      Sched sch(prm, blockIdx.x, grouped_tiles);
-      Unit u;
-      int st = 0, pb = 0;
-      uint32_t ph = 0, pph = 0;
-      bool ok = true;
-      if constexpr (C::FUSED) ok = mbar_wait(act_ready, 0, abort_flag, prm.err, kDevErrTimeoutMma);
-      while (ok && sch.next(u)) {
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait(&full[st], ph, abort_flag, prm.err, kDevErrTimeoutMma) ||
-              !mbar_wait(&tempty[pb], pph ^ 1u, abort_flag, prm.err, kDevErrTimeoutMma)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
+    // The whole warp walks the schedule and waits; one elected lane issues the
+    // MMAs and commits, so the warp stays converged around the tcgen05 issue
+    // (a loop run by a lone lane issues them far more slowly).
+    const bool leader = elect_one_sync();
+    constexpr uint32_t kIdesc = idesc_e4m3_f32(128, C::BN);
+    Sched sch(prm, worker, grouped_tiles);
+    Unit u;
+    int st = 0, pb = 0;
+    uint32_t ph = 0, pph = 0;
+    bool ok = true;
+    // Every lane waits; a wait that gave up in any lane stops the whole warp.
+    if constexpr (C::FUSED) ok = __all_sync(0xFFFFFFFFu, mbar_wait(act_ready, 0, abort_flag, prm.err, kDevErrTimeoutMma));
 #ifdef FP8BLK_TRACE
+    long long tw_full = 0, tw_tmem = 0, n_kb = 0;
+    FP8BLK_TIC(t_loop);
+#endif
+    while (ok && sch.next(u)) {
+      for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        FP8BLK_TIC(t0);
+        bool w = mbar_wait(&full[st], ph, abort_flag, prm.err, kDevErrTimeoutMma);
+        FP8BLK_TOC(tw_full, t0);
+#ifdef FP8BLK_TRACE
+        if (leader) FP8BLK_TL(1, n_kb);
+#endif
+        FP8BLK_TIC(t1);
+        w = w && mbar_wait(&tempty[pb], pph ^ 1u, abort_flag, prm.err, kDevErrTimeoutMma);
+        FP8BLK_TOC(tw_tmem, t1);
+        if (!__all_sync(0xFFFFFFFFu, w)) {
+          ok = false;
+          break;
+        }
+#ifdef FP8BLK_TRACE
+        if (leader) {
+          FP8BLK_TL(2, n_kb);
           if (st == 0 && ph == 0 && pb == 0) FP8BLK_STAMP(3);
           if (st == 0 && ph == 1) FP8BLK_STAMP(12);
+        }
+        ++n_kb;
 #endif
-          const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
-          const uint64_t ad = sdesc_kmajor_sw128(a_addr);
-          const uint64_t bd = C::FUSED ? sdesc_kmajor_sw128(smem_u32(act_smem + kb * (C::BN * 128)))
-                                       : sdesc_kmajor_sw128(a_addr + C::kABytes);
-          const uint32_t d = tmem_base + static_cast<uint32_t>(pb * C::BN);
+        tc_fence_after_sync();
+        const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
+        const uint64_t ad = sdesc_kmajor_sw128(a_addr);
+        const uint64_t bd = C::FUSED ? sdesc_kmajor_sw128(smem_u32(act_smem + kb * (C::BN * 128)))
+                                     : sdesc_kmajor_sw128(a_addr + C::kABytes);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(pb * C::BN);
+        if (leader) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)  // 32-byte K slices: start address advances by 32 B (2 x 16 B)
             mma_e4m3(d, ad + 2 * k, bd + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-          mma_commit(&empty[st]);
+          if constexpr (C::CLUSTER > 1) mma_commit_multicast(&empty[st], 0x3);  // the stage is shared
+          else mma_commit(&empty[st]);
           mma_commit(&tfull[pb]);
-          if (++st == C::STAGES) {
-            st = 0;
-            ph ^= 1u;
-          }
-          if (++pb == C::P) {
-            pb = 0;
-            pph ^= 1u;
-          }
+          FP8BLK_TL(3, n_kb - 1);
+        }
+        __syncwarp();
+        if (++st == C::STAGES) {
+          st = 0;
+          ph ^= 1u;
+        }
+        if (++pb == C::P) {
+          pb = 0;
+          pph ^= 1u;
         }
       }
+    }
+#ifdef FP8BLK_TRACE
+    if (leader) {
       FP8BLK_STAMP(4);
-      // Wait for every MMA this thread issued before TMEM is released.
+      FP8BLK_PUT(16, tw_full);
+      FP8BLK_PUT(17, tw_tmem);
+      FP8BLK_PUT(18, n_kb);
+      FP8BLK_PUT(19, clock64() - t_loop);
+    }
+#endif
+    // Wait for every MMA the leader issued before TMEM is released.
+    if (leader) {
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr, prm.err, kDevErrTimeoutDrain);
     }
+    __syncwarp();
+  }
   } else {
+    if constexpr (C::kSplitRegs) setmaxnreg_inc<C::kRegsHigh>();
     // ---------------- promotion + epilogue ----------------
-    const int ew = warp - 2;
+    const int ew = warp - C::kEpiWarp0;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int group = ew >> 2;     // column group
     const int row = quarter * 32 + lane;
@@ -602,7 +721,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     };
 
     griddep_wait();  // activation scales and every output are the previous kernel's business
-    if (threadIdx.x == 64) FP8BLK_STAMP(5);
+    if (threadIdx.x == C::kEpiWarp0 * 32) FP8BLK_STAMP(5);
     if constexpr (C::FUSED) {
       // act_quant of x [M, K] into the resident MMA operand: the act_quant rule
       // per (row, 128 columns) -- amax, max(amax, 1e-4) / 448 (ue8m0: rounded
@@ -610,7 +729,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // Rows M..BN-1 of the operand are zero. Layout: block kb at kb*BN*128,
       // row m at (m / 8) * 1024 + (m % 8) * 128, its 16-byte chunk c stored at
       // chunk c ^ (m % 8) (the 128-byte swizzle the descriptors name).
-      const int et = threadIdx.x - 64;  // 0 .. 127
+      const int et = threadIdx.x - C::kEpiWarp0 * 32;  // 0 .. 127
       const int sub = et & 15, hw = et >> 4;
       const int total = prm.M * prm.Kb;
       const int K = prm.Kb * 128;
@@ -671,7 +790,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
       named_barrier_sync(1, C::EPI_WARPS * 32);
       if (lane == 0) mbar_arrive(act_ready);
-      if (threadIdx.x == 64) FP8BLK_STAMP(6);
+      if (threadIdx.x == C::kEpiWarp0 * 32) FP8BLK_STAMP(6);
     }
     // Raw scale loads of one K block, issued kAhead blocks before their use so
     // that their L2 round trips overlap the MMAs of the blocks in between.
@@ -693,7 +812,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           r.w = __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
           r.w3 = __ldg(prm.w3_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
         } else {
-          const int nb = t.wblock + group;
+          const int nb = t.wblock + (group * C::kCpt) / 128;
           if (C::GROUPED || nb < prm.n_wblocks) r.w = __ldg(prm.w_s + static_cast<size_t>(nb) * prm.Kb + kb);
         }
       } else {
@@ -710,14 +829,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       return r;
     };
 
-    Sched sch(prm, blockIdx.x, grouped_tiles);
+    Sched sch(prm, worker, grouped_tiles);
     Unit u;
     int pb = 0;
     uint32_t pph = 0;
     uint32_t unit_parity = 0;
     bool ok = true;
+#ifdef FP8BLK_TRACE
+    long long tw_tfull = 0, t_busy = 0, t_fin = 0;
+    int ekb = 0;
+#endif
     while (ok && sch.next(u)) {
-      const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles);
+      const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
       float acc[C::kCpt];
 #pragma unroll
       for (int i = 0; i < C::kCpt; ++i) acc[i] = 0.0f;
@@ -749,17 +872,59 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               sc_col[i] = cur.col[i < kColRegs ? i : 0] * cur.w;
           }
         }
+        FP8BLK_TIC(t0);
         if (!mbar_wait(&tfull[pb], pph, abort_flag, prm.err, kDevErrTimeoutEpilogue)) {
           ok = false;
           break;
         }
+        FP8BLK_TOC(tw_tfull, t0);
 #ifdef FP8BLK_TRACE
-        if (threadIdx.x == 64 && pb == 0 && pph == 0) FP8BLK_STAMP(7);
-        if (threadIdx.x == 64 && kb == u.kb0 + C::STAGES) FP8BLK_STAMP(13);
+        if (lane == 0 && ew == 0) FP8BLK_TL(4, ekb);
+        if (lane == 0 && ew == C::EPI_WARPS - 1) FP8BLK_TL(6, ekb);
+#endif
+        FP8BLK_TIC(t1);
+#ifdef FP8BLK_TRACE
+        if (threadIdx.x == C::kEpiWarp0 * 32 && pb == 0 && pph == 0) FP8BLK_STAMP(7);
+        if (threadIdx.x == C::kEpiWarp0 * 32 && kb == u.kb0 + C::STAGES) FP8BLK_STAMP(13);
 #endif
         tc_fence_after_sync();
         const uint32_t col0 = static_cast<uint32_t>(pb * C::BN + group * C::kCpt);
-        if constexpr (C::kCpt == 16 || C::EPI_WARPS == 8) {
+        if constexpr (C::kSplitRegs) {
+          // Two loads of 64 columns, one wait each; sc_lo scales the first 64
+          // columns, sc_hi the second (w1 and w3 in SwiGLU mode).
+#pragma unroll
+          for (int h = 0; h < C::kCpt / FP8BLK_SPLIT_LD; ++h) {
+            uint32_t v[FP8BLK_SPLIT_LD];
+#if FP8BLK_SPLIT_LD == 64
+            tmem_ld_32x32b_x64(t_lane + col0 + h * 64, v);
+#else
+            tmem_ld_32x32b_x32(t_lane + col0 + h * 32, v);
+#endif
+            const float sc = h * FP8BLK_SPLIT_LD < 64 ? sc_lo : sc_hi;
+            const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+            for (int i = 0; i < FP8BLK_SPLIT_LD; i += 2) {
+              const int j = h * FP8BLK_SPLIT_LD + i;
+              const float2 r = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc2,
+                                          make_float2(acc[j], acc[j + 1]));
+              acc[j] = r.x;
+              acc[j + 1] = r.y;
+            }
+          }
+        } else if constexpr (!C::SWAP && C::kCpt == 64) {
+          // All 64 columns in one load and one wait, then packed f32x2 FMAs
+          // (the same fp32 fma per element).
+          uint32_t v[64];
+          tmem_ld_32x32b_x64(t_lane + col0, v);
+          const float2 sc2 = make_float2(sc_lo, sc_lo);
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            const float2 r = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc2,
+                                        make_float2(acc[i], acc[i + 1]));
+            acc[i] = r.x;
+            acc[i + 1] = r.y;
+          }
+        } else if constexpr (C::kCpt == 16 || C::EPI_WARPS == 8) {
           // 16-column loads: fewer live registers next to 128 accumulators
           // (ten warps leave 168 registers per thread).
 #pragma unroll
@@ -789,13 +954,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[pb]);
+#ifdef FP8BLK_TRACE
+        if (lane == 0 && ew == 0) FP8BLK_TL(5, ekb);
+        if (lane == 0 && ew == C::EPI_WARPS - 1) FP8BLK_TL(7, ekb);
+        ++ekb;
+#endif
+        FP8BLK_TOC(t_busy, t1);
         if (++pb == C::P) {
           pb = 0;
           pph ^= 1u;
         }
       }
       if (!ok) break;
-
+      FP8BLK_TIC(t2);
       if (u.nparts == 1) {
         ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync);
       } else {
@@ -807,31 +978,47 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!epi_sync()) break;
         if (ew == 0 && lane == 0) {
           __threadfence();
-          const int prev = atomicAdd(prm.counters + u.tile, 1);
+          const int prev = atomicAdd(prm.counters + u.tile * C::CLUSTER + rank, 1);
           *last_flag = (prev == u.nparts - 1) ? 1 : 0;
         }
         if (!epi_sync()) break;
         if (*last_flag) {
           __threadfence();
-          const int first = static_cast<int>(blockIdx.x) - u.part;
+          const int first = worker - u.part;
 #pragma unroll
           for (int i = 0; i < C::kCpt; ++i) acc[i] = 0.0f;
           for (int q = 0; q < u.nparts; ++q) {
-            const float* src = prm.slots + static_cast<size_t>(2 * (first + q) + (q == 0 ? 1 : 0)) * (C::BN * 128);
+            const int cta = (first + q) * C::CLUSTER + rank;
+            const float* src = prm.slots + static_cast<size_t>(2 * cta + (q == 0 ? 1 : 0)) * (C::BN * 128);
 #pragma unroll
             for (int i = 0; i < C::kCpt; ++i) acc[i] += __ldcg(src + (group * C::kCpt + i) * 128 + row);
           }
           ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync);
-          if (ew == 0 && lane == 0) prm.counters[u.tile] = 0;
+          if (ew == 0 && lane == 0) prm.counters[u.tile * C::CLUSTER + rank] = 0;
         }
       }
+      FP8BLK_TOC(t_fin, t2);
       unit_parity ^= 1u;
     }
+#ifdef FP8BLK_TRACE
+    if (threadIdx.x == C::kEpiWarp0 * 32) {
+      FP8BLK_PUT(21, tw_tfull);
+      FP8BLK_PUT(22, t_busy);
+      FP8BLK_PUT(23, t_fin);
+    }
+    if (threadIdx.x == C::kEpiWarp0 * 32 + 32 * 5) {  // a warp of the second column group
+      FP8BLK_PUT(24, tw_tfull);
+      FP8BLK_PUT(25, t_busy);
+    }
+#endif
   }
 
-  if (threadIdx.x == 64) FP8BLK_STAMP(8);
+  if (threadIdx.x == C::kEpiWarp0 * 32) FP8BLK_STAMP(8);
   tc_fence_before_sync();
-  __syncthreads();
+  // Clusters: neither CTA leaves while its peer may still write its stages or
+  // arrive on its barriers.
+  if constexpr (C::CLUSTER > 1) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -879,7 +1066,18 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 // Kernel variants. Non-swapped: BN = 256 (two epilogue warpgroups) or 128.
 // Swapped (decode-sized M): BN = 16..128 token columns.
 using CfgN256 = Cfg<256, false, 4, 2, 8>;
-using CfgN128 = Cfg<128, false, 6, 4, 4>;
+using CfgN256C2 = Cfg<256, false, 4, 2, 8, kEpiBf16, false, false, 2>;
+// Large-M tiles of 128 x 128 with a four-deep TMEM ring and two column groups of
+// 64: the promotion of one K block finishes while the next three are multiplied.
+#ifndef FP8BLK_N128_STAGES
+#define FP8BLK_N128_STAGES 6
+#endif
+using CfgN128E8 = Cfg<128, false, FP8BLK_N128_STAGES, 4, 8>;
+// Large-M GEMMs run as CTA pairs (clusters of 2) unless built with
+// -DFP8BLK_CLUSTER_PAIRS=0.
+#ifndef FP8BLK_CLUSTER_PAIRS
+#define FP8BLK_CLUSTER_PAIRS 1
+#endif
 #ifndef FP8BLK_DECODE_STAGES
 #define FP8BLK_DECODE_STAGES 8
 #endif
@@ -899,6 +1097,7 @@ using CfgS128 = Cfg<128, true, 6, 4, 4>;
 // Fused w1/w3 GEMM with the SwiGLU + act_quant epilogue (dense and grouped),
 // and the grouped GEMM whose rows are scattered back to token order.
 using CfgSwiGLU = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false>;
+using CfgSwiGLUC2 = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false, false, 2>;
 using CfgSwiGLUGrouped = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, true>;
 using CfgScatterGrouped = Cfg<256, false, 4, 2, 8, kEpiScatter, true>;
 // Decode linear with the act_quant fused in (M <= 16): weights-only stages.
@@ -909,6 +1108,7 @@ constexpr int kMaxDynSmem = 232448;
 struct Plan {
   int bn;
   bool swap;
+  int cluster;  // CTAs per schedule worker (2: lane-tile pairs); grid counts workers
   int tiles_lane, tiles_col;
   int grid, dp_waves, sk_tiles;
   long long sk_iters;
@@ -931,8 +1131,10 @@ void plan_schedule(Plan& pl, int64_t Kb, int sm_count) {
   pl.sk_iters = static_cast<long long>(pl.sk_tiles) * Kb;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
+// pair_workers: co-resident CTA pairs of the cluster kernel (0: no clusters).
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers) {
   Plan pl{};
+  pl.cluster = 1;
   if (M <= 128) {
     pl.swap = true;
     pl.bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
@@ -956,6 +1158,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
     pl.bn = N <= 128 ? 128 : 256;
     pl.tiles_lane = static_cast<int>((M + 127) / 128);
     pl.tiles_col = static_cast<int>((N + pl.bn - 1) / pl.bn);
+    if (pl.bn == 256 && pair_workers > 0) {
+      pl.cluster = 2;
+      pl.tiles_lane = (pl.tiles_lane + 1) / 2;
+      plan_schedule(pl, K / kBlock, pair_workers);
+      return pl;
+    }
   }
   plan_schedule(pl, K / kBlock, sm_count);
   return pl;
@@ -963,26 +1171,27 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
 
 // The fused w1/w3 GEMM: 128 activation rows x 128 output columns per tile
 // (MMA N = 256: 128 columns of w1 and the same 128 of w3).
-Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count) {
+Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count, int pair_workers) {
   Plan pl{};
   pl.swap = false;
   pl.bn = 256;
+  pl.cluster = pair_workers > 0 ? 2 : 1;
   pl.tiles_lane = static_cast<int>((M + 127) / 128);
+  pl.tiles_lane = (pl.tiles_lane + pl.cluster - 1) / pl.cluster;
   pl.tiles_col = static_cast<int>(inter / 128);
-  plan_schedule(pl, K / kBlock, sm_count);
+  plan_schedule(pl, K / kBlock, pair_workers > 0 ? pair_workers : sm_count);
   return pl;
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
-size_t plan_workspace(const Plan& pl) {
-  const size_t tiles = static_cast<size_t>(pl.tiles_lane) * pl.tiles_col;
-  return align256(tiles * sizeof(int)) + static_cast<size_t>(2) * pl.grid * pl.bn * 128 * sizeof(float);
+// Workspace: one arrival counter per output tile, then two partial slots per CTA.
+size_t plan_counter_bytes(const Plan& pl) {
+  return align256(static_cast<size_t>(pl.tiles_lane) * pl.tiles_col * pl.cluster * sizeof(int));
 }
 
-int sm_count_or_default() {
-  const DevInfo* d;
-  return current_device(&d) == FP8BLK_OK ? d->sm_count : 256;
+size_t plan_workspace(const Plan& pl) {
+  return plan_counter_bytes(pl) + static_cast<size_t>(2) * pl.grid * pl.cluster * pl.bn * 128 * sizeof(float);
 }
 
 template <class C>
@@ -994,6 +1203,12 @@ int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const
   if (d->device >= 64 || !attr_done[d->device]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_attr) != cudaSuccess)
       return FP8BLK_ERR_CUDA;
+    if constexpr (C::kSplitRegs) {
+      // setmaxnreg.inc would wait forever if the build gave the kernel fewer
+      // registers per thread than the split hands out: refuse to launch.
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs < C::kLaunchRegs) return FP8BLK_ERR_CUDA;
+    }
     if (d->device < 64) attr_done[d->device] = true;
   }
 #ifdef FP8BLK_TRACE
@@ -1001,23 +1216,59 @@ int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const
   const_cast<GemmParams&>(prm).trace_id = trace_counter++ & 7;
 #endif
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(prm.grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(prm.grid * C::CLUSTER));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes + extra_smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C::CLUSTER;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = C::CLUSTER > 1 ? 2 : 1;
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, ml, mc, mc2, prm));
+}
+
+// How many clusters of C fit on the device at once (0 if none, or if clusters
+// are disabled): the persistent schedule's worker count. Cached per device.
+template <class C>
+int cluster_workers(const DevInfo* d) {
+  if (!FP8BLK_CLUSTER_PAIRS) return 0;
+  static int cached[64] = {};
+  if (d->device < 64 && cached[d->device] != 0) return cached[d->device] > 0 ? cached[d->device] : 0;
+  int n = 0;
+  auto kern = fp8_gemm_kernel<C>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(d->sm_count));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C::CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();  // the query's error is not the caller's
+    }
+  }
+  if (d->device < 64) cached[d->device] = n > 0 ? n : -1;
+  return n > 0 ? n : 0;
 }
 
 }  // namespace
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 256;
-  return plan_workspace(make_plan(M, N, K, sm_count_or_default()));
+  const DevInfo* d;
+  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_plan(M, N, K, 256, 0));
+  return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d)));
 }
 
 int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
@@ -1035,7 +1286,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     return FP8BLK_ERR_ALIGN;
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  const Plan pl = make_plan(M, N, K, d->sm_count);
+  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d));
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
@@ -1044,9 +1295,8 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   prm.a_s = a_s;
   prm.w_s = w_s;
   prm.c = static_cast<__nv_bfloat16*>(c);
-  const size_t tiles = static_cast<size_t>(pl.tiles_lane) * pl.tiles_col;
   prm.counters = static_cast<int*>(workspace);
-  prm.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(tiles * sizeof(int)));
+  prm.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan_counter_bytes(pl));
   prm.err = d->err_word;
   prm.M = static_cast<int>(M);
   prm.N = static_cast<int>(N);
@@ -1066,13 +1316,16 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   const void* col_src = pl.swap ? a : w;
   const uint64_t lane_rows = static_cast<uint64_t>(pl.swap ? N : M);
   const uint64_t col_rows = static_cast<uint64_t>(pl.swap ? M : N);
+  // Cluster pairs load the column tile in two 128-row halves.
+  const uint32_t col_box = static_cast<uint32_t>(pl.cluster == 2 ? 128 : pl.bn);
   if (!make_kmajor_map(&ml, lane_src, lane_rows, static_cast<uint64_t>(K), 128) ||
-      !make_kmajor_map(&mc, col_src, col_rows, static_cast<uint64_t>(K), static_cast<uint32_t>(pl.bn)))
+      !make_kmajor_map(&mc, col_src, col_rows, static_cast<uint64_t>(K), col_box))
     return FP8BLK_ERR_CUDA;
 
   if (!pl.swap) {
+    if (pl.cluster == 2) return launch<CfgN256C2>(d, ml, mc, mc, prm, stream);
     if (pl.bn == 256) return launch<CfgN256>(d, ml, mc, mc, prm, stream);
-    return launch<CfgN128>(d, ml, mc, mc, prm, stream);
+    return launch<CfgN128E8>(d, ml, mc, mc, prm, stream);
   }
   switch (pl.bn) {
     case 16: return launch<CfgS16>(d, ml, mc, mc, prm, stream);
@@ -1132,7 +1385,9 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
 
 size_t swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t K) {
   if (M <= 0 || inter <= 0 || K <= 0) return 256;
-  return plan_workspace(make_swiglu_plan(M, inter, K, sm_count_or_default()));
+  const DevInfo* d;
+  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_swiglu_plan(M, inter, K, 256, 0));
+  return plan_workspace(make_swiglu_plan(M, inter, K, d->sm_count, cluster_workers<CfgSwiGLUC2>(d)));
 }
 
 // u = act_quant(bf16(silu(bf16(x w1^T))) * bf16(x w3^T)) in one kernel.
@@ -1150,7 +1405,7 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
     return FP8BLK_ERR_ALIGN;
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  const Plan pl = make_swiglu_plan(M, inter, K, d->sm_count);
+  const Plan pl = make_swiglu_plan(M, inter, K, d->sm_count, cluster_workers<CfgSwiGLUC2>(d));
   if (!workspace || workspace_bytes < plan_workspace(pl)) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   GemmParams prm{};
@@ -1159,9 +1414,8 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
   prm.w3_s = w3s;
   prm.uq = static_cast<uint8_t*>(uq);
   prm.us = us;
-  const size_t tiles = static_cast<size_t>(pl.tiles_lane) * pl.tiles_col;
   prm.counters = static_cast<int*>(workspace);
-  prm.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(tiles * sizeof(int)));
+  prm.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan_counter_bytes(pl));
   prm.err = d->err_word;
   prm.M = static_cast<int>(M);
   prm.N = static_cast<int>(inter);
@@ -1180,6 +1434,7 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
       !make_kmajor_map(&m1, w1, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64) ||
       !make_kmajor_map(&m3, w3, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64))
     return FP8BLK_ERR_CUDA;
+  if (pl.cluster == 2) return launch<CfgSwiGLUC2>(d, ml, m1, m3, prm, stream);
   return launch<CfgSwiGLU>(d, ml, m1, m3, prm, stream);
 }
 
@@ -1283,9 +1538,6 @@ int noalloc_scratch(int dev, void** out) {
 }
 
 // Bytes at the start of a plan's workspace that hold the tile counters.
-size_t plan_counter_bytes(const Plan& pl) {
-  return align256(static_cast<size_t>(pl.tiles_lane) * pl.tiles_col * sizeof(int));
-}
 
 }  // namespace
 }  // namespace fp8blk
@@ -1299,7 +1551,7 @@ extern "C" int fp8blk_gemm_noalloc(const void* a_e4m3, const float* a_s, const v
   if (M > 0 && N > 0 && K > 0 && K % kBlock == 0 && M <= lim && N <= lim && K <= lim) {
     const DevInfo* d;
     if (int st = current_device(&d)) return st;
-    const Plan pl = make_plan(M, N, K, d->sm_count);
+    const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d));
     if (plan_workspace(pl) > FP8BLK_NOALLOC_SCRATCH_BYTES) return FP8BLK_ERR_TOO_LARGE;
     void* scratch = nullptr;
     if (int st = noalloc_scratch(d->device, &scratch)) return st;
@@ -1322,12 +1574,15 @@ extern "C" int fp8blk_gemm(const void* a_e4m3, const float* a_s, const void* w_e
 }
 
 #ifdef FP8BLK_TRACE
-// Phase-trace reader (trace builds only): copies n stamps (16 per CTA) to host.
+// Phase-trace reader (trace builds only): copies n stamps (kTraceSlots per CTA) to host.
 extern "C" __attribute__((visibility("default"))) int fp8trace_read(unsigned long long* host, int n) {
   return cudaMemcpyFromSymbol(host, fp8blk::g_trace, sizeof(unsigned long long) * n) == cudaSuccess ? 0 : 1;
 }
+extern "C" __attribute__((visibility("default"))) int fp8trace_timeline(long long* host) {
+  return cudaMemcpyFromSymbol(host, fp8blk::g_timeline, sizeof(fp8blk::g_timeline)) == cudaSuccess ? 0 : 1;
+}
 extern "C" __attribute__((visibility("default"))) int fp8trace_clear(void) {
-  static unsigned long long zeros[8 * 4096 * 16];
+  static unsigned long long zeros[8 * 4096 * fp8blk::kTraceSlots];
   return cudaMemcpyToSymbol(fp8blk::g_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 1;
 }
 #endif

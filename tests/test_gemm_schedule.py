@@ -11,7 +11,12 @@ CTAs race on one slot."""
 import pytest
 
 
-def make_plan(M, N, K, sms):
+def make_plan(M, N, K, sms, pairs=None):
+    """pairs: co-resident CTA pairs of the cluster kernel (default sms // 2;
+    0 disables clusters). With pairs, large-M tiles of 128 x 256 run as
+    cluster pairs: the schedule's lane index counts pairs of 128-row tiles."""
+    if pairs is None:
+        pairs = sms // 2
     Kb = K // 128
     if M <= 128:
         swap = True
@@ -19,22 +24,27 @@ def make_plan(M, N, K, sms):
         tl, tc = -(-N // 128), -(-M // bn)
         if bn <= 32 and tl * tc <= sms:   # decode: one CTA per whole weight tile
             return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tl * tc, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
-                        tiles=tl * tc)
+                        tiles=tl * tc, cluster=1)
     else:
         swap = False
         bn = 128 if N <= 128 else 256
         tl, tc = -(-M // 128), -(-N // bn)
+    cluster = 1
+    workers = sms
+    if not swap and bn == 256 and pairs > 0:
+        cluster, workers = 2, pairs
+        tl = (tl + 1) // 2
     tiles = tl * tc
-    if tiles >= 2 * sms:
-        grid = sms
-        dp = tiles // sms - 1
-        sk_tiles = tiles - dp * sms
+    if tiles >= 2 * workers:
+        grid = workers
+        dp = tiles // workers - 1
+        sk_tiles = tiles - dp * workers
     else:
         dp = 0
         sk_tiles = tiles
-        grid = min(sms, tiles * Kb)
+        grid = min(workers, tiles * Kb)
     return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=grid, dp=dp, sk_tiles=sk_tiles,
-                sk_iters=sk_tiles * Kb, Kb=Kb, tiles=tiles)
+                sk_iters=sk_tiles * Kb, Kb=Kb, tiles=tiles, cluster=cluster)
 
 
 def units(p, c):
@@ -114,8 +124,55 @@ def test_decode_plan_uses_whole_tiles():
 
 
 def test_prefill_plan_is_hybrid():
-    p = make_plan(4096, 18432, 7168, 152)
+    p = make_plan(4096, 18432, 7168, 152, pairs=0)
     assert not p["swap"] and p["bn"] == 256 and p["dp"] == 14 and p["sk_tiles"] == 2304 - 14 * 152
+    # cluster pairs: 16 pair rows x 72 column tiles over 76 pairs
+    p = make_plan(4096, 18432, 7168, 152)
+    assert p["cluster"] == 2 and p["tl"] == 16 and p["grid"] == 76 and p["dp"] == 14
+    assert p["sk_tiles"] == 1152 - 14 * 76
+
+
+def tile_of(p, tile, rank):
+    """Mirror of the kernel's (schedule tile, cluster rank) -> (128-row lane tile,
+    column tile, counter index)."""
+    tl = (tile % p["tl"]) * p["cluster"] + rank
+    tc = tile // p["tl"]
+    return tl, tc, tile * p["cluster"] + rank
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 18432, 7168), (300, 700, 384), (129, 300, 128), (2048, 576, 7168),
+                                   (5000, 1000, 256)])
+def test_cluster_pairs_cover_every_output_tile_once(M, N, K):
+    p = make_plan(M, N, K, 152)
+    assert p["cluster"] == 2
+    m_tiles, n_tiles = -(-M // 128), -(-N // 256)
+    seen, counters = set(), set()
+    for tile in range(p["tiles"]):
+        for rank in range(2):
+            tl, tc, ctr = tile_of(p, tile, rank)
+            assert ctr not in counters and 0 <= ctr < p["tiles"] * 2
+            counters.add(ctr)
+            if tl < m_tiles:            # the second CTA of the last pair may own no rows
+                assert (tl, tc) not in seen
+                seen.add((tl, tc))
+            else:
+                assert tl == m_tiles and m_tiles % 2 == 1
+    assert seen == {(a, b) for a in range(m_tiles) for b in range(n_tiles)}
+
+
+def test_cluster_pair_slots_are_distinct():
+    """Stream-K partial slots: CTA (worker w, rank r) owns slots 2 (2 w + r) and
+    2 (2 w + r) + 1; the reducer of part q reads worker first + q, same rank."""
+    p = make_plan(4096, 7168, 18432, 152)
+    G = p["grid"]
+    owners = {}
+    for w in range(G):
+        for r in range(2):
+            for k in range(2):
+                s = 2 * (2 * w + r) + k
+                assert s not in owners
+                owners[s] = (w, r)
+    assert len(owners) == 4 * G
 
 
 # ---- grouped (per-expert) tiles and the routing permutation -------------------
