@@ -57,6 +57,8 @@ WORKLOADS = {
     "attn_wkv_a_m2048": ("linear", dict(M=2048, N=576, K=7168, frac=0.0, seed=synthetic.SEED_ATTN)),
     "attn_wq_b_m64": ("linear", dict(M=64, N=24576, K=1536, frac=0.0, seed=synthetic.SEED_ATTN)),
     "attn_wkv_b_m64": ("linear", dict(M=64, N=32768, K=512, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "attn_wq_a_m64": ("linear", dict(M=64, N=1536, K=7168, frac=0.0, seed=synthetic.SEED_ATTN)),
+    "attn_wkv_a_m64": ("linear", dict(M=64, N=576, K=7168, frac=0.0, seed=synthetic.SEED_ATTN)),
     "weight_dequant_18432x7168": ("dequant", dict(N=18432, K=7168, seed=synthetic.SEED_ATTN)),
     "prefill_ffn_4096": ("ffn", dict(M=4096, dim=7168, inter=18432, seed=synthetic.SEED_PREFILL)),
     "moe_t4096_uniform": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, seed=synthetic.SEED_MOE)),

@@ -81,6 +81,7 @@ struct GemmParams {
   int vec_store;       // C rows 16-byte aligned and N % 8 == 0
   int ue8m0;           // power-of-two scales for a fused act_quant (SwiGLU output, decode input)
   int whole_tiles;     // > 0: that many whole tiles, round-robin over the CTAs (no stream-K)
+  int ksplit;          // > 1: clusters of ksplit CTAs share one tile, each a K slice, reduced in DSMEM
   const __nv_bfloat16* x;  // fused decode linear: the bf16 activation [M, Kb * 128]
   int trace_id;        // phase-trace builds only: which of 8 trace slots this launch fills
 };
@@ -98,10 +99,12 @@ struct Sched {
   int c, j;
   long long it, it_end;
   int grouped_total;  // grouped GEMM: tile count read on the device (-1: dense)
+  int krank;          // split-K clusters: this CTA's K slice
 
-  __device__ Sched(const GemmParams& prm, int cta, int grouped_tiles = -1)
+  __device__ Sched(const GemmParams& prm, int cta, int grouped_tiles = -1, int k_rank = 0)
       : p(prm), c(cta), j(0), grouped_total(grouped_tiles >= 0 ? grouped_tiles
-                                                               : (prm.whole_tiles > 0 ? prm.whole_tiles : -1)) {
+                                                               : (prm.whole_tiles > 0 ? prm.whole_tiles : -1)),
+        krank(k_rank) {
     it = static_cast<long long>(c) * p.sk_iters / p.grid;
     it_end = static_cast<long long>(c + 1) * p.sk_iters / p.grid;
   }
@@ -110,6 +113,16 @@ struct Sched {
   __device__ long long cta_of(long long i) const { return ((i + 1) * p.grid - 1) / p.sk_iters; }
 
   __device__ bool next(Unit& u) {
+    if (p.ksplit > 1) {  // split-K cluster: one tile per cluster, K slice `krank` of it
+      if (j > 0) return false;
+      u.tile = c;
+      u.kb0 = static_cast<int>(static_cast<long long>(krank) * p.Kb / p.ksplit);
+      u.kb1 = static_cast<int>(static_cast<long long>(krank + 1) * p.Kb / p.ksplit);
+      u.part = 0;
+      u.nparts = 1;
+      ++j;
+      return true;
+    }
     if (grouped_total >= 0) {  // grouped: whole tiles, round-robin
       const long long t = c + static_cast<long long>(j) * p.grid;
       if (t >= grouped_total) return false;
@@ -440,7 +453,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Cluster rank, and the index of the schedule this CTA (pair) walks.
   const int rank = C::CLUSTER > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int worker = static_cast<int>(blockIdx.x) / C::CLUSTER;
+  // Split-K clusters (swapped tiles only): ksplit CTAs per tile.
+  const int ksplit = C::SWAP ? prm.ksplit : 1;
+  const int krank = ksplit > 1 ? static_cast<int>(blockIdx.x) % ksplit : 0;
+  const int worker = static_cast<int>(blockIdx.x) / (ksplit > 1 ? ksplit : C::CLUSTER);
   if (threadIdx.x == 0) FP8BLK_STAMP(0);
   // The next kernel on the stream may begin its prologue (and its weight
   // loads) now; it waits for this one before touching anything we write.
@@ -533,7 +549,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // activations follow once the previous kernel has completed.
       int npre = 0;
       if constexpr (!C::GROUPED) {
-        Sched pre(prm, worker);
+        Sched pre(prm, worker, -1, krank);
         Unit u;
         int nl2 = 0;
         while ((npre < C::STAGES || nl2 < C::kL2Ahead) && pre.next(u)) {
@@ -554,7 +570,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       griddep_wait();
       FP8BLK_STAMP(2);
-      Sched sch(prm, worker, grouped_tiles);
+      Sched sch(prm, worker, grouped_tiles, krank);
       Unit u;
       int st = 0;
       uint32_t ph = 0;
@@ -623,7 +639,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // (a loop run by a lone lane issues them far more slowly).
     const bool leader = elect_one_sync();
     constexpr uint32_t kIdesc = idesc_e4m3_f32(128, C::BN);
-    Sched sch(prm, worker, grouped_tiles);
+    Sched sch(prm, worker, grouped_tiles, krank);
     Unit u;
     int st = 0, pb = 0;
     uint32_t ph = 0, pph = 0;
@@ -829,7 +845,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       return r;
     };
 
-    Sched sch(prm, worker, grouped_tiles);
+    Sched sch(prm, worker, grouped_tiles, krank);
     Unit u;
     int pb = 0;
     uint32_t pph = 0;
@@ -967,7 +983,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       if (!ok) break;
       FP8BLK_TIC(t2);
-      if (u.nparts == 1) {
+      if (ksplit > 1) {
+        // Split-K cluster: park the partial in this CTA's (now idle) stage
+        // ring as [column][lane]; the cluster reduces it after the roles end.
+        float* part = reinterpret_cast<float*>(smem);
+#pragma unroll
+        for (int i = 0; i < C::kCpt; ++i) part[(group * C::kCpt + i) * 128 + row] = acc[i];
+      } else if (u.nparts == 1) {
         ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync);
       } else {
         // Stream-K fixup: publish this part, count arrivals, the last part sums.
@@ -1013,6 +1035,28 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #endif
   }
 
+  if constexpr (C::SWAP) {
+    if (ksplit > 1) {
+      // Split-K reduction: CTA krank sums columns [krank, krank + 1) * BN / ksplit
+      // of the tile over the ksplit partials, in rank order, and stores them.
+      cluster_sync();  // every partial of the cluster is in shared memory
+      if (warp >= C::kEpiWarp0) {
+        const TileInfo t = tile_info<C>(prm, worker, grp_rows, grp_mtiles, 0);
+        const int e = static_cast<int>(threadIdx.x) - C::kEpiWarp0 * 32;  // weight row of the tile
+        const int n = t.lane_y + e;
+        const int per = C::BN / ksplit;
+        const float* part = reinterpret_cast<const float*>(smem);
+        for (int jj = 0; jj < per; ++jj) {
+          const int j = krank * per + jj;
+          float sum = 0.0f;
+          for (int q = 0; q < ksplit; ++q) sum += ld_shared_cluster_f32(part + j * 128 + e, static_cast<uint32_t>(q));
+          const int m = t.col0 + j;
+          if (m < prm.M && n < prm.N) prm.c[static_cast<size_t>(m) * prm.ldc + n] = __float2bfloat16_rn(sum);
+        }
+      }
+      cluster_sync();  // no CTA leaves while a peer still reads its partial
+    }
+  }
   if (threadIdx.x == C::kEpiWarp0 * 32) FP8BLK_STAMP(8);
   tc_fence_before_sync();
   // Clusters: neither CTA leaves while its peer may still write its stages or
@@ -1087,12 +1131,19 @@ using CfgN128E8 = Cfg<128, false, FP8BLK_N128_STAGES, 4, 8>;
 #ifndef FP8BLK_SWAP_WHOLE_TILES
 #define FP8BLK_SWAP_WHOLE_TILES 1
 #endif
+// Widest token tile that still runs one whole weight tile per CTA.
+#ifndef FP8BLK_WHOLE_TILE_MAX_BN
+#define FP8BLK_WHOLE_TILE_MAX_BN 64
+#endif
 #ifndef FP8BLK_DECODE_OCC
 #define FP8BLK_DECODE_OCC 1
 #endif
 using CfgS16 = Cfg<16, true, FP8BLK_DECODE_STAGES, FP8BLK_DECODE_P, 4>;
 using CfgS32 = Cfg<32, true, (FP8BLK_DECODE_STAGES > 10 ? 10 : FP8BLK_DECODE_STAGES), 8, 4>;
-using CfgS64 = Cfg<64, true, 6, 4, 4>;
+#ifndef FP8BLK_S64_STAGES
+#define FP8BLK_S64_STAGES 6
+#endif
+using CfgS64 = Cfg<64, true, FP8BLK_S64_STAGES, 4, 4>;
 using CfgS128 = Cfg<128, true, 6, 4, 4>;
 // Fused w1/w3 GEMM with the SwiGLU + act_quant epilogue (dense and grouped),
 // and the grouped GEMM whose rows are scattered back to token order.
@@ -1109,6 +1160,7 @@ struct Plan {
   int bn;
   bool swap;
   int cluster;  // CTAs per schedule worker (2: lane-tile pairs); grid counts workers
+  int ksplit;   // > 1: split-K clusters of that many CTAs per tile; grid counts CTAs
   int tiles_lane, tiles_col;
   int grid, dp_waves, sk_tiles;
   long long sk_iters;
@@ -1131,23 +1183,48 @@ void plan_schedule(Plan& pl, int64_t Kb, int sm_count) {
   pl.sk_iters = static_cast<long long>(pl.sk_tiles) * Kb;
 }
 
+// Co-resident clusters of 2, 4 and 8 CTAs of the swapped kernel a plan would
+// launch (index 1, 2, 3); zero where none fit.
+struct SplitCaps {
+  int clusters[4];
+};
+
+int swap_bn(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
 // pair_workers: co-resident CTA pairs of the cluster kernel (0: no clusters).
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers) {
+// caps: split-K cluster capacity of the swapped kernel (null: no split-K).
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, const SplitCaps* caps) {
   Plan pl{};
   pl.cluster = 1;
+  pl.ksplit = 1;
   if (M <= 128) {
     pl.swap = true;
-    pl.bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    pl.bn = swap_bn(M);
     pl.tiles_lane = static_cast<int>((N + 127) / 128);
     pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
     const long long tiles = static_cast<long long>(pl.tiles_lane) * pl.tiles_col;
-    if (FP8BLK_SWAP_WHOLE_TILES && pl.bn <= 32 && tiles <= sm_count) {
+    if (FP8BLK_SWAP_WHOLE_TILES && pl.bn <= FP8BLK_WHOLE_TILE_MAX_BN && tiles <= sm_count && 2 * tiles >= sm_count) {
       // One CTA streams each whole weight tile: no stream-K fixup.
       pl.grid = static_cast<int>(tiles);
       pl.dp_waves = 1;
       pl.sk_tiles = 0;
       pl.sk_iters = 0;
       return pl;
+    }
+    // Few weight tiles: a cluster of ks CTAs per tile, each one K slice, the
+    // partials reduced in distributed shared memory (no global fixup).
+    if (caps && 2 * tiles < sm_count) {
+      const int64_t Kb = K / kBlock;
+      for (int ks = 8, idx = 3; ks >= 2; ks >>= 1, --idx) {
+        if (Kb >= 2 * ks && tiles * ks <= sm_count && tiles <= caps->clusters[idx]) {
+          pl.ksplit = ks;
+          pl.grid = static_cast<int>(tiles * ks);
+          pl.dp_waves = 1;
+          pl.sk_tiles = 0;
+          pl.sk_iters = 0;
+          return pl;
+        }
+      }
     }
     if (pl.bn <= 32) {
       plan_schedule(pl, K / kBlock, sm_count * FP8BLK_DECODE_OCC);
@@ -1196,7 +1273,7 @@ size_t plan_workspace(const Plan& pl) {
 
 template <class C>
 int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const CUtensorMap& mc2,
-           const GemmParams& prm, cudaStream_t stream, size_t extra_smem = 0) {
+           const GemmParams& prm, cudaStream_t stream, size_t extra_smem = 0, int kcluster = 1) {
   static bool attr_done[64] = {};
   auto kern = fp8_gemm_kernel<C>;
   const int smem_attr = C::FUSED ? kMaxDynSmem : C::kSmemBytes;
@@ -1224,11 +1301,11 @@ int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = C::CLUSTER;
+  attr[1].val.clusterDim.x = C::CLUSTER > 1 ? C::CLUSTER : kcluster;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = C::CLUSTER > 1 ? 2 : 1;
+  cfg.numAttrs = (C::CLUSTER > 1 || kcluster > 1) ? 2 : 1;
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, ml, mc, mc2, prm));
 }
 
@@ -1262,13 +1339,66 @@ int cluster_workers(const DevInfo* d) {
   return n > 0 ? n : 0;
 }
 
+// Co-resident clusters of `size` CTAs of kernel C (0 if none or on error).
+template <class C>
+int max_clusters(const DevInfo* d, int size) {
+  auto kern = fp8_gemm_kernel<C>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((d->sm_count / size) * size));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = size;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <class C>
+SplitCaps split_caps_of(const DevInfo* d) {
+  SplitCaps c{};
+  c.clusters[1] = max_clusters<C>(d, 2);
+  c.clusters[2] = max_clusters<C>(d, 4);
+  c.clusters[3] = max_clusters<C>(d, 8);
+  return c;
+}
+
+// Split-K capacity of the swapped kernel for M tokens, cached per device.
+const SplitCaps* split_caps(const DevInfo* d, int64_t M) {
+  static SplitCaps cache[64][4];
+  static bool done[64][4] = {};
+  const int bn = swap_bn(M);
+  const int bi = bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : 3;
+  if (d->device >= 64) return nullptr;
+  if (!done[d->device][bi]) {
+    cache[d->device][bi] = bi == 0 ? split_caps_of<CfgS16>(d)
+                           : bi == 1 ? split_caps_of<CfgS32>(d)
+                           : bi == 2 ? split_caps_of<CfgS64>(d)
+                                     : split_caps_of<CfgS128>(d);
+    done[d->device][bi] = true;
+  }
+  return &cache[d->device][bi];
+}
+
 }  // namespace
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 256;
   const DevInfo* d;
-  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_plan(M, N, K, 256, 0));
-  return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d)));
+  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_plan(M, N, K, 256, 0, nullptr));
+  return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M)));
 }
 
 int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
@@ -1286,7 +1416,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     return FP8BLK_ERR_ALIGN;
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d));
+  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
@@ -1308,6 +1438,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   prm.dp_waves = pl.dp_waves;
   prm.sk_tiles = pl.sk_tiles;
   prm.sk_iters = pl.sk_iters;
+  prm.ksplit = pl.ksplit;
   prm.vec_store = (N % 8 == 0 && is_aligned(c, 16)) ? 1 : 0;
   prm.ldc = static_cast<int>(N);
 
@@ -1328,10 +1459,10 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     return launch<CfgN128E8>(d, ml, mc, mc, prm, stream);
   }
   switch (pl.bn) {
-    case 16: return launch<CfgS16>(d, ml, mc, mc, prm, stream);
-    case 32: return launch<CfgS32>(d, ml, mc, mc, prm, stream);
-    case 64: return launch<CfgS64>(d, ml, mc, mc, prm, stream);
-    default: return launch<CfgS128>(d, ml, mc, mc, prm, stream);
+    case 16: return launch<CfgS16>(d, ml, mc, mc, prm, stream, 0, pl.ksplit);
+    case 32: return launch<CfgS32>(d, ml, mc, mc, prm, stream, 0, pl.ksplit);
+    case 64: return launch<CfgS64>(d, ml, mc, mc, prm, stream, 0, pl.ksplit);
+    default: return launch<CfgS128>(d, ml, mc, mc, prm, stream, 0, pl.ksplit);
   }
 }
 
@@ -1551,7 +1682,7 @@ extern "C" int fp8blk_gemm_noalloc(const void* a_e4m3, const float* a_s, const v
   if (M > 0 && N > 0 && K > 0 && K % kBlock == 0 && M <= lim && N <= lim && K <= lim) {
     const DevInfo* d;
     if (int st = current_device(&d)) return st;
-    const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d));
+    const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
     if (plan_workspace(pl) > FP8BLK_NOALLOC_SCRATCH_BYTES) return FP8BLK_ERR_TOO_LARGE;
     void* scratch = nullptr;
     if (int st = noalloc_scratch(d->device, &scratch)) return st;

@@ -276,6 +276,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Reads the fp32 at `local`'s shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ float ld_shared_cluster_f32(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // Every thread of every CTA of the cluster arrives, then waits for all.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -22,9 +22,15 @@ def make_plan(M, N, K, sms, pairs=None):
         swap = True
         bn = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
         tl, tc = -(-N // 128), -(-M // bn)
-        if bn <= 32 and tl * tc <= sms:   # decode: one CTA per whole weight tile
-            return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tl * tc, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
-                        tiles=tl * tc, cluster=1)
+        tiles = tl * tc
+        if bn <= 64 and tiles <= sms and 2 * tiles >= sms:   # decode: one CTA per whole weight tile
+            return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tiles, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
+                        tiles=tiles, cluster=1, ksplit=1)
+        if 2 * tiles < sms:          # few tiles: split-K clusters of ks CTAs per tile
+            for ks in (8, 4, 2):      # (co-resident clusters assumed: sms // ks)
+                if Kb >= 2 * ks and tiles * ks <= sms:
+                    return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tiles * ks, dp=1, sk_tiles=0, sk_iters=0,
+                                Kb=Kb, tiles=tiles, cluster=1, ksplit=ks)
     else:
         swap = False
         bn = 128 if N <= 128 else 256
@@ -44,10 +50,15 @@ def make_plan(M, N, K, sms, pairs=None):
         sk_tiles = tiles
         grid = min(workers, tiles * Kb)
     return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=grid, dp=dp, sk_tiles=sk_tiles,
-                sk_iters=sk_tiles * Kb, Kb=Kb, tiles=tiles, cluster=cluster)
+                sk_iters=sk_tiles * Kb, Kb=Kb, tiles=tiles, cluster=cluster, ksplit=1)
 
 
 def units(p, c):
+    if p["ksplit"] > 1:      # CTA c: tile c // ks, K slice c % ks (mirror of the split-K branch)
+        ks, Kb = p["ksplit"], p["Kb"]
+        r = c % ks
+        yield (c // ks, r * Kb // ks, (r + 1) * Kb // ks, 0, 1)
+        return
     G, Kb, S = p["grid"], p["Kb"], p["sk_iters"]
     for j in range(p["dp"]):
         yield (c + j * G, 0, Kb, 0, 1)
@@ -99,7 +110,7 @@ def test_schedule_covers_every_iteration_once(M, N, K, sms):
                 assert slot not in slots, "two partials in one slot"
                 slots[slot] = (tile, part)
                 parts.setdefault(tile, {})[part] = (c, kb0, kb1)
-            else:
+            elif p["ksplit"] == 1:
                 assert kb0 == 0 and kb1 == Kb
     assert len(cover) == p["tiles"] * Kb
     for tile, ps in parts.items():
@@ -116,10 +127,30 @@ def test_schedule_covers_every_iteration_once(M, N, K, sms):
             assert slots[2 * (cs[0] + i) + (1 if i == 0 else 0)] == (tile, i)
 
 
+@pytest.mark.parametrize("M,N,K", [(64, 1536, 7168), (64, 576, 7168), (8, 1536, 7168), (50, 300, 1024),
+                                   (1, 640, 4096), (100, 1536, 512), (17, 576, 7168)])
+def test_split_k_clusters(M, N, K):
+    """Few weight tiles: clusters of ks CTAs per tile, every CTA a non-empty K
+    slice, and the reduction's column slices (BN / ks per rank) cover the tile."""
+    p = make_plan(M, N, K, 152)
+    ks = p["ksplit"]
+    assert ks in (2, 4, 8) and p["grid"] == p["tiles"] * ks and p["grid"] <= 152
+    assert p["bn"] % ks == 0
+    per = p["bn"] // ks
+    cols = sorted(r * per + j for r in range(ks) for j in range(per))
+    assert cols == list(range(p["bn"]))
+    for t in range(p["tiles"]):
+        slices = [u for c in range(t * ks, (t + 1) * ks) for u in units(p, c)]
+        assert all(u[0] == t and u[2] - u[1] >= 2 for u in slices)
+        assert sorted((u[1], u[2]) for u in slices)[0][0] == 0 and max(u[2] for u in slices) == p["Kb"]
+
+
 def test_decode_plan_uses_whole_tiles():
     p = make_plan(8, 10944, 2048, 152)
     assert p["swap"] and p["bn"] == 16 and p["grid"] == 86 and p["dp"] == 1 and p["sk_iters"] == 0
-    p = make_plan(64, 10944, 2048, 152)      # BN 64: stream-K over the whole machine
+    p = make_plan(64, 10944, 2048, 152)      # BN 64: whole tiles as well
+    assert p["bn"] == 64 and p["grid"] == 86 and p["dp"] == 1
+    p = make_plan(128, 10944, 2048, 152)     # BN 128: stream-K over the whole machine
     assert p["grid"] == 152 and p["dp"] == 0
 
 

@@ -44,6 +44,10 @@ SHAPES = [
     (257, 128, 2048, 0.0),    # BN 128 path
     (1000, 1000, 128, 0.0),   # single K block, N % 8 == 0
     (512, 2304, 1536, 0.0),   # several data-parallel waves
+    (64, 1536, 7168, 0.0),    # few weight tiles: split-K clusters (8 CTAs per tile)
+    (8, 1536, 7168, 0.01),
+    (50, 300, 1024, 0.0),     # split-K clusters of 4, ragged M and N
+    (1, 640, 4096, 0.01),     # split-K, one token
 ]
 
 
@@ -88,6 +92,19 @@ def test_gemm_deterministic_and_workspace_restored():
     tiles = (10944 + 127) // 128
     assert torch.count_nonzero(wsb[: tiles * 4]) == 0      # counters back at zero
     c2 = fb.fp8_gemm(a, a_s, q, s, ws=wsb)
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 576, 7168), (4096, 7168, 18432)])
+def test_gemm_split_paths_deterministic(M, N, K):
+    """Split-K clusters (few weight tiles) and stream-K cluster pairs reduce
+    partials in a fixed order: two calls give identical bits."""
+    dev = torch.device("cuda")
+    x = synthetic.device_activations(M, K, 77, dev)
+    a, a_s = fb.act_quant(x)
+    q, s = fb.weight_quant(synthetic.device_normal((N, K), 78, 0.02, dev))
+    c1 = fb.fp8_gemm(a, a_s, q, s)
+    c2 = fb.fp8_gemm(a, a_s, q, s)
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
     assert fb.last_device_error() == 0
 
