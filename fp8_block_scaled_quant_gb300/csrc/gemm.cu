@@ -42,6 +42,7 @@
 #include "fp8blk.h"
 #include "host.cuh"
 #include "ptx.cuh"
+#include "quotient.cuh"
 
 namespace fp8blk {
 
@@ -345,6 +346,7 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
     if (!epi_sync()) return false;
     amax = fmaxf(x[row], x[128 + row]);
     const float sc = quant_block_scale(amax, p.ue8m0 != 0);
+    const float rc = __frcp_rn(sc);  // the block's quotients: see quotient.cuh
     if (row < t.lane_valid) {
       const size_t r = static_cast<size_t>(t.lane_y + row);
       uint4* dst = reinterpret_cast<uint4*>(p.uq + r * p.ldc + t.col0 + group * 64);
@@ -354,8 +356,8 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = v * 16 + e * 4;
-          w[e] = pack_e4m3x4(__fdiv_rn(acc[i], sc), __fdiv_rn(acc[i + 1], sc), __fdiv_rn(acc[i + 2], sc),
-                             __fdiv_rn(acc[i + 3], sc));
+          w[e] = pack_e4m3x4(div_by_scale(acc[i], sc, rc), div_by_scale(acc[i + 1], sc, rc),
+                             div_by_scale(acc[i + 2], sc, rc), div_by_scale(acc[i + 3], sc, rc));
         }
         dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
       }
@@ -782,10 +784,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off, 16));
           const float sc = quant_block_scale(amax, prm.ue8m0 != 0);
-          const uint32_t lo = pack_e4m3x4(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc), __fdiv_rn(f[2], sc),
-                                          __fdiv_rn(f[3], sc));
-          const uint32_t hi = pack_e4m3x4(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc), __fdiv_rn(f[6], sc),
-                                          __fdiv_rn(f[7], sc));
+          const float rc = __frcp_rn(sc);  // the block's quotients: see quotient.cuh
+          const uint32_t lo = pack_e4m3x4(div_by_scale(f[0], sc, rc), div_by_scale(f[1], sc, rc),
+                                          div_by_scale(f[2], sc, rc), div_by_scale(f[3], sc, rc));
+          const uint32_t hi = pack_e4m3x4(div_by_scale(f[4], sc, rc), div_by_scale(f[5], sc, rc),
+                                          div_by_scale(f[6], sc, rc), div_by_scale(f[7], sc, rc));
           if (valid) {
             uint8_t* rowp = act_smem + kb * (C::BN * 128) + (m >> 3) * 1024 + (m & 7) * 128;
             *reinterpret_cast<uint2*>(rowp + (((sub >> 1) ^ (m & 7)) << 4) + (sub & 1) * 8) = make_uint2(lo, hi);

@@ -15,6 +15,7 @@
 #include "fp8blk.h"
 #include "host.cuh"
 #include "ptx.cuh"
+#include "quotient.cuh"
 
 namespace fp8blk {
 namespace {
@@ -84,10 +85,13 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint4* __re
 #pragma unroll
       for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off, 16));
       const float sc = block_scale(amax, ue8m0);
-      const uint32_t lo = e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
-                          (static_cast<uint32_t>(e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc))) << 16);
-      const uint32_t hi = e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
-                          (static_cast<uint32_t>(e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc))) << 16);
+      const float rc = __frcp_rn(sc);  // the block's quotients: see quotient.cuh
+      const uint32_t lo = e4m3x2(div_by_scale(f[0], sc, rc), div_by_scale(f[1], sc, rc)) |
+                          (static_cast<uint32_t>(e4m3x2(div_by_scale(f[2], sc, rc), div_by_scale(f[3], sc, rc)))
+                           << 16);
+      const uint32_t hi = e4m3x2(div_by_scale(f[4], sc, rc), div_by_scale(f[5], sc, rc)) |
+                          (static_cast<uint32_t>(e4m3x2(div_by_scale(f[6], sc, rc), div_by_scale(f[7], sc, rc)))
+                           << 16);
       if (blk[u] < nblocks) {
         q[blk[u] * 16 + sub] = make_uint2(lo, hi);
         if (sub == 0) s[blk[u]] = sc;
