@@ -57,7 +57,10 @@ void init_device(int dev) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
-constexpr int64_t kFusedLinearMaxM = 2;
+#ifndef FP8BLK_FUSED_LINEAR_MAX_M
+#define FP8BLK_FUSED_LINEAR_MAX_M 2
+#endif
+constexpr int64_t kFusedLinearMaxM = FP8BLK_FUSED_LINEAR_MAX_M;
 
 }  // namespace
 

@@ -41,6 +41,11 @@ __device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t w) {
+  __nv_bfloat162 b;
+  *reinterpret_cast<uint32_t*>(&b) = w;
+  return b;
+}
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---- act_quant -------------------------------------------------------------
@@ -52,7 +57,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // the warp (the shuffles use the full mask); lanes past the end compute on
 // zeros and store nothing.
 constexpr int kAqThreads = 256;
-constexpr int kAqUnroll = 2;
+#ifndef FP8BLK_AQ_UNROLL
+#define FP8BLK_AQ_UNROLL 4
+#endif
+constexpr int kAqUnroll = FP8BLK_AQ_UNROLL;
 
 __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint4* __restrict__ x, uint2* __restrict__ q,
                                                                float* __restrict__ s, int64_t nblocks,
@@ -77,21 +85,25 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint4* __re
     }
 #pragma unroll
     for (int u = 0; u < kAqUnroll; ++u) {
-      const float f[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
-                          bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      // amax on the bf16 pairs (|.| by clearing the sign bits; bf16 max is
+      // exact), then across the 16 lanes of the block.
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      __nv_bfloat162 m = __hmax2(__hmax2(as_bf162(w[0] & 0x7FFF7FFFu), as_bf162(w[1] & 0x7FFF7FFFu)),
+                                 __hmax2(as_bf162(w[2] & 0x7FFF7FFFu), as_bf162(w[3] & 0x7FFF7FFFu)));
+      float amax = fmaxf(__low2float(m), __high2float(m));
 #pragma unroll
       for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off, 16));
       const float sc = block_scale(amax, ue8m0);
       const float rc = __frcp_rn(sc);  // the block's quotients: see quotient.cuh
-      const uint32_t lo = e4m3x2(div_by_scale(f[0], sc, rc), div_by_scale(f[1], sc, rc)) |
-                          (static_cast<uint32_t>(e4m3x2(div_by_scale(f[2], sc, rc), div_by_scale(f[3], sc, rc)))
-                           << 16);
-      const uint32_t hi = e4m3x2(div_by_scale(f[4], sc, rc), div_by_scale(f[5], sc, rc)) |
-                          (static_cast<uint32_t>(e4m3x2(div_by_scale(f[6], sc, rc), div_by_scale(f[7], sc, rc)))
-                           << 16);
+      const float2 sn2 = make_float2(-sc, -sc), r2 = make_float2(rc, rc);
+      uint32_t c[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 qk = div2_by_scale(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), sn2, r2);
+        c[k] = e4m3x2(qk.x, qk.y);
+      }
+      const uint32_t lo = c[0] | (c[1] << 16);
+      const uint32_t hi = c[2] | (c[3] << 16);
       if (blk[u] < nblocks) {
         q[blk[u] * 16 + sub] = make_uint2(lo, hi);
         if (sub == 0) s[blk[u]] = sc;
@@ -167,27 +179,47 @@ __device__ __forceinline__ uint32_t dequant_pair(uint16_t two, float sc) {
 constexpr int kDqThreads = 256;
 
 // Vector path: K % 16 == 0 and both buffers 16-byte aligned. Thread i handles
-// the 16 consecutive elements of vector i (one 128-block column, so one scale).
+// the 16 consecutive elements of vector i (one 128-block column, so one
+// scale); each pass issues kDqUnroll vector loads before any arithmetic so that
+// several are in flight per thread.
+#ifndef FP8BLK_DQ_UNROLL
+#define FP8BLK_DQ_UNROLL 1
+#endif
+constexpr int kDqUnroll = FP8BLK_DQ_UNROLL;
+
 template <typename Index>
 __global__ void __launch_bounds__(kDqThreads) weight_dequant_vec_kernel(const uint4* __restrict__ q,
                                                                         const float* __restrict__ s,
                                                                         uint4* __restrict__ out, Index nvec,
                                                                         Index kvec, Index nbk) {
   const Index stride = static_cast<Index>(gridDim.x) * kDqThreads;
-  for (Index i = static_cast<Index>(blockIdx.x) * kDqThreads + threadIdx.x; i < nvec; i += stride) {
-    const Index n = i / kvec;
-    const Index kv = i - n * kvec;
-    const float sc = __ldg(s + (n / kBlock) * nbk + (kv >> 3));   // 8 vectors per 128 columns
-    const uint4 v = __ldcs(q + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[8];
+  for (Index i0 = static_cast<Index>(blockIdx.x) * kDqThreads + threadIdx.x; i0 < nvec; i0 += stride * kDqUnroll) {
+    uint4 v[kDqUnroll];
+    float sc[kDqUnroll];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      o[2 * j] = dequant_pair(static_cast<uint16_t>(w[j] & 0xFFFF), sc);
-      o[2 * j + 1] = dequant_pair(static_cast<uint16_t>(w[j] >> 16), sc);
+    for (int u = 0; u < kDqUnroll; ++u) {
+      const Index i = i0 + u * stride;
+      if (i < nvec) {
+        const Index n = i / kvec;
+        const Index kv = i - n * kvec;
+        sc[u] = __ldg(s + (n / kBlock) * nbk + (kv >> 3));  // 8 vectors per 128 columns
+        v[u] = __ldcs(q + i);
+      }
     }
-    __stcs(out + 2 * i, make_uint4(o[0], o[1], o[2], o[3]));
-    __stcs(out + 2 * i + 1, make_uint4(o[4], o[5], o[6], o[7]));
+#pragma unroll
+    for (int u = 0; u < kDqUnroll; ++u) {
+      const Index i = i0 + u * stride;
+      if (i >= nvec) break;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        o[2 * j] = dequant_pair(static_cast<uint16_t>(w[j] & 0xFFFF), sc[u]);
+        o[2 * j + 1] = dequant_pair(static_cast<uint16_t>(w[j] >> 16), sc[u]);
+      }
+      __stcs(out + 2 * i, make_uint4(o[0], o[1], o[2], o[3]));
+      __stcs(out + 2 * i + 1, make_uint4(o[4], o[5], o[6], o[7]));
+    }
   }
 }
 

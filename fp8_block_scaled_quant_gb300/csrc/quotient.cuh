@@ -30,4 +30,14 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
   return __uint_as_float(__float_as_uint(q) | (__float_as_uint(q0) & 0x80000000u));
 }
 
+// The same for two values at once (packed f32x2 multiply and FMAs: per
+// component the identical operations and roundings). sn2 = (-s, -s),
+// r2 = (r, r).
+__device__ __forceinline__ float2 div2_by_scale(float2 x, float2 sn2, float2 r2) {
+  const float2 q0 = __fmul2_rn(x, r2);
+  const float2 q = __ffma2_rn(__ffma2_rn(q0, sn2, x), r2, q0);
+  return make_float2(__uint_as_float(__float_as_uint(q.x) | (__float_as_uint(q0.x) & 0x80000000u)),
+                     __uint_as_float(__float_as_uint(q.y) | (__float_as_uint(q0.y) & 0x80000000u)));
+}
+
 }  // namespace fp8blk

@@ -2,7 +2,8 @@
 // csrc/quotient.cuh) against CUDA's IEEE division: for every positive finite
 // bf16 amax, the act_quant scale s (fp32: RN(max(amax, 1e-4) / 448); ue8m0:
 // that rounded up to a power of two) and every finite bf16 x with |x| <= amax,
-// the e4m3 codes of div_by_scale(x, s, RN(1/s)) and RN(x / s) must agree.
+// the e4m3 codes of div_by_scale(x, s, RN(1/s)) and RN(x / s) must agree, and
+// the packed div2_by_scale must give div_by_scale's bits in both lanes.
 // Prints one line per format and exits non-zero on any difference.
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -29,10 +30,15 @@ __global__ void check(bool ue8m0, unsigned long long* counts) {
   for (uint32_t xb = threadIdx.x; xb < 65536u; xb += blockDim.x) {
     if ((xb & 0x7FFFu) > amax_bits) continue;  // |x| <= amax (this also excludes inf and nan)
     const float x = __uint_as_float(xb << 16);
-    const auto got = __nv_cvt_float_to_fp8(fp8blk::div_by_scale(x, s, r), __NV_SATFINITE, __NV_E4M3);
+    const float q = fp8blk::div_by_scale(x, s, r);
+    const float2 q2 = fp8blk::div2_by_scale(make_float2(x, -x), make_float2(-s, -s), make_float2(r, r));
+    const auto got = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
     const auto want = __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3);
+    const float qn = fp8blk::div_by_scale(-x, s, r);
     ++n;
-    bad += got != want;
+    // the packed form must give the scalar form's bits in both lanes
+    bad += (got != want) || (__float_as_uint(q2.x) != __float_as_uint(q)) ||
+           (__float_as_uint(q2.y) != __float_as_uint(qn));
   }
   atomicAdd(counts, n);
   atomicAdd(counts + 1, bad);
