@@ -382,7 +382,7 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(shape, dev, torch, fb, qs[0], ss[0], min(steps, 20000), hbm_bound, step_bytes, flops)
+        e2e = run_e2e(shape, dev, torch, fb, qs, ss, min(steps, 20000), hbm_bound, step_bytes, flops)
 
     out = {
         "value": metric_val, "unit": unit, "ms_per_step": el_max / steps * 1e3,
@@ -399,16 +399,19 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     return out
 
 
-def run_e2e(shape, dev, torch, fb, q, s, n, hbm_bound, step_bytes, flops):
+def run_e2e(shape, dev, torch, fb, qs, ss, n, hbm_bound, step_bytes, flops):
     """End to end through fp8blk_linear_host: each step copies X from pinned
-    host memory, runs the layer, and copies Y back; timed on the stream."""
+    host memory, runs the layer, and copies Y back; timed on the stream and by
+    the wall clock (the larger counts). The weight rotates over the same
+    copies as the device-timed leg, so no step finds its weight in L2."""
     M, N, K = shape["M"], shape["N"], shape["K"]
     xh = [synthetic.device_activations(M, K, shape["seed"] + 7 + i, dev, shape["frac"]).cpu().pin_memory()
           for i in range(4)]
     yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
     ws = fb.workspace(fb.linear_host_workspace_bytes(M, N, K), dev, "bench_e2e")
+    R = len(qs)
     for i in range(3):
-        fb.linear_host(xh[i % 4], q, s, yh[i % 4], ws=ws)
+        fb.linear_host(xh[i % 4], qs[i % R], ss[i % R], yh[i % 4], ws=ws)
     stream = torch.cuda.current_stream(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -416,7 +419,7 @@ def run_e2e(shape, dev, torch, fb, q, s, n, hbm_bound, step_bytes, flops):
     t0 = time.time()
     start.record(stream)
     for i in range(n):
-        fb.linear_host(xh[i % 4], q, s, yh[i % 4], ws=ws)
+        fb.linear_host(xh[i % 4], qs[i % R], ss[i % R], yh[i % 4], ws=ws)
     end.record(stream)
     torch.cuda.synchronize()
     wall = time.time() - t0
@@ -425,7 +428,7 @@ def run_e2e(shape, dev, torch, fb, q, s, n, hbm_bound, step_bytes, flops):
     val = units / el / (1e9 if hbm_bound else 1e12)
     return {"value": val, "unit": "GB/s" if hbm_bound else "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
             "d2h_bytes_per_step": M * N * 2, "steps": n, "ms_per_step": el / n * 1e3,
-            "api": "fp8blk_linear_host (pinned host buffers)"}
+            "api": "fp8blk_linear_host (pinned host buffers)", "weights": f"rotating over {R} copies"}
 
 
 def run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
