@@ -215,12 +215,22 @@ def barrier():
 # traffic figures recorded from ncu (profiles/), valid only for unchanged sources
 # ---------------------------------------------------------------------------
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def kernel_source_digest() -> str:
+    """Digest of the kernel sources' code: comments and whitespace removed, so
+    an edit to a comment keeps a profile's traffic record valid and any change
+    to the code invalidates it. (A string literal holding "//" would lose its
+    tail here; the sources have none that matters to the digest.)"""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_quant_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        if not name.endswith((".cu", ".cuh", ".h")):
+            continue
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            code = "".join(_COMMENT.sub(" ", f.read()).split())
+        h.update(name.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

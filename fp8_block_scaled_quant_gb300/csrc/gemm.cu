@@ -3,17 +3,23 @@
 //
 //   C[m, n] = sum_kb a_s[m, kb] * w_s[n/128, kb] * sum_{k in kb} a[m, k] w[n, k]
 //
-// Design (one CTA per SM, warp-specialised, persistent):
+// Design (persistent, warp-specialised CTAs):
 //   warp 0      TMA producer: per 128-wide K block, one 128x128 tile of the
 //               "lane" operand and one BN x 128 tile of the "column" operand
-//               into a STAGES-deep shared-memory ring (mbarrier full/empty).
-//   warp 1      MMA issuer: four tcgen05.mma kind::f8f6f4 (K = 32 each) per K
-//               block into a fresh TMEM partial (a ring of P partials of BN
-//               fp32 columns), then tcgen05.commit to free the smem stage and
-//               to publish the partial.
-//   warps 2..   promotion / epilogue: tcgen05.ld each partial, multiply by
-//               the block's a_s * w_s and add into fp32 registers (the pages'
-//               acc += dot(a, b) * a_s * b_s), then bf16 stores.
+//               into a STAGES-deep shared-memory ring (mbarrier full/empty);
+//               the first STAGES weight tiles are requested before the
+//               programmatic-dependent-launch wait.
+//   warp 1      MMA issuer: the whole warp walks the schedule and waits; one
+//               elected lane issues four tcgen05.mma kind::f8f6f4 (K = 32
+//               each) per K block into a fresh TMEM partial (a ring of P
+//               partials of BN fp32 columns), then tcgen05.commit to free the
+//               smem stage and to publish the partial.
+//   epilogue    promotion: tcgen05.ld each partial, multiply by the block's
+//   warps       a_s * w_s and add into fp32 registers (the pages'
+//               acc += dot(a, b) * a_s * b_s); at the end of a tile bf16
+//               stores, or the SwiGLU + act_quant epilogue, or scattered rows.
+//   Large-M tiles (BN = 256, two column groups) run 12 warps: warps 0-3 give
+//   registers to the two epilogue warpgroups (setmaxnreg 56 / 224).
 //
 // Operand roles. For M > 128 the activation rows are the MMA's M (TMEM lanes)
 // and weight rows its N (columns), BN = 128 or 256. For decode-sized M <= 128
@@ -21,12 +27,21 @@
 // number per CTA tile, and the M tokens (padded to BN = 16..128 by the TMA
 // zero fill) are the columns, each with its own activation scale.
 //
-// Schedule. Tiles are numbered lane-tile fastest. The first dp_waves * grid
-// tiles go round-robin to whole CTAs (data-parallel waves: concurrent tiles
-// share column-operand tiles in L2); the rest are split stream-K: the K-block
-// iterations of those tiles are divided evenly over all CTAs, and a tile cut
-// between CTAs is finished by whichever of them arrives last on its counter,
-// which sums the fp32 partials in part order (deterministic) and stores bf16.
+// Schedules (all deterministic).
+//   - Large M, BN = 256: CTA pairs in clusters of 2 over adjacent 128-row lane
+//     tiles; each CTA loads its own lane tile and one half of the weight tile,
+//     multicast into both CTAs.
+//   - Decode with SMs/2..SMs weight tiles: one CTA per whole tile.
+//   - Decode with fewer tiles: split-K clusters of 2, 4 or 8 CTAs per tile,
+//     partials reduced in rank order through distributed shared memory.
+//   - Otherwise (and for the pairs): tiles numbered lane-tile fastest; the first
+//     dp_waves * workers tiles go round-robin to whole workers (data-parallel
+//     waves: concurrent tiles share column-operand tiles in L2); the rest are
+//     split stream-K, and a tile cut between workers is finished by whichever
+//     of them arrives last on its counter, summing the fp32 partials in part
+//     order and storing bf16.
+//   - Grouped (MoE) tiles: (group, column tile, 128-row tile), whole tiles
+//     round-robin.
 //
 // Every mbarrier wait is bounded (2 s): on expiry the CTA records an error bit,
 // stops issuing work, waits (bounded) for its own copies and MMAs in flight,
