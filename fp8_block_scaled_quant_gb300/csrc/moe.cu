@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
     const long long t = __ldg(perm + r) / topk;
     const uint4* src = xq + t * dv;
     uint4* dst = xg + r * dv;
+#pragma unroll 4
     for (int v = lane; v < dv; v += 32) dst[v] = __ldg(src + v);
     for (int k = lane; k < kb; k += 32) xgs[r * kb + k] = __ldg(xs + t * kb + k);
   }
@@ -167,6 +168,12 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
 
 // y[t, :] = bf16( sum over slots j in order of w[t, j] * o[t * topk + j, :] ),
 // fp32 accumulation; slots routed to no valid expert contribute nothing.
+// y[t] = bf16(sum over slots j in order of w[t, j] * o[t * topk + j]) in fp32.
+// For topk <= kCombineMax all slots' ids, weights and output vectors are
+// requested before the first FMA (the loads are independent; the FMAs keep the
+// slot order); larger topk takes the plain loop.
+constexpr int kCombineMax = 8;
+
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restrict__ o, const int* __restrict__ idx,
                                                           const float* __restrict__ w, int T, int topk, int E,
                                                           int dim, uint4* __restrict__ y) {
@@ -177,16 +184,34 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
     const long long t = v / dv;
     const int c = static_cast<int>(v - t * dv);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < topk; ++j) {
-      const int e = __ldg(idx + t * topk + j);
-      if (e < 0 || e >= E) continue;
-      const float wj = __ldg(w + t * topk + j);
-      const uint4 ov = __ldg(o + (t * topk + j) * dv + c);
+    auto add = [&](float wj, const uint4& ov) {
       const uint32_t u[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         acc[2 * q] = fmaf(wj, __uint_as_float(u[q] << 16), acc[2 * q]);
         acc[2 * q + 1] = fmaf(wj, __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
+      }
+    };
+    if (topk <= kCombineMax) {
+      int e[kCombineMax];
+      float wj[kCombineMax];
+      uint4 ov[kCombineMax];
+#pragma unroll
+      for (int j = 0; j < kCombineMax; ++j) {
+        e[j] = j < topk ? __ldg(idx + t * topk + j) : -1;
+        wj[j] = j < topk ? __ldg(w + t * topk + j) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kCombineMax; ++j)
+        if (e[j] >= 0 && e[j] < E) ov[j] = __ldg(o + (t * topk + j) * dv + c);
+#pragma unroll
+      for (int j = 0; j < kCombineMax; ++j)
+        if (e[j] >= 0 && e[j] < E) add(wj[j], ov[j]);
+    } else {
+      for (int j = 0; j < topk; ++j) {
+        const int ej = __ldg(idx + t * topk + j);
+        if (ej < 0 || ej >= E) continue;
+        add(__ldg(w + t * topk + j), __ldg(o + (t * topk + j) * dv + c));
       }
     }
     uint32_t r[4];
