@@ -36,6 +36,10 @@ SHAPES = [
     (1, 10944, 2048, 0.01),   # decode
     (8, 10944, 2048, 0.01),
     (64, 10944, 2048, 0.01),
+    (5, 2999, 1024, 0.0),     # swapped, ragged last weight tile (N % 128 = 55)
+    (24, 4000, 1024, 0.0),    # swapped, BN 32
+    (40, 9000, 2048, 0.01),   # swapped, BN 64, ragged last weight tile
+    (8, 1000, 8192, 0.0),     # swapped, 64 K blocks through the stage and TMEM rings
     (17, 576, 7168, 0.0),     # swapped, BN 32, N not 128-aligned
     (100, 1536, 512, 0.0),    # swapped, BN 128
     (128, 260, 384, 0.0),
@@ -235,5 +239,6 @@ def test_fused_decode_linear(M, N, K, fmt):
     c = fb.fp8_gemm(a, a_s, q, s, scale_fmt=fmt)
     if -(-N // 128) <= torch.cuda.get_device_properties(0).multi_processor_count:
         assert torch.equal(y.view(torch.int16), c.view(torch.int16))
+    assert_gemm_close(dev_to_bits(c), oracle.gemm(xq, xs, wq, ws), what=f"act_quant + fp8_gemm {M}x{N}x{K}")
     assert_gemm_close(dev_to_bits(y), oracle.gemm(xq, xs, wq, ws), what=f"fused linear {M}x{N}x{K}")
     assert fb.last_device_error() == 0
