@@ -385,8 +385,10 @@ extern "C" int fp8blk_moe_grouped_gemm(const void* x_e4m3, const float* x_s, con
   void* o = ws + l.o;
 
   if (int st = launch_permute(d, topk_idx, n, E, counts, offsets, mtiles, perm, cs)) return st;
-  const int gather_grid = d->sm_count * 8;
-  moe_gather_kernel<<<gather_grid, 256, 0, cs>>>(static_cast<const uint4*>(x_e4m3), x_s, perm, offsets,
+  // One warp per routed row (at most T * topk of them), as many CTAs as that
+  // takes: the resident CTAs then copy one contiguous window of rows at a time.
+  const long long gather_grid = (static_cast<long long>(n) + 7) / 8;
+  moe_gather_kernel<<<static_cast<unsigned>(gather_grid < (1LL << 30) ? gather_grid : (1LL << 30)), 256, 0, cs>>>(static_cast<const uint4*>(x_e4m3), x_s, perm, offsets,
                                                  static_cast<int>(E), static_cast<int>(topk), static_cast<int>(dim),
                                                  reinterpret_cast<uint4*>(xg), xgs);
   if (int st = launch_status()) return st;
@@ -395,9 +397,9 @@ extern "C" int fp8blk_moe_grouped_gemm(const void* x_e4m3, const float* x_s, con
     return st;
   if (int st = grouped_scatter_run(uq, us, w2_e4m3, w2_s, o, perm, n, E, dim, inter, offsets, mtiles, cs))
     return st;
+  // One thread per 8-element output vector (grid-stride past 2^30 CTAs).
   const long long vecs = T * (dim / 8);
-  const long long cap = static_cast<long long>(d->sm_count) * 8;
-  const int grid = static_cast<int>((vecs + 255) / 256 < cap ? (vecs + 255) / 256 : cap);
+  const int grid = static_cast<int>((vecs + 255) / 256 < (1LL << 30) ? (vecs + 255) / 256 : (1LL << 30));
   moe_combine_kernel<<<grid, 256, 0, cs>>>(static_cast<const uint4*>(o), topk_idx, topk_w, static_cast<int>(T),
                                            static_cast<int>(topk), static_cast<int>(E), static_cast<int>(dim),
                                            static_cast<uint4*>(y_bf16));

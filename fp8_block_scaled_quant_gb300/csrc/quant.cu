@@ -244,6 +244,17 @@ int grid_for(const DevInfo* d, int64_t work_items, int threads, int per_sm) {
   return static_cast<int>(need < cap ? (need < 1 ? 1 : need) : cap);
 }
 
+// One thread per work item, as many CTAs as that takes (the grid-stride loops
+// cover anything past 2^30 CTAs). For the dequant stream this beats a grid
+// capped at a few CTAs per SM: at any moment the resident CTAs work on one
+// contiguous window of the matrix, and it measured 60 us against 79 us for a
+// 18432 x 7168 weight (8 CTAs per SM, each striding over the whole matrix).
+int grid_all(int64_t work_items, int threads) {
+  const int64_t need = (work_items + threads - 1) / threads;
+  const int64_t cap = int64_t{1} << 30;
+  return static_cast<int>(need < 1 ? 1 : need < cap ? need : cap);
+}
+
 }  // namespace
 }  // namespace fp8blk
 
@@ -316,7 +327,7 @@ extern "C" int fp8blk_weight_dequant(const void* q_e4m3, const float* s, int64_t
   const int64_t nbk = (K + kBlock - 1) / kBlock;
   if (K % 16 == 0 && is_aligned(q_e4m3, 16) && is_aligned(out_bf16, 16)) {
     const int64_t kvec = K / 16, nvec = N * kvec;
-    const int grid = grid_for(d, nvec, kDqThreads, 8);
+    const int grid = grid_all(nvec, kDqThreads);
     if (nvec < (int64_t{1} << 31)) {
       weight_dequant_vec_kernel<uint32_t><<<grid, kDqThreads, 0, cs>>>(
           static_cast<const uint4*>(q_e4m3), s, static_cast<uint4*>(out_bf16), static_cast<uint32_t>(nvec),
@@ -328,7 +339,7 @@ extern "C" int fp8blk_weight_dequant(const void* q_e4m3, const float* s, int64_t
     }
   } else {
     const int64_t total = N * K;
-    const int grid = grid_for(d, total, kDqThreads, 8);
+    const int grid = grid_all(total, kDqThreads);
     weight_dequant_scalar_kernel<<<grid, kDqThreads, 0, cs>>>(static_cast<const uint8_t*>(q_e4m3), s,
                                                               static_cast<__nv_bfloat16*>(out_bf16), total, K, nbk);
   }
