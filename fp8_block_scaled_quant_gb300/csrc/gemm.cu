@@ -1250,7 +1250,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, 
     }
   } else {
     pl.swap = false;
-    pl.bn = N <= 128 ? 128 : 256;
+    // 128 x 128 tiles (four TMEM partials) where 128 x 256 tiles would be too
+    // few to fill the machine twice, or too short (K <= 512) for two partials
+    // to carry the MMA of the next tile past the current tile's epilogue.
+    const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+    pl.bn = (N <= 128 || K / kBlock <= 4 || tiles256 < 2LL * sm_count) ? 128 : 256;
     pl.tiles_lane = static_cast<int>((M + 127) / 128);
     pl.tiles_col = static_cast<int>((N + pl.bn - 1) / pl.bn);
     if (pl.bn == 256 && pair_workers > 0) {

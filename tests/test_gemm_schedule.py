@@ -33,7 +33,8 @@ def make_plan(M, N, K, sms, pairs=None):
                                 Kb=Kb, tiles=tiles, cluster=1, ksplit=ks)
     else:
         swap = False
-        bn = 128 if N <= 128 else 256
+        tiles256 = -(-M // 128) * -(-N // 256)
+        bn = 128 if (N <= 128 or Kb <= 4 or tiles256 < 2 * sms) else 256
         tl, tc = -(-M // 128), -(-N // bn)
     cluster = 1
     workers = sms
@@ -154,6 +155,16 @@ def test_decode_plan_uses_whole_tiles():
     assert p["grid"] == 152 and p["dp"] == 0
 
 
+def test_tile_width_rule():
+    """128-column tiles where 128 x 256 tiles would number fewer than two per
+    SM or K <= 512; 128 x 256 cluster pairs for the large prefill shapes."""
+    for M, N, K in [(2048, 1536, 7168), (2048, 576, 7168), (2048, 32768, 512), (300, 576, 1024)]:
+        assert make_plan(M, N, K, 152)["bn"] == 128
+    for M, N, K in [(4096, 18432, 7168), (4096, 7168, 18432), (2048, 24576, 1536), (1300, 7000, 640)]:
+        p = make_plan(M, N, K, 152)
+        assert p["bn"] == 256 and p["cluster"] == 2
+
+
 def test_prefill_plan_is_hybrid():
     p = make_plan(4096, 18432, 7168, 152, pairs=0)
     assert not p["swap"] and p["bn"] == 256 and p["dp"] == 14 and p["sk_tiles"] == 2304 - 14 * 152
@@ -171,10 +182,12 @@ def tile_of(p, tile, rank):
     return tl, tc, tile * p["cluster"] + rank
 
 
-@pytest.mark.parametrize("M,N,K", [(4096, 18432, 7168), (300, 700, 384), (129, 300, 128), (2048, 576, 7168),
-                                   (5000, 1000, 256)])
-def test_cluster_pairs_cover_every_output_tile_once(M, N, K):
-    p = make_plan(M, N, K, 152)
+# (SM counts chosen so that each shape takes 128 x 256 tiles in cluster pairs:
+# at least two such tiles per SM, K > 512.)
+@pytest.mark.parametrize("M,N,K,sms", [(4096, 18432, 7168, 152), (300, 700, 640, 4), (129, 300, 1024, 2),
+                                       (2048, 576, 7168, 16), (5000, 1000, 640, 64), (1300, 7000, 640, 152)])
+def test_cluster_pairs_cover_every_output_tile_once(M, N, K, sms):
+    p = make_plan(M, N, K, sms)
     assert p["cluster"] == 2
     m_tiles, n_tiles = -(-M // 128), -(-N // 256)
     seen, counters = set(), set()

@@ -44,7 +44,8 @@ SHAPES = [
     (100, 1536, 512, 0.0),    # swapped, BN 128
     (128, 260, 384, 0.0),
     (129, 320, 256, 0.0),     # first non-swapped size, ragged M tail
-    (300, 576, 1024, 0.02),   # N = 576: last block partial, BN 256
+    (300, 576, 1024, 0.02),   # N = 576: last block partial, 128-column tiles (few tiles)
+    (1300, 7000, 640, 0.0),   # 128 x 256 cluster pairs: odd row-tile count, ragged N
     (257, 128, 2048, 0.0),    # BN 128 path
     (1000, 1000, 128, 0.0),   # single K block, N % 8 == 0
     (512, 2304, 1536, 0.0),   # several data-parallel waves
