@@ -81,6 +81,8 @@ def lib():
             L.orc_expert_ffn_u.restype = i32
             L.orc_moe_token.argtypes = [vp, vp, vp, vp, i64, i64] + [vp] * 6 + [i64, i64, i32, vp]
             L.orc_moe_token.restype = i32
+            L.orc_moe_gate.argtypes = [vp, vp, i64, i64, i64, i64, i64, i32, ctypes.c_float, i32, vp, vp]
+            L.orc_moe_gate.restype = i32
             L.orc_e4m3_encode_array.argtypes = [vp, i64, vp]
             L.orc_bf16_encode_array.argtypes = [vp, i64, vp]
             _lib = L
@@ -280,3 +282,21 @@ def moe_tokens(xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s, tokens, ue8m0=Fal
             raise MemoryError("oracle MoE token failed")
         y[i] = row
     return y
+
+
+# ---- MoE gate (scores, group-limited top-k, weights) -----------------------------
+
+def moe_gate(logits, bias, n_groups: int, topk_groups: int, topk: int, sigmoid: bool,
+             route_scale: float = 1.0, normalize: bool = True):
+    """logits fp32 [T, E] (+ bias fp32 [E] or None) -> (indices int32 [T, topk]
+    in descending selection-key order, weights fp32 [T, topk])."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    b = None if bias is None else _c(bias, np.float32)
+    idx = np.empty((T, topk), np.int32)
+    w = np.empty((T, topk), np.float32)
+    rc = lib().orc_moe_gate(_ptr(logits), None if b is None else _ptr(b), T, E, n_groups, topk_groups, topk,
+                            int(bool(sigmoid)), float(route_scale), int(bool(normalize)), _ptr(idx), _ptr(w))
+    if rc:
+        raise ValueError("gate shape outside the rules")
+    return idx, w

@@ -29,6 +29,15 @@
  *        steps 2-5: per expert, the tokens routed to it, weighted by their
  *        gate weight, summed into y.
  *   [ML] same guide, 1.2 module map (MLP / Expert): w2(silu(w1 x) * w3 x).
+ *   [GT] same guide, 8.4 (the Gate: with n_groups > 1 the scores are viewed as
+ *        groups, a group's score is its max without a bias and the sum of its
+ *        top two with one, the top topk_groups groups are kept and the rest
+ *        masked to -inf, then the top-k experts are picked) and 3.3 (score_func
+ *        softmax or sigmoid, route_scale, expert groups and limited groups per
+ *        config); "Repository overview" page, MoE data flow (scores, optional
+ *        group masking, top-k indices, gather the original scores, normalize,
+ *        route_scale); "User Guide", 7 FAQ (the gate bias of the dim-7168
+ *        configs, used with sigmoid scores).
  *
  * Readings where the pages are silent:
  *   - "x / s" and "amax / 448" are IEEE fp32 divisions, correctly rounded.
@@ -396,6 +405,96 @@ int orc_moe_token(const uint8_t *xq, const float *xs,
     for (int64_t c = 0; c < dim; ++c)
         y_row[c] = orc_bf16_encode(acc[c]);
     free(acc); free(o);
+    return 0;
+}
+
+/* ---- MoE gate: scores, group-limited top-k, weights [GT] ----------------- */
+
+/* Per token t: scores s[e] from logits l[t, e] (sigmoid 1/(1+e^-l), or the
+ * softmax over all E), computed in fp64 and rounded to fp32 once; selection
+ * keys z[e] = s[e] + bias[e] in fp32 (z = s without a bias). With G > 1
+ * groups of E/G consecutive experts: a group's score is its largest z (no
+ * bias) or the fp32 sum of its two largest z (bias); the TG best groups stay,
+ * the others' experts are masked out. The K best unmasked z give the experts,
+ * in descending z order; every tie goes to the lower index. The weights are
+ * the chosen experts' scores s (not z), divided by their sum when `normalize`
+ * is set, times route_scale: fp64, rounded to fp32 once.
+ * Returns 0, or -1 on a shape the rules cannot apply to. */
+int orc_moe_gate(const float *logits, const float *bias, int64_t T, int64_t E, int64_t G, int64_t TG,
+                 int64_t K, int sigmoid, float route_scale, int normalize, int32_t *idx, float *w)
+{
+    if (E < 1 || G < 1 || E % G || TG < 1 || TG > G || K < 1 || K > TG * (E / G))
+        return -1;
+    if (bias && G > 1 && E / G < 2)
+        return -1;
+    float *s = malloc(sizeof(float) * E), *z = malloc(sizeof(float) * E), *gs = malloc(sizeof(float) * G);
+    int *allowed = malloc(sizeof(int) * E), *keep = malloc(sizeof(int) * G), *taken = malloc(sizeof(int) * E);
+    if (!s || !z || !gs || !allowed || !keep || !taken) {
+        free(s); free(z); free(gs); free(allowed); free(keep); free(taken);
+        return -1;
+    }
+    const int64_t GS = E / G;
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        if (sigmoid) {
+            for (int64_t e = 0; e < E; ++e)
+                s[e] = (float)(1.0 / (1.0 + exp(-(double)l[e])));
+        } else {
+            double m = (double)l[0], sum = 0.0;
+            for (int64_t e = 1; e < E; ++e)
+                if ((double)l[e] > m)
+                    m = (double)l[e];
+            for (int64_t e = 0; e < E; ++e)
+                sum += exp((double)l[e] - m);
+            for (int64_t e = 0; e < E; ++e)
+                s[e] = (float)(exp((double)l[e] - m) / sum);
+        }
+        for (int64_t e = 0; e < E; ++e) {
+            z[e] = bias ? s[e] + bias[e] : s[e];
+            allowed[e] = 1;
+            taken[e] = 0;
+        }
+        if (G > 1) {
+            for (int64_t g = 0; g < G; ++g) {
+                /* the two largest z of the group, first index first on ties */
+                int64_t a = g * GS, b = -1;
+                for (int64_t e = g * GS + 1; e < (g + 1) * GS; ++e)
+                    if (z[e] > z[a])
+                        a = e;
+                for (int64_t e = g * GS; e < (g + 1) * GS; ++e)
+                    if (e != a && (b < 0 || z[e] > z[b]))
+                        b = e;
+                gs[g] = bias ? z[a] + z[b] : z[a];
+                keep[g] = 0;
+            }
+            for (int64_t r = 0; r < TG; ++r) {
+                int64_t best = -1;
+                for (int64_t g = 0; g < G; ++g)
+                    if (!keep[g] && (best < 0 || gs[g] > gs[best]))
+                        best = g;
+                keep[best] = 1;
+            }
+            for (int64_t e = 0; e < E; ++e)
+                allowed[e] = keep[e / GS];
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < K; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e)
+                if (allowed[e] && !taken[e] && (best < 0 || z[e] > z[best]))
+                    best = e;
+            taken[best] = 1;
+            idx[t * K + j] = (int32_t)best;
+            sum += (double)s[best];
+        }
+        for (int64_t j = 0; j < K; ++j) {
+            double v = (double)s[idx[t * K + j]];
+            if (normalize)
+                v /= sum;
+            w[t * K + j] = (float)(v * (double)route_scale);
+        }
+    }
+    free(s); free(z); free(gs); free(allowed); free(keep); free(taken);
     return 0;
 }
 

@@ -24,6 +24,7 @@ SEED_DECODE = 1
 SEED_PREFILL = 2
 SEED_ATTN = 3
 SEED_MOE = 4
+SEED_GATE = 5
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -126,3 +127,13 @@ def moe_routing(T: int, E: int, topk: int, seed: int, zipf_s: float = 0.0):
     w = np.exp(sel)
     w /= w.sum(axis=1, keepdims=True)
     return idx.astype(np.int32), w.astype(np.float32)
+
+
+def gate_logits(T: int, E: int, seed: int, std: float = 1.0) -> np.ndarray:
+    """Gate logits fp32 [T, E] ~ N(0, std^2), one draw per (token, expert)."""
+    return (rng(seed).standard_normal((T, E)) * std).astype(np.float32)
+
+
+def gate_bias(E: int, seed: int, std: float = 0.1) -> np.ndarray:
+    """Per-expert gate bias fp32 [E] ~ N(0, std^2)."""
+    return (rng(seed + 1000).standard_normal(E) * std).astype(np.float32)
