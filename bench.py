@@ -63,6 +63,8 @@ WORKLOADS = {
     "prefill_ffn_4096": ("ffn", dict(M=4096, dim=7168, inter=18432, seed=synthetic.SEED_PREFILL)),
     "moe_t4096_uniform": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, seed=synthetic.SEED_MOE)),
     "moe_t4096_zipf": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=1.2, seed=synthetic.SEED_MOE)),
+    "moe_gate_t4096_e256": ("gate", dict(T=4096, E=256, groups=8, kept=4, k=8, route_scale=2.5,
+                                         seed=synthetic.SEED_GATE)),
 }
 DEFAULT = "decode_linear_m8"
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
@@ -598,6 +600,61 @@ def run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     }
 
 
+def run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
+    """The 671B gate (sigmoid scores, per-expert bias, 8 groups with 4 kept,
+    top-8, route_scale 2.5) on T tokens of fp32 logits, then the routing
+    permutation of its output: the step that turns gate logits into the
+    grouped GEMMs' row order."""
+    T, E, G, TG, k, scale, seed = (shape[n] for n in ("T", "E", "groups", "kept", "k", "route_scale", "seed"))
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
+    R = min(128, max(2, math.ceil(3 * l2 / (T * E * 4))))
+    ls = [torch.from_numpy(synthetic.gate_logits(T, E, seed + i)).to(dev) for i in range(R)]
+    b = torch.from_numpy(synthetic.gate_bias(E, seed)).to(dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+
+    def gate(i):
+        fb.moe_gate(ls[i % R], b, G, TG, k, fb.SCORE_SIGMOID, scale, True, idx=idx, w=w)
+
+    def step(i):
+        gate(i)
+        fb.moe_permute(idx, E)
+
+    for i in range(3):
+        step(i)
+    stream = torch.cuda.current_stream(dev)
+    g_warm = make_runs(step, warmup, 50, torch, args.eager)
+    g_main = make_runs(step, steps, 50, torch, args.eager)
+    g_gate = make_runs(gate, steps, 50, torch, args.eager)
+    for g in g_warm:
+        g.replay()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        el, t0, t1 = timed_replay(g_main, stream, torch)
+        el_gate, _, _ = timed_replay(g_gate, stream, torch)
+    assert fb.last_device_error(dev) == 0
+    b_gate = T * E * 4 + E * 4 + T * k * 8            # logits, bias in; ids, weights out
+    b_step = b_gate + T * k * 4 + T * k * 4 + (2 * E + 1) * 4   # + ids read by the permutation, perm, counts
+    el_max, units = reduce_over_ranks(el, steps * b_step, dev)
+    achieved = b_gate / (el_gate / steps) / 1e9
+    return {
+        "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
+        "clocks": clk.summary(t0, t1), "gpu_launches": 2 * steps,
+        "kernels_us": {"gate_and_permute": el / steps * 1e6, "gate_alone": el_gate / steps * 1e6},
+        "roofline": {"bound": "hbm", "kernel": "moe_gate", "achieved": achieved, "peak": peaks["hbm"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None,
+                     "peak_source": f"hbm_gbs ({peaks['src']})", "algorithmic_bytes_per_launch": b_gate,
+                     "kernel_us": el_gate / steps * 1e6},
+        "e2e": None,
+        "config": {"workload": args.workload, "T": T, "E": E, "groups": G, "kept_groups": TG, "topk": k,
+                   "score": "sigmoid + per-expert bias", "route_scale": scale,
+                   "logits": "fp32 N(0,1), bias N(0,0.01)",
+                   "l2": f"logits rotate over {R} copies ({R * T * E * 4 / 1e6:.0f} MB > 3x L2)"},
+        "dtype": "f32",
+    }
+
+
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
@@ -719,6 +776,8 @@ def main():
         res = run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     elif kind == "moe":
         res = run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
+    elif kind == "gate":
+        res = run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     else:
         res = run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     cpu = None

@@ -313,10 +313,37 @@ def moe_permute(topk_idx: torch.Tensor, E: int):
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     perm = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
-    vp, i64 = ctypes.c_void_p, ctypes.c_int64
-    f = _set_types("fp8blk_moe_permute", [vp, i64, i64, i64, vp, vp, vp, vp])
-    _check(f(_ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm), _stream(dev)), "moe_permute")
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    nbytes = int(_set_types("fp8blk_moe_permute_workspace_bytes", [i64] * 3, sz)(T, k, E))
+    ws = workspace(nbytes, dev, "moe_permute")
+    f = _set_types("fp8blk_moe_permute", [vp, i64, i64, i64, vp, vp, vp, vp, sz, vp])
+    _check(f(_ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(ws), ws.numel(), _stream(dev)),
+           "moe_permute")
     return counts, offsets, perm[: T * k]
+
+
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
+
+
+def moe_gate(logits: torch.Tensor, bias: torch.Tensor | None = None, n_groups: int = 1, topk_groups: int = 1,
+             topk: int = 8, score_func: int = SCORE_SIGMOID, route_scale: float = 1.0, normalize: bool = True,
+             idx: torch.Tensor | None = None, w: torch.Tensor | None = None):
+    """Gate logits fp32 [T, E] (+ bias fp32 [E]) -> (topk_idx int32 [T, topk],
+    topk_w fp32 [T, topk]): scores, group-limited top-k, weights."""
+    _need(logits, torch.float32, "logits")
+    if bias is not None:
+        _need(bias, torch.float32, "bias", ndim=1)
+    T, E = logits.shape
+    dev = logits.device
+    if idx is None:
+        idx = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    if w is None:
+        w = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    f = _set_types("fp8blk_moe_gate", [vp, vp, i64, i64, i64, i64, i64, i32, ctypes.c_float, i32, vp, vp, vp])
+    _check(f(_ptr(logits), _ptr(bias), T, E, n_groups, topk_groups, topk, score_func, float(route_scale),
+             int(bool(normalize)), _ptr(idx), _ptr(w), _stream(dev)), "moe_gate")
+    return idx, w
 
 
 def moe_workspace_bytes(T: int, topk: int, E: int, dim: int, inter: int) -> int:

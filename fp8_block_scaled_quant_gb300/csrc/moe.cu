@@ -4,9 +4,12 @@
 // summed per token with the gate weights. The pages' loop (a host-side
 // bincount + tolist(), then one Python iteration per expert) becomes:
 //
-//   moe_permute   one CTA: histogram of expert ids, exclusive scans (row
-//                 offsets and 128-row tile counts per expert), and a stable
-//                 scatter of the (token, slot) pairs into expert order;
+//   moe_permute   three passes: per chunk of 1024 pairs, each pair's rank
+//                 among the chunk's earlier pairs of its expert and the
+//                 chunk's histogram; one CTA turns the histograms into
+//                 per-(chunk, expert) bases, row offsets and 128-row tile
+//                 counts; a scatter puts every pair at base + rank (a stable
+//                 sort of the (token, slot) pairs by expert id);
 //   moe_gather    the quantised token rows (and their scales) in that order;
 //   grouped w1/w3 GEMM with the SwiGLU + act_quant epilogue (gemm.cu);
 //   grouped w2 GEMM, each row written back to its (token, slot) position;
@@ -77,74 +80,87 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int* total
   return r;
 }
 
-// One CTA groups the n (token, slot) pairs by expert, keeping pair order
-// (t * topk + j) inside each expert: counts, offsets[E + 1] (exclusive scan),
-// mtiles[E + 1] (exclusive scan of ceil(count / 128)), and perm[offsets[e] + r]
-// = the r-th pair of expert e. Pairs whose expert id is outside [0, E) join
-// no expert and set an error bit.
-__global__ void __launch_bounds__(kPermThreads) moe_permute_kernel(const int* __restrict__ idx, int n, int E,
+// The permutation groups the n (token, slot) pairs by expert, keeping pair
+// order (t * topk + j) inside each expert: counts, offsets[E + 1] (exclusive
+// scan), mtiles[E + 1] (exclusive scan of ceil(count / 128)), and
+// perm[offsets[e] + r] = the r-th pair of expert e. Pairs whose expert id is
+// outside [0, E) join no expert and set an error bit.
+//
+// Rank pass: CTA c takes pairs [1024 c, 1024 c + 1024). A pair's rank among
+// the chunk's earlier pairs of its expert is its rank inside its warp
+// (__match_any_sync) plus the counts of that expert in the chunk's earlier
+// warps; hist[c][e] is the chunk's count of expert e.
+constexpr int kPermChunk = kPermThreads;
+
+__global__ void __launch_bounds__(kPermThreads) moe_rank_kernel(const int* __restrict__ idx, int n, int E,
+                                                                int* __restrict__ rank, int* __restrict__ hist,
+                                                                unsigned* err) {
+  extern __shared__ int wtab[];  // [32][E]: per-warp counts, then their prefix over warps
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int k = tid; k < 32 * E; k += kPermThreads) wtab[k] = 0;
+  __syncthreads();
+  const int i = static_cast<int>(blockIdx.x) * kPermChunk + tid;
+  int e = i < n ? __ldg(idx + i) : -1;
+  if (i < n && (e < 0 || e >= E)) atomicOr(err, kDevErrBadExpert);
+  if (e < 0 || e >= E) e = -1;
+  const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+  const int wrank = __popc(m & ((1u << lane) - 1u));
+  if (e >= 0 && wrank == 0) wtab[warp * E + e] = __popc(m);
+  __syncthreads();
+  for (int x = tid; x < E; x += kPermThreads) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = wtab[w * E + x];
+      wtab[w * E + x] = run;
+      run += c;
+    }
+    hist[static_cast<size_t>(blockIdx.x) * E + x] = run;
+  }
+  __syncthreads();
+  if (e >= 0) rank[i] = wtab[warp * E + e] + wrank;
+}
+
+// Offsets pass (one CTA, thread x for expert x): the histograms become
+// per-chunk bases (offsets[x] + the expert's pairs in earlier chunks), and
+// counts, offsets and tile counts are written.
+__global__ void __launch_bounds__(kPermThreads) moe_offsets_kernel(int* __restrict__ hist_base, int nchunks, int E,
                                                                    int* __restrict__ counts,
                                                                    int* __restrict__ offsets,
-                                                                   int* __restrict__ mtiles,
-                                                                   int* __restrict__ perm, unsigned* err) {
-  extern __shared__ int sm[];
-  int* cnt = sm;              // [E]
-  int* base = cnt + E;        // [E] running output position per expert
-  int* wsum = base + E;       // [40] scan scratch
-  int* wtab = wsum + 40;      // [32][E] per-warp counts of the current chunk
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  for (int e = tid; e < E; e += kPermThreads) cnt[e] = 0;
-  __syncthreads();
-  bool bad = false;
-  for (int i = tid; i < n; i += kPermThreads) {
-    const int e = __ldg(idx + i);
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else bad = true;
-  }
-  if (bad) atomicOr(err, kDevErrBadExpert);
-  __syncthreads();
-
-  const int c = tid < E ? cnt[tid] : 0;
-  int total_rows, total_tiles;
-  const int off = block_exclusive_scan(c, wsum, &total_rows);
-  const int mt = block_exclusive_scan((c + 127) / 128, wsum, &total_tiles);
+                                                                   int* __restrict__ mtiles) {
+  __shared__ int wsum[40];
+  const int tid = threadIdx.x;
+  int total = 0;
   if (tid < E) {
-    if (counts) counts[tid] = c;
+    for (int c = 0; c < nchunks; ++c) {
+      const int h = hist_base[static_cast<size_t>(c) * E + tid];
+      hist_base[static_cast<size_t>(c) * E + tid] = total;
+      total += h;
+    }
+  }
+  int rows, tiles;
+  const int off = block_exclusive_scan(total, wsum, &rows);
+  const int mt = block_exclusive_scan((total + 127) / 128, wsum, &tiles);
+  if (tid < E) {
+    if (counts) counts[tid] = total;
     offsets[tid] = off;
     if (mtiles) mtiles[tid] = mt;
-    base[tid] = off;
+    for (int c = 0; c < nchunks; ++c) hist_base[static_cast<size_t>(c) * E + tid] += off;
   }
   if (tid == 0) {
-    offsets[E] = total_rows;
-    if (mtiles) mtiles[E] = total_tiles;
+    offsets[E] = rows;
+    if (mtiles) mtiles[E] = tiles;
   }
-  __syncthreads();
+}
 
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < n; c0 += kPermThreads) {
-    for (int k = tid; k < 32 * E; k += kPermThreads) wtab[k] = 0;
-    __syncthreads();
-    const int i = c0 + tid;
-    int e = i < n ? __ldg(idx + i) : -1;
-    if (e < 0 || e >= E) e = -1;
-    const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
-    const int wrank = __popc(m & lt_mask);
-    if (e >= 0 && wrank == 0) wtab[warp * E + e] = __popc(m);
-    __syncthreads();
-    if (e >= 0) {
-      int pre = 0;
-      for (int w = 0; w < warp; ++w) pre += wtab[w * E + e];
-      perm[base[e] + pre + wrank] = i;
-    }
-    __syncthreads();
-    for (int x = tid; x < E; x += kPermThreads) {
-      int s = 0;
-      for (int w = 0; w < 32; ++w) s += wtab[w * E + x];
-      base[x] += s;
-    }
-    __syncthreads();
-  }
+// Scatter pass: perm[base[chunk][e] + rank] = pair, for every valid pair.
+__global__ void __launch_bounds__(256) moe_scatter_kernel(const int* __restrict__ idx, const int* __restrict__ rank,
+                                                          const int* __restrict__ base, int n, int E,
+                                                          int* __restrict__ perm) {
+  const int i = static_cast<int>(blockIdx.x) * 256 + static_cast<int>(threadIdx.x);
+  if (i >= n) return;
+  const int e = __ldg(idx + i);
+  if (e < 0 || e >= E) return;
+  perm[__ldg(base + static_cast<size_t>(i / kPermChunk) * E + e) + __ldg(rank + i)] = i;
 }
 
 // xg[r] = xq[perm[r] / topk] and its scales, for r < offsets[E] (one warp per row).
@@ -226,20 +242,197 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
 
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
-size_t permute_smem_bytes(int64_t E) { return static_cast<size_t>(2 * E + 40 + 32 * E) * sizeof(int); }
+
+// Scratch of the permutation: ranks [n], then per-(chunk, expert) bases.
+size_t permute_scratch_bytes(int64_t n, int64_t E) {
+  const int64_t nchunks = (n + kPermChunk - 1) / kPermChunk;
+  return align256(static_cast<size_t>(n) * 4) + align256(static_cast<size_t>(nchunks) * E * 4);
+}
 
 int launch_permute(const DevInfo* d, const int* idx, int64_t n, int64_t E, int* counts, int* offsets, int* mtiles,
-                   int* perm, cudaStream_t stream) {
+                   int* perm, void* scratch, cudaStream_t stream) {
   static bool attr_done[64] = {};
-  const size_t smem = permute_smem_bytes(kMaxExperts);
   if (d->device >= 64 || !attr_done[d->device]) {
-    if (cudaFuncSetAttribute(moe_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(moe_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             32 * kMaxExperts * 4) != cudaSuccess)
       return FP8BLK_ERR_CUDA;
     if (d->device < 64) attr_done[d->device] = true;
   }
-  moe_permute_kernel<<<1, kPermThreads, permute_smem_bytes(E), stream>>>(
-      idx, static_cast<int>(n), static_cast<int>(E), counts, offsets, mtiles, perm, d->err_word);
+  const int nchunks = static_cast<int>((n + kPermChunk - 1) / kPermChunk);
+  int* rank = static_cast<int*>(scratch);
+  int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) + align256(static_cast<size_t>(n) * 4));
+  if (nchunks > 0) {
+    moe_rank_kernel<<<nchunks, kPermThreads, static_cast<size_t>(32) * E * 4, stream>>>(
+        idx, static_cast<int>(n), static_cast<int>(E), rank, base, d->err_word);
+    if (int st = launch_status()) return st;
+  }
+  moe_offsets_kernel<<<1, kPermThreads, 0, stream>>>(base, nchunks, static_cast<int>(E), counts, offsets, mtiles);
+  if (int st = launch_status()) return st;
+  if (n > 0) {
+    moe_scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(idx, rank, base, static_cast<int>(n),
+                                                                                   static_cast<int>(E), perm);
+  }
+  return launch_status();
+}
+
+// ---- MoE gate ------------------------------------------------------------------
+// Per token ("Administrator & Developer Guide", 8.4 and 3.3; "Repository
+// overview" MoE data flow): scores s from the logits (sigmoid, or softmax over
+// the E experts), selection keys z = s + bias (z = s without a bias); with G > 1
+// groups of E/G consecutive experts a group scores its largest z (no bias) or
+// the sum of its two largest (bias), and only the TG best groups' experts stay
+// eligible; the K best eligible z give the experts in descending order (ties:
+// lower index); the weights are their s, divided by the sum of the K when
+// `normalize`, times route_scale.
+//
+// One warp per token. Lane l holds experts [l V, l V + V) (E = 32 V), so a
+// group is a run of 32 / G whole lanes: group maxima and top-two pairs merge
+// with shuffles inside that run. Each top-k round is a warp argmax over 64-bit
+// keys (order-preserving bits of z, then the complement of the index).
+constexpr int kGateWarps = 8;
+
+__device__ __forceinline__ uint64_t gate_key(float z, int e) {
+  const uint32_t u = __float_as_uint(z);
+  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+template <int V>
+__global__ void __launch_bounds__(kGateWarps * 32) moe_gate_kernel(const float* __restrict__ logits,
+                                                                   const float* __restrict__ bias, int T, int G,
+                                                                   int TG, int K, int sigmoid, float route_scale,
+                                                                   int normalize, int32_t* __restrict__ idx,
+                                                                   float* __restrict__ w) {
+  constexpr int E = 32 * V;
+  const int lane = threadIdx.x & 31;
+  const int t = static_cast<int>(blockIdx.x) * kGateWarps + static_cast<int>(threadIdx.x >> 5);
+  if (t >= T) return;  // whole warps leave together
+  const float* l = logits + static_cast<size_t>(t) * E + lane * V;
+  float s[V], z[V];
+  if (sigmoid) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) s[i] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-__ldg(l + i))));
+  } else {
+    float x[V], m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      x[i] = __ldg(l + i);
+      m = fmaxf(m, x[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      x[i] = expf(__fsub_rn(x[i], m));
+      sum = __fadd_rn(sum, x[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+#pragma unroll
+    for (int i = 0; i < V; ++i) s[i] = __fdiv_rn(x[i], sum);
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) z[i] = bias ? __fadd_rn(s[i], __ldg(bias + lane * V + i)) : s[i];
+
+  // Group selection: a lane is eligible while its group is kept.
+  bool eligible = true;
+  if (G > 1) {
+    const int lpg = 32 / G;  // lanes per group
+    float a = -INFINITY, b = -INFINITY;  // this lane's two largest z
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      if (z[i] > a) {
+        b = a;
+        a = z[i];
+      } else if (z[i] > b) {
+        b = z[i];
+      }
+    }
+    for (int o = lpg >> 1; o > 0; o >>= 1) {  // merge the pairs of the group's lanes
+      const float a2 = __shfl_xor_sync(0xFFFFFFFFu, a, o);
+      const float b2 = __shfl_xor_sync(0xFFFFFFFFu, b, o);
+      const float hi = fmaxf(a, a2);
+      b = fmaxf(fminf(a, a2), fmaxf(b, b2));
+      a = hi;
+    }
+    const float gscore = bias ? __fadd_rn(a, b) : a;
+    const int g = lane / lpg;
+    bool kept = false;
+    for (int r = 0; r < TG; ++r) {
+      const uint64_t best = warp_max_u64(kept ? 0ull : gate_key(gscore, g));
+      if (static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best)) == g) kept = true;
+    }
+    eligible = kept;
+  }
+
+  // Top-k experts among the eligible lanes' z.
+  uint32_t taken = 0;
+  int my_idx = 0;
+  float my_s = 0.0f, sum = 0.0f;
+  for (int j = 0; j < K; ++j) {
+    uint64_t key = 0;
+    if (eligible) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const uint64_t k = (taken >> i) & 1u ? 0ull : gate_key(z[i], lane * V + i);
+        key = k > key ? k : key;
+      }
+    }
+    key = warp_max_u64(key);
+    const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+    const int owner = e / V;
+    float se = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (lane == owner && e - lane * V == i) {
+        se = s[i];
+        taken |= 1u << i;
+      }
+    se = __shfl_sync(0xFFFFFFFFu, se, owner);
+    sum = __fadd_rn(sum, se);
+    if (lane == j) {
+      my_idx = e;
+      my_s = se;
+    }
+  }
+  if (lane < K) {
+    const float v = normalize ? __fdiv_rn(my_s, sum) : my_s;
+    idx[static_cast<size_t>(t) * K + lane] = my_idx;
+    w[static_cast<size_t>(t) * K + lane] = __fmul_rn(v, route_scale);
+  }
+}
+
+int launch_gate(const float* logits, const float* bias, int64_t T, int64_t E, int64_t G, int64_t TG, int64_t K,
+                int sigmoid, float route_scale, int normalize, int32_t* idx, float* w, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((T + kGateWarps - 1) / kGateWarps);
+  const int t = static_cast<int>(T), g = static_cast<int>(G), tg = static_cast<int>(TG), k = static_cast<int>(K);
+#define FP8BLK_GATE_CASE(v)                                                                                   \
+  case v:                                                                                                     \
+    moe_gate_kernel<v><<<grid, kGateWarps * 32, 0, stream>>>(logits, bias, t, g, tg, k, sigmoid, route_scale, \
+                                                              normalize, idx, w);                             \
+    break;
+  switch (E / 32) {
+    FP8BLK_GATE_CASE(1)
+    FP8BLK_GATE_CASE(2)
+    FP8BLK_GATE_CASE(3)
+    FP8BLK_GATE_CASE(4)
+    FP8BLK_GATE_CASE(5)
+    FP8BLK_GATE_CASE(6)
+    FP8BLK_GATE_CASE(7)
+    FP8BLK_GATE_CASE(8)
+    default: return FP8BLK_ERR_SHAPE;
+  }
+#undef FP8BLK_GATE_CASE
   return launch_status();
 }
 
@@ -248,15 +441,43 @@ int launch_permute(const DevInfo* d, const int* idx, int64_t n, int64_t E, int* 
 
 using namespace fp8blk;
 
+extern "C" size_t fp8blk_moe_permute_workspace_bytes(int64_t T, int64_t topk, int64_t E) {
+  if (T < 0 || topk < 0 || E <= 0) return 0;
+  const size_t b = permute_scratch_bytes(T * topk, E);
+  return b > 256 ? b : 256;
+}
+
 extern "C" int fp8blk_moe_permute(const int32_t* topk_idx, int64_t T, int64_t topk, int64_t E, int32_t* counts,
-                                  int32_t* offsets, int32_t* perm, fp8blk_stream_t stream) {
+                                  int32_t* offsets, int32_t* perm, void* workspace, size_t workspace_bytes,
+                                  fp8blk_stream_t stream) {
   if (T < 0 || topk < 0 || E <= 0 || E > kMaxExperts || T * topk > (int64_t{1} << 31) - 1) return FP8BLK_ERR_SHAPE;
   if (!counts || !offsets) return FP8BLK_ERR_NULL;
   if (T * topk > 0 && (!topk_idx || !perm)) return FP8BLK_ERR_NULL;
+  if (!workspace || workspace_bytes < fp8blk_moe_permute_workspace_bytes(T, topk, E)) return FP8BLK_ERR_WORKSPACE;
+  if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  return launch_permute(d, topk_idx, T * topk, E, counts, offsets, nullptr, perm,
+  return launch_permute(d, topk_idx, T * topk, E, counts, offsets, nullptr, perm, workspace,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8blk_moe_gate(const float* logits, const float* bias, int64_t T, int64_t E, int64_t n_groups,
+                               int64_t topk_groups, int64_t topk, int score_func, float route_scale, int normalize,
+                               int32_t* topk_idx, float* topk_w, fp8blk_stream_t stream) {
+  if (score_func != FP8BLK_SCORE_SOFTMAX && score_func != FP8BLK_SCORE_SIGMOID) return FP8BLK_ERR_ARG;
+  if (!(route_scale == route_scale) || route_scale == INFINITY || route_scale == -INFINITY) return FP8BLK_ERR_ARG;
+  if (T < 0 || T > (int64_t{1} << 31) - 1 || E < 32 || E > 256 || E % 32 || n_groups < 1 || 32 % n_groups ||
+      topk_groups < 1 || topk_groups > n_groups || topk < 1 || topk > 32 || topk > topk_groups * (E / n_groups) ||
+      (bias && n_groups > 1 && E / n_groups < 2))
+    return FP8BLK_ERR_SHAPE;
+  if (T == 0) return FP8BLK_OK;
+  if (!logits || !topk_idx || !topk_w) return FP8BLK_ERR_NULL;
+  if (!is_aligned(logits, 4) || !is_aligned(topk_idx, 4) || !is_aligned(topk_w, 4) || (bias && !is_aligned(bias, 4)))
+    return FP8BLK_ERR_ALIGN;
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  return launch_gate(logits, bias, T, E, n_groups, topk_groups, topk, score_func == FP8BLK_SCORE_SIGMOID,
+                     route_scale, normalize != 0, topk_idx, topk_w, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t fp8blk_swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t dim) {
@@ -313,7 +534,7 @@ extern "C" int fp8blk_ffn(const void* x_bf16, const void* w1_e4m3, const float* 
 namespace {
 
 struct MoeLayout {
-  size_t counts, offsets, mtiles, perm, xg, xgs, uq, us, o, total;
+  size_t counts, offsets, mtiles, perm, pscratch, xg, xgs, uq, us, o, total;
 };
 
 MoeLayout moe_layout(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t inter) {
@@ -329,6 +550,7 @@ MoeLayout moe_layout(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t in
   l.offsets = take((E + 1) * 4);
   l.mtiles = take((E + 1) * 4);
   l.perm = take(n * 4);
+  l.pscratch = take(permute_scratch_bytes(static_cast<int64_t>(n), E));
   l.xg = take(n * dim);
   l.xgs = take(n * (dim / kBlock) * 4);
   l.uq = take(n * inter);
@@ -384,7 +606,7 @@ extern "C" int fp8blk_moe_grouped_gemm(const void* x_e4m3, const float* x_s, con
   float* us = reinterpret_cast<float*>(ws + l.us);
   void* o = ws + l.o;
 
-  if (int st = launch_permute(d, topk_idx, n, E, counts, offsets, mtiles, perm, cs)) return st;
+  if (int st = launch_permute(d, topk_idx, n, E, counts, offsets, mtiles, perm, ws + l.pscratch, cs)) return st;
   // One warp per routed row (at most T * topk of them), as many CTAs as that
   // takes: the resident CTAs then copy one contiguous window of rows at a time.
   const long long gather_grid = (static_cast<long long>(n) + 7) / 8;

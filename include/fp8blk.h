@@ -207,9 +207,43 @@ FP8BLK_API int fp8blk_ffn(const void *x_bf16, const void *w1_e4m3, const float *
  *                   increasing pair order (a stable sort by expert id).
  * Integer work, no host synchronisation. E <= 1024. Ids outside [0, E) join no
  * expert and set a bit read by fp8blk_last_device_error.
+ * Workspace: device scratch of fp8blk_moe_permute_workspace_bytes(T, topk, E),
+ * 256-byte aligned (ranks and per-chunk bases; any contents on entry).
  */
+FP8BLK_API size_t fp8blk_moe_permute_workspace_bytes(int64_t T, int64_t topk, int64_t E);
 FP8BLK_API int fp8blk_moe_permute(const int32_t *topk_idx, int64_t T, int64_t topk, int64_t E, int32_t *counts,
-                                  int32_t *offsets, int32_t *perm, fp8blk_stream_t stream);
+                                  int32_t *offsets, int32_t *perm, void *workspace, size_t workspace_bytes,
+                                  fp8blk_stream_t stream);
+
+/*
+ * MoE gate ("Administrator & Developer Guide", 8.4 the Gate and 3.3 per-config
+ * fields; "Repository overview" page, MoE data flow: scores, optional group
+ * masking, top-k indices, the original scores, normalize, route_scale).
+ * Per token t, from the gate logits l[t, :] (fp32 [T, E]):
+ *     s[e] = 1 / (1 + exp(-l[e]))   (FP8BLK_SCORE_SIGMOID), or
+ *            softmax of l[t, :] over the E experts (FP8BLK_SCORE_SOFTMAX),
+ *     z[e] = s[e] + bias[e]   (bias fp32 [E], optional: NULL means z = s),
+ *     with n_groups > 1 groups of E / n_groups consecutive experts, a group
+ *     scores its largest z (no bias) or the sum of its two largest z (bias);
+ *     only the topk_groups best groups' experts stay eligible,
+ *     topk_idx[t, j] = the eligible expert with the j-th largest z (ties go to
+ *                      the lower index: j = 0 is the largest),
+ *     topk_w[t, j]   = s[topk_idx[t, j]] / (normalize ? sum over j of those s : 1)
+ *                      * route_scale.
+ * Scores and sums are fp32 (the exponential is CUDA's expf, within 2 ulp).
+ * Outputs: topk_idx int32 [T, topk], topk_w fp32 [T, topk] (device), ready for
+ * fp8blk_moe_permute / fp8blk_moe_grouped_gemm. Shapes: E % 32 == 0 and
+ * 32 <= E <= 256; n_groups divides 32 (so 1, 2, 4, 8, 16 or 32);
+ * 1 <= topk_groups <= n_groups; 1 <= topk <= min(32, topk_groups * E / n_groups);
+ * with a bias and n_groups > 1, groups of at least two experts. Otherwise
+ * FP8BLK_ERR_SHAPE; a score_func other than the two, or a non-finite
+ * route_scale, gives FP8BLK_ERR_ARG. Pointers 4-byte aligned. No workspace.
+ */
+#define FP8BLK_SCORE_SOFTMAX 0
+#define FP8BLK_SCORE_SIGMOID 1
+FP8BLK_API int fp8blk_moe_gate(const float *logits, const float *bias, int64_t T, int64_t E, int64_t n_groups,
+                               int64_t topk_groups, int64_t topk, int score_func, float route_scale, int normalize,
+                               int32_t *topk_idx, float *topk_w, fp8blk_stream_t stream);
 
 /*
  * Routed-expert FFN ("Administrator & Developer Guide", 6.4 and 8.4 steps

@@ -252,36 +252,41 @@ def test_grouped_tiles_cover_every_group_tile_once(seed):
 
 
 def permute_mirror(idx, E, chunk=1024):
-    """Mirror of the one-CTA permutation: per-chunk per-warp counts (match_any
-    ranks within a warp, prefix over earlier warps), running bases."""
+    """Mirror of the three-pass permutation. Rank pass, per chunk of pairs:
+    a pair's rank is its rank among its warp's earlier pairs of the same
+    expert plus that expert's count in the chunk's earlier warps, and the
+    chunk's histogram. Offsets pass: per-(chunk, expert) bases. Scatter pass:
+    perm[base + rank] = pair."""
     import numpy as np
 
     flat = idx.ravel()
     n = flat.size
-    valid = (flat >= 0) & (flat < E)
-    counts = np.bincount(flat[valid], minlength=E)
-    offsets = np.concatenate([[0], np.cumsum(counts)])
-    base = offsets[:-1].copy()
-    perm = np.full(n, -1)
-    for c0 in range(0, n, chunk):
-        ids = np.arange(c0, min(c0 + chunk, n))
+    nchunks = -(-n // chunk)
+    rank = np.full(n, -1)
+    hist = np.zeros((nchunks, E), np.int64)
+    for c in range(nchunks):
+        c0 = c * chunk
         wtab = np.zeros((chunk // 32, E), np.int64)
-        rank = {}
-        for i in ids:
-            e = flat[i]
-            if not (0 <= e < E):
-                continue
-            w, lane = (i - c0) // 32, (i - c0) % 32
-            same = [j for j in range(c0 + w * 32, i) if flat[j] == e]
-            rank[i] = len(same)
-            wtab[w, e] += 1
-        for i in ids:
+        wrank = {}
+        for i in range(c0, min(c0 + chunk, n)):
             e = flat[i]
             if not (0 <= e < E):
                 continue
             w = (i - c0) // 32
-            perm[base[e] + wtab[:w, e].sum() + rank[i]] = i
-        base += wtab.sum(axis=0)
+            wrank[i] = sum(1 for j in range(c0 + w * 32, i) if flat[j] == e)
+            wtab[w, e] += 1
+        for i, r in wrank.items():
+            w = (i - c0) // 32
+            rank[i] = wtab[:w, flat[i]].sum() + r
+        hist[c] = wtab.sum(axis=0)
+    counts = hist.sum(axis=0)
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    base = offsets[:-1][None, :] + np.cumsum(hist, axis=0) - hist
+    perm = np.full(n, -1)
+    for i in range(n):
+        e = flat[i]
+        if 0 <= e < E:
+            perm[base[i // chunk, e] + rank[i]] = i
     return counts, offsets, perm[: offsets[-1]]
 
 
