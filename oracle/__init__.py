@@ -79,7 +79,7 @@ def lib():
             L.orc_expert_ffn.restype = i32
             L.orc_expert_ffn_u.argtypes = [vp] * 8 + [i64, i64, i32, vp, vp, vp]
             L.orc_expert_ffn_u.restype = i32
-            L.orc_moe_token.argtypes = [vp, vp, vp, vp, i64, i64] + [vp] * 6 + [i64, i64, i32, vp]
+            L.orc_moe_token.argtypes = [vp, vp, vp, vp, i64, i64] + [vp] * 6 + [i64, i64, i32, i64, i64, vp]
             L.orc_moe_token.restype = i32
             L.orc_moe_gate.argtypes = [vp, vp, i64, i64, i64, i64, i64, i32, ctypes.c_float, i32, vp, vp]
             L.orc_moe_gate.restype = i32
@@ -261,9 +261,10 @@ def moe_permute(idx: np.ndarray, E: int):
 
 # ---- A6/A7 MoE output -----------------------------------------------------------
 
-def moe_tokens(xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s, tokens, ue8m0=False):
+def moe_tokens(xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s, tokens, ue8m0=False, n_shared=0):
     """MoE output rows (bf16 bits [len(tokens), dim]) for the listed tokens.
-    Stacked expert weights: w1q/w3q [E*inter, dim], w2q [E*dim, inter]."""
+    Stacked expert weights: w1q/w3q [(E+n_shared)*inter, dim], w2q [(E+n_shared)*dim, inter];
+    the last n_shared experts are shared: every token uses them with weight 1."""
     xq, xs = _c(xq, np.uint8), _c(xs, np.float32)
     idx, wts = _c(idx, np.int32), _c(wts, np.float32)
     w1q, w3q, w2q = _c(w1q, np.uint8), _c(w3q, np.uint8), _c(w2q, np.uint8)
@@ -271,13 +272,14 @@ def moe_tokens(xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s, tokens, ue8m0=Fal
     T, dim = xq.shape
     topk = idx.shape[1]
     inter = w2q.shape[1]
+    E = w2q.shape[0] // dim - n_shared
     y = np.empty((len(tokens), dim), np.uint16)
     L = lib()
     for i, t in enumerate(tokens):
         row = np.empty(dim, np.uint16)
         rc = L.orc_moe_token(_ptr(xq), _ptr(xs), _ptr(idx), _ptr(wts), int(t), topk,
                              _ptr(w1q), _ptr(w1s), _ptr(w3q), _ptr(w3s), _ptr(w2q), _ptr(w2s),
-                             dim, inter, int(bool(ue8m0)), _ptr(row))
+                             dim, inter, int(bool(ue8m0)), E, n_shared, _ptr(row))
         if rc:
             raise MemoryError("oracle MoE token failed")
         y[i] = row

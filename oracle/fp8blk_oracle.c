@@ -370,6 +370,9 @@ int orc_expert_ffn_u(const uint8_t *xq, const float *xs,
 
 /* MoE output of one token t: y[t] = bf16( sum over slots j in order of
  * fp64(w[t, j]) * fp64(bf16(o_j)) ), o_j the expert FFN of expert idx[t, j].
+ * With n_shared > 0 (Guide 8.4 steps 6 and 8: the shared MLP runs on every
+ * token and the result is y + z), experts E .. E+n_shared-1 are shared:
+ * z = bf16( sum of their bf16 outputs ) and the row is bf16(y + z).
  * Expert e's weights sit at row offset e*inter (w1, w3) and e*dim (w2) of the
  * stacked tensors; their scales at block-row offset e*inter/128 and
  * e*dim/128. y_row: bf16 bits [dim]. */
@@ -378,33 +381,45 @@ int orc_moe_token(const uint8_t *xq, const float *xs,
                   const uint8_t *w1, const float *w1s,
                   const uint8_t *w3, const float *w3s,
                   const uint8_t *w2, const float *w2s,
-                  int64_t dim, int64_t inter, int ue8m0, uint16_t *y_row)
+                  int64_t dim, int64_t inter, int ue8m0, int64_t E, int64_t n_shared, uint16_t *y_row)
 {
     int64_t kbd = dim / ORC_BLOCK, kbi = inter / ORC_BLOCK;
     double *acc = calloc((size_t)dim, sizeof(double));
+    double *accs = calloc((size_t)dim, sizeof(double));
     double *o = malloc(sizeof(double) * dim);
-    if (!acc || !o) {
-        free(acc); free(o);
+    if (!acc || !accs || !o) {
+        free(acc); free(accs); free(o);
         return -1;
     }
-    for (int64_t j = 0; j < topk; ++j) {
-        int64_t e = idx[t * topk + j];
+    /* routed slots, then (step 6 of 8.4) the shared experts E .. E+n_shared-1 */
+    for (int64_t j = 0; j < topk + n_shared; ++j) {
+        int64_t e = j < topk ? idx[t * topk + j] : E + (j - topk);
         int rc = orc_expert_ffn(xq + t * dim, xs + t * kbd,
                                 w1 + e * inter * dim, w1s + e * (inter / ORC_BLOCK) * kbd,
                                 w3 + e * inter * dim, w3s + e * (inter / ORC_BLOCK) * kbd,
                                 w2 + e * dim * inter, w2s + e * (dim / ORC_BLOCK) * kbi,
                                 dim, inter, ue8m0, o);
         if (rc) {
-            free(acc); free(o);
+            free(acc); free(accs); free(o);
             return rc;
         }
-        double wj = (double)wts[t * topk + j];
+        double wj = j < topk ? (double)wts[t * topk + j] : 1.0;
+        double *dst = j < topk ? acc : accs;
         for (int64_t c = 0; c < dim; ++c)
-            acc[c] += wj * orc_bf16_decode(orc_bf16_encode(o[c]));
+            dst[c] += wj * orc_bf16_decode(orc_bf16_encode(o[c]));
     }
-    for (int64_t c = 0; c < dim; ++c)
-        y_row[c] = orc_bf16_encode(acc[c]);
-    free(acc); free(o);
+    /* y = routed sum (bf16); with shared experts the output is bf16(y + z),
+     * z = bf16 of their summed (bf16) outputs: the guide's "Return (y + z)" */
+    for (int64_t c = 0; c < dim; ++c) {
+        if (n_shared == 0) {
+            y_row[c] = orc_bf16_encode(acc[c]);
+        } else {
+            double y = orc_bf16_decode(orc_bf16_encode(acc[c]));
+            double z = orc_bf16_decode(orc_bf16_encode(accs[c]));
+            y_row[c] = orc_bf16_encode(y + z);
+        }
+    }
+    free(acc); free(accs); free(o);
     return 0;
 }
 

@@ -214,3 +214,22 @@ def test_moe_topk1_unit_weight_is_dense_chain():
                             w3q[e * inter:(e + 1) * inter], w3s[e * bi:(e + 1) * bi],
                             w2q[e * dim:(e + 1) * dim], w2s[e * bd:(e + 1) * bd], [0])[0]
         assert np.array_equal(y[t], oracle.bf16_round(o))
+
+
+def test_moe_shared_expert_is_routed_plus_dense():
+    """With a shared expert stacked after the E routed ones (Guide 8.4 steps 6
+    and 8: z = shared MLP of every token, output y + z), each row equals the
+    routed-only row y plus the dense chain z of the shared expert, added as
+    two bf16 tensors by torch (fp32 add, one bf16 rounding)."""
+    E, dim, inter, topk = 4, 256, 256, 2
+    xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s = _moe_problem(5, E + 1, dim, inter, topk, 63)
+    idx = idx % E                       # routed ids only
+    bi, bd = inter // 128, dim // 128
+    y = oracle.moe_tokens(xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s, range(5), n_shared=1)
+    routed = oracle.moe_tokens(xq, xs, idx, wts, w1q[:E * inter], w1s[:E * bi], w3q[:E * inter], w3s[:E * bi],
+                               w2q[:E * dim], w2s[:E * bd], range(5))
+    z = oracle.bf16_round(oracle.ffn_rows(xq, xs, w1q[E * inter:], w1s[E * bi:], w3q[E * inter:], w3s[E * bi:],
+                                          w2q[E * dim:], w2s[E * bd:], range(5)))
+    as_bf16 = lambda b: torch.from_numpy(b.astype(np.int16)).view(torch.bfloat16)
+    want = (as_bf16(routed) + as_bf16(z)).view(torch.int16).numpy().astype(np.uint16)
+    assert np.array_equal(y, want)
