@@ -63,6 +63,8 @@ WORKLOADS = {
     "prefill_ffn_4096": ("ffn", dict(M=4096, dim=7168, inter=18432, seed=synthetic.SEED_PREFILL)),
     "moe_t4096_uniform": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, seed=synthetic.SEED_MOE)),
     "moe_t4096_zipf": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=1.2, seed=synthetic.SEED_MOE)),
+    "moe_t4096_uniform_shared": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, shared=1,
+                                             seed=synthetic.SEED_MOE)),
     "moe_gate_t4096_e256": ("gate", dict(T=4096, E=256, groups=8, kept=4, k=8, route_scale=2.5,
                                          seed=synthetic.SEED_GATE)),
 }
@@ -512,6 +514,7 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     + act_quant epilogue, grouped w2 GEMM scattered to slots, weighted combine.
     HBM-bound on the touched experts' weights at this token count."""
     T, E, dim, inter, k, seed = (shape[n] for n in ("T", "E", "dim", "inter", "k", "seed"))
+    ns = shape.get("shared", 0)
     x = synthetic.device_activations(T, dim, seed, dev)
     xq, xs = fb.act_quant(x)
     idx_np, w_np = synthetic.moe_routing(T, E, k, seed, zipf_s=shape["zipf"])
@@ -521,14 +524,14 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     for which in range(3):
         sh = (inter, dim) if which < 2 else (dim, inter)
         qs, ss = zip(*[fb.weight_quant(synthetic.device_normal(sh, seed * 100000 + 3 * e + which, 0.02, dev))
-                       for e in range(E)])
+                       for e in range(E + ns)])
         stacks.append((torch.cat(qs), torch.cat(ss)))
         del qs, ss
     y = torch.empty((T, dim), dtype=torch.bfloat16, device=dev)
     (q1, s1), (q3, s3), (q2, s2) = stacks
 
     def step(i):
-        fb.moe_grouped_gemm(xq, xs, idx, wts, q1, s1, q3, s3, q2, s2, E, out=y)
+        fb.moe_grouped_gemm(xq, xs, idx, wts, q1, s1, q3, s3, q2, s2, E, out=y, n_shared=ns)
 
     for i in range(3):
         step(i)
@@ -542,22 +545,24 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
         time.sleep(0.3)
         el, t0, t1 = timed_replay(g_main, stream, torch)
     assert fb.last_device_error(dev) == 0
-    touched = int(np.unique(idx_np).size)
+    touched = int(np.unique(idx_np).size) + ns
     b = moe_weight_bytes(touched, dim, inter) + T * dim + T * (dim // 128) * 4 + T * dim * 2 + T * k * 8
-    flops = 3 * 2.0 * T * k * dim * inter
+    flops = 3 * 2.0 * T * (k + ns) * dim * inter
     el_max, units = reduce_over_ranks(el, steps * b, dev)
     achieved = b / (el / steps) / 1e9
     return {
         "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
         "tflops": steps * flops / el / 1e12,
-        "clocks": clk.summary(t0, t1), "gpu_launches": 5 * steps,
-        "roofline": {"bound": "hbm", "kernel": "whole routed-expert step (5 kernels)", "achieved": achieved,
+        "clocks": clk.summary(t0, t1), "gpu_launches": (7 + (1 if ns else 0)) * steps,
+        "roofline": {"bound": "hbm", "kernel": f"whole routed-expert step ({7 + (1 if ns else 0)} kernels)",
+                     "achieved": achieved,
                      "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
                      "traffic": recorded_traffic(args.workload, "moe_step"),
                      "peak_source": f"hbm_gbs ({peaks['src']})", "algorithmic_bytes_per_launch": b},
         "e2e": None,
         "config": {"workload": args.workload, "T": T, "E": E, "dim": dim, "inter": inter, "topk": k,
-                   "routing": "Zipf(1.2)" if shape["zipf"] else "uniform", "experts_touched": touched,
+                   "routing": "Zipf(1.2)" if shape["zipf"] else "uniform", "shared_experts": ns,
+                   "experts_touched": touched,
                    "l2": f"{touched} experts' weights ({moe_weight_bytes(touched, dim, inter) / 1e9:.2f} GB) per step"},
         "dtype": "e4m3 x e4m3 -> f32 accumulate; SwiGLU in fp32/bf16; e4m3 re-quantisation",
     }
@@ -640,7 +645,7 @@ def run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     achieved = b_gate / (el_gate / steps) / 1e9
     return {
         "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
-        "clocks": clk.summary(t0, t1), "gpu_launches": 2 * steps,
+        "clocks": clk.summary(t0, t1), "gpu_launches": 4 * steps,
         "kernels_us": {"gate_and_permute": el / steps * 1e6, "gate_alone": el_gate / steps * 1e6},
         "roofline": {"bound": "hbm", "kernel": "moe_gate", "achieved": achieved, "peak": peaks["hbm"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None,

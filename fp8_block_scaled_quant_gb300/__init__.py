@@ -346,17 +346,19 @@ def moe_gate(logits: torch.Tensor, bias: torch.Tensor | None = None, n_groups: i
     return idx, w
 
 
-def moe_workspace_bytes(T: int, topk: int, E: int, dim: int, inter: int) -> int:
+def moe_workspace_bytes(T: int, topk: int, E: int, dim: int, inter: int, n_shared: int = 0) -> int:
     i64 = ctypes.c_int64
-    return int(_set_types("fp8blk_moe_workspace_bytes", [i64] * 5, ctypes.c_size_t)(T, topk, E, dim, inter))
+    return int(_set_types("fp8blk_moe_workspace_bytes", [i64] * 6, ctypes.c_size_t)(T, topk, E, dim, inter, n_shared))
 
 
 def moe_grouped_gemm(x: torch.Tensor, x_s: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
                      w1, w1_s, w3, w3_s, w2, w2_s, E: int, scale_fmt: int = SCALE_FP32,
-                     out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+                     out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                     n_shared: int = 0) -> torch.Tensor:
     """Routed-expert SwiGLU FFN over stacked block-FP8 experts.
-    x e4m3 [T, dim] (+ x_s), topk_idx int32 / topk_w fp32 [T, topk],
-    w1/w3 e4m3 [E*inter, dim], w2 e4m3 [E*dim, inter] (+ block scales) -> bf16 [T, dim]."""
+    x e4m3 [T, dim] (+ x_s), topk_idx int32 / topk_w fp32 [T, topk] (ids < E),
+    w1/w3 e4m3 [(E+n_shared)*inter, dim], w2 e4m3 [(E+n_shared)*dim, inter] (+ block scales)
+    -> bf16 [T, dim]; the last n_shared experts are shared (every token, weight 1, added as y + z)."""
     _need(x, torch.float8_e4m3fn, "x")
     _need(topk_idx, torch.int32, "topk_idx")
     _need(topk_w, torch.float32, "topk_w")
@@ -364,12 +366,12 @@ def moe_grouped_gemm(x: torch.Tensor, x_s: torch.Tensor, topk_idx: torch.Tensor,
     k = topk_idx.shape[1]
     inter = w2.shape[1]
     if ws is None:
-        ws = workspace(moe_workspace_bytes(T, k, E, dim, inter), x.device, "moe")
+        ws = workspace(moe_workspace_bytes(T, k, E, dim, inter, n_shared), x.device, "moe")
     if out is None:
         out = torch.empty((T, dim), dtype=torch.bfloat16, device=x.device)
     vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
-    f = _set_types("fp8blk_moe_grouped_gemm", [vp] * 11 + [i64] * 5 + [i32, vp, sz, vp])
+    f = _set_types("fp8blk_moe_grouped_gemm", [vp] * 11 + [i64] * 6 + [i32, vp, sz, vp])
     _check(f(_ptr(x), _ptr(x_s), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w1_s), _ptr(w3), _ptr(w3_s),
-             _ptr(w2), _ptr(w2_s), _ptr(out), T, k, E, dim, inter, scale_fmt, _ptr(ws), ws.numel(),
+             _ptr(w2), _ptr(w2_s), _ptr(out), T, k, E, dim, inter, n_shared, scale_fmt, _ptr(ws), ws.numel(),
              _stream(x.device)), "moe_grouped_gemm")
     return out

@@ -182,17 +182,20 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
   }
 }
 
-// y[t, :] = bf16( sum over slots j in order of w[t, j] * o[t * topk + j, :] ),
-// fp32 accumulation; slots routed to no valid expert contribute nothing.
-// y[t] = bf16(sum over slots j in order of w[t, j] * o[t * topk + j]) in fp32.
-// For topk <= kCombineMax all slots' ids, weights and output vectors are
-// requested before the first FMA (the loads are independent; the FMAs keep the
-// slot order); larger topk takes the plain loop.
+// y[t] = bf16(sum over routed slots j < n_routed, in order, of w[t, j] * o[t * topk + j]),
+// fp32 accumulation; slots routed to no valid expert contribute nothing. Slots
+// n_routed .. topk-1 are shared experts (weight 1): their fp32 sum z is
+// rounded to bf16 and the row is bf16(bf16(routed sum) + z), the guide's y + z.
+// For n_routed <= kCombineMax all routed slots' ids, weights and output vectors
+// are requested before the first FMA (the loads are independent; the FMAs keep
+// the slot order); more slots take the plain loop.
 constexpr int kCombineMax = 8;
 
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restrict__ o, const int* __restrict__ idx,
-                                                          const float* __restrict__ w, int T, int topk, int E,
-                                                          int dim, uint4* __restrict__ y) {
+                                                          const float* __restrict__ w, int T, int topk,
+                                                          int n_routed, int E, int dim, uint4* __restrict__ y) {
   const int dv = dim / 8;
   const long long total = static_cast<long long>(T) * dv;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -200,43 +203,75 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
     const long long t = v / dv;
     const int c = static_cast<int>(v - t * dv);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    auto add = [&](float wj, const uint4& ov) {
+    auto add = [](float* a, float wj, const uint4& ov) {
       const uint32_t u[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        acc[2 * q] = fmaf(wj, __uint_as_float(u[q] << 16), acc[2 * q]);
-        acc[2 * q + 1] = fmaf(wj, __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
+        a[2 * q] = fmaf(wj, __uint_as_float(u[q] << 16), a[2 * q]);
+        a[2 * q + 1] = fmaf(wj, __uint_as_float(u[q] & 0xFFFF0000u), a[2 * q + 1]);
       }
     };
-    if (topk <= kCombineMax) {
+    if (n_routed <= kCombineMax) {
       int e[kCombineMax];
       float wj[kCombineMax];
       uint4 ov[kCombineMax];
 #pragma unroll
       for (int j = 0; j < kCombineMax; ++j) {
-        e[j] = j < topk ? __ldg(idx + t * topk + j) : -1;
-        wj[j] = j < topk ? __ldg(w + t * topk + j) : 0.0f;
+        e[j] = j < n_routed ? __ldg(idx + t * topk + j) : -1;
+        wj[j] = j < n_routed ? __ldg(w + t * topk + j) : 0.0f;
       }
 #pragma unroll
       for (int j = 0; j < kCombineMax; ++j)
         if (e[j] >= 0 && e[j] < E) ov[j] = __ldg(o + (t * topk + j) * dv + c);
 #pragma unroll
       for (int j = 0; j < kCombineMax; ++j)
-        if (e[j] >= 0 && e[j] < E) add(wj[j], ov[j]);
+        if (e[j] >= 0 && e[j] < E) add(acc, wj[j], ov[j]);
     } else {
-      for (int j = 0; j < topk; ++j) {
+      for (int j = 0; j < n_routed; ++j) {
         const int ej = __ldg(idx + t * topk + j);
         if (ej < 0 || ej >= E) continue;
-        add(__ldg(w + t * topk + j), __ldg(o + (t * topk + j) * dv + c));
+        add(acc, __ldg(w + t * topk + j), __ldg(o + (t * topk + j) * dv + c));
       }
     }
     uint32_t r[4];
+    if (n_routed < topk) {
+      float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = n_routed; j < topk; ++j) add(z, __ldg(w + t * topk + j), __ldg(o + (t * topk + j) * dv + c));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(round_bf16(acc[q]), round_bf16(z[q]));
+    }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
       r[q] = *reinterpret_cast<const uint32_t*>(&b);
     }
     y[v] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+// Routing with shared experts: slot j < k of token t copies the routed id
+// (ids outside [0, E) become -1, join no expert, and set the error bit) and
+// its weight; slots k .. k+ns-1 name the shared experts E .. E+ns-1, weight 1.
+__global__ void __launch_bounds__(256) moe_augment_kernel(const int* __restrict__ idx, const float* __restrict__ w,
+                                                          long long T, int k, int E, int ns,
+                                                          int* __restrict__ aidx, float* __restrict__ aw,
+                                                          unsigned* err) {
+  const int kk = k + ns;
+  const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= T * kk) return;
+  const long long t = i / kk;
+  const int j = static_cast<int>(i - t * kk);
+  if (j < k) {
+    int e = __ldg(idx + t * k + j);
+    if (e < 0 || e >= E) {
+      e = -1;
+      atomicOr(err, kDevErrBadExpert);
+    }
+    aidx[i] = e;
+    aw[i] = __ldg(w + t * k + j);
+  } else {
+    aidx[i] = E + (j - k);
+    aw[i] = 1.0f;
   }
 }
 
@@ -534,9 +569,10 @@ extern "C" int fp8blk_ffn(const void* x_bf16, const void* w1_e4m3, const float* 
 namespace {
 
 struct MoeLayout {
-  size_t counts, offsets, mtiles, perm, pscratch, xg, xgs, uq, us, o, total;
+  size_t counts, offsets, mtiles, perm, pscratch, aidx, aw, xg, xgs, uq, us, o, total;
 };
 
+// topk counts every slot of a token, shared experts included; E every expert.
 MoeLayout moe_layout(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t inter) {
   MoeLayout l{};
   const size_t n = static_cast<size_t>(T) * topk;
@@ -551,6 +587,8 @@ MoeLayout moe_layout(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t in
   l.mtiles = take((E + 1) * 4);
   l.perm = take(n * 4);
   l.pscratch = take(permute_scratch_bytes(static_cast<int64_t>(n), E));
+  l.aidx = take(n * 4);
+  l.aw = take(n * 4);
   l.xg = take(n * dim);
   l.xgs = take(n * (dim / kBlock) * 4);
   l.uq = take(n * inter);
@@ -562,34 +600,39 @@ MoeLayout moe_layout(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t in
 
 }  // namespace
 
-extern "C" size_t fp8blk_moe_workspace_bytes(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t inter) {
-  if (T < 0 || topk < 0 || E <= 0 || dim < 0 || inter < 0) return 0;
-  return moe_layout(T, topk, E, dim, inter).total;
+extern "C" size_t fp8blk_moe_workspace_bytes(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t inter,
+                                             int64_t n_shared) {
+  if (T < 0 || topk < 0 || E <= 0 || dim < 0 || inter < 0 || n_shared < 0) return 0;
+  return moe_layout(T, topk + n_shared, E + n_shared, dim, inter).total;
 }
 
 extern "C" int fp8blk_moe_grouped_gemm(const void* x_e4m3, const float* x_s, const int32_t* topk_idx,
                                        const float* topk_w, const void* w1_e4m3, const float* w1_s,
                                        const void* w3_e4m3, const float* w3_s, const void* w2_e4m3,
                                        const float* w2_s, void* y_bf16, int64_t T, int64_t topk, int64_t E,
-                                       int64_t dim, int64_t inter, int scale_fmt, void* workspace,
+                                       int64_t dim, int64_t inter, int64_t n_shared, int scale_fmt, void* workspace,
                                        size_t workspace_bytes, fp8blk_stream_t stream) {
   if (scale_fmt != FP8BLK_SCALE_FP32 && scale_fmt != FP8BLK_SCALE_UE8M0) return FP8BLK_ERR_ARG;
-  if (T < 0 || topk < 0 || E <= 0 || E > kMaxExperts || dim <= 0 || inter <= 0 || dim % 256 || inter % kBlock)
+  if (T < 0 || topk < 0 || n_shared < 0 || E <= 0 || E + n_shared > kMaxExperts || dim <= 0 || inter <= 0 ||
+      dim % 256 || inter % kBlock)
     return FP8BLK_ERR_SHAPE;
-  const int64_t n = T * topk;
-  if (n > (int64_t{1} << 31) - 1 || E * inter > (int64_t{1} << 31) - 1 || E * dim > (int64_t{1} << 31) - 1)
+  const int64_t slots = topk + n_shared, experts = E + n_shared;  // per token; in the stacked weights
+  const int64_t n = T * slots;
+  if (n > (int64_t{1} << 31) - 1 || experts * inter > (int64_t{1} << 31) - 1 ||
+      experts * dim > (int64_t{1} << 31) - 1)
     return FP8BLK_ERR_SHAPE;
   if (T == 0) return FP8BLK_OK;
   if (!y_bf16) return FP8BLK_ERR_NULL;
-  if (topk == 0) return cuda_status(cudaMemsetAsync(y_bf16, 0, static_cast<size_t>(T) * dim * 2,
-                                                    reinterpret_cast<cudaStream_t>(stream)));
-  if (!x_e4m3 || !x_s || !topk_idx || !topk_w || !w1_e4m3 || !w1_s || !w3_e4m3 || !w3_s || !w2_e4m3 || !w2_s)
+  if (slots == 0) return cuda_status(cudaMemsetAsync(y_bf16, 0, static_cast<size_t>(T) * dim * 2,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
+  if (!x_e4m3 || !x_s || (topk > 0 && (!topk_idx || !topk_w)) || !w1_e4m3 || !w1_s || !w3_e4m3 || !w3_s ||
+      !w2_e4m3 || !w2_s)
     return FP8BLK_ERR_NULL;
   if (!is_aligned(x_e4m3, 16) || !is_aligned(w1_e4m3, 16) || !is_aligned(w3_e4m3, 16) ||
       !is_aligned(w2_e4m3, 16) || !is_aligned(y_bf16, 16) || !is_aligned(x_s, 4) || !is_aligned(w1_s, 4) ||
       !is_aligned(w3_s, 4) || !is_aligned(w2_s, 4) || !is_aligned(topk_idx, 4) || !is_aligned(topk_w, 4))
     return FP8BLK_ERR_ALIGN;
-  const MoeLayout l = moe_layout(T, topk, E, dim, inter);
+  const MoeLayout l = moe_layout(T, slots, experts, dim, inter);
   if (!workspace || workspace_bytes < l.total) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   const DevInfo* d;
@@ -606,24 +649,40 @@ extern "C" int fp8blk_moe_grouped_gemm(const void* x_e4m3, const float* x_s, con
   float* us = reinterpret_cast<float*>(ws + l.us);
   void* o = ws + l.o;
 
-  if (int st = launch_permute(d, topk_idx, n, E, counts, offsets, mtiles, perm, ws + l.pscratch, cs)) return st;
-  // One warp per routed row (at most T * topk of them), as many CTAs as that
+  // Shared experts (Guide 8.4 step 6: the shared MLP runs on every token)
+  // become extra slots naming experts E .. E+n_shared-1, so one permutation,
+  // one pair of grouped GEMMs and one combine serve routed and shared rows.
+  const int32_t* ridx = topk_idx;
+  const float* rw = topk_w;
+  if (n_shared > 0) {
+    int* aidx = reinterpret_cast<int*>(ws + l.aidx);
+    float* aw = reinterpret_cast<float*>(ws + l.aw);
+    moe_augment_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, cs>>>(
+        topk_idx, topk_w, T, static_cast<int>(topk), static_cast<int>(E), static_cast<int>(n_shared), aidx, aw,
+        d->err_word);
+    if (int st = launch_status()) return st;
+    ridx = aidx;
+    rw = aw;
+  }
+  if (int st = launch_permute(d, ridx, n, experts, counts, offsets, mtiles, perm, ws + l.pscratch, cs)) return st;
+  // One warp per routed row (at most T * slots of them), as many CTAs as that
   // takes: the resident CTAs then copy one contiguous window of rows at a time.
   const long long gather_grid = (static_cast<long long>(n) + 7) / 8;
-  moe_gather_kernel<<<static_cast<unsigned>(gather_grid < (1LL << 30) ? gather_grid : (1LL << 30)), 256, 0, cs>>>(static_cast<const uint4*>(x_e4m3), x_s, perm, offsets,
-                                                 static_cast<int>(E), static_cast<int>(topk), static_cast<int>(dim),
-                                                 reinterpret_cast<uint4*>(xg), xgs);
+  moe_gather_kernel<<<static_cast<unsigned>(gather_grid < (1LL << 30) ? gather_grid : (1LL << 30)), 256, 0, cs>>>(
+      static_cast<const uint4*>(x_e4m3), x_s, perm, offsets, static_cast<int>(experts), static_cast<int>(slots),
+      static_cast<int>(dim), reinterpret_cast<uint4*>(xg), xgs);
   if (int st = launch_status()) return st;
-  if (int st = grouped_swiglu_run(xg, xgs, w1_e4m3, w1_s, w3_e4m3, w3_s, uq, us, n, E, inter, dim, offsets, mtiles,
-                                  scale_fmt, cs))
+  if (int st = grouped_swiglu_run(xg, xgs, w1_e4m3, w1_s, w3_e4m3, w3_s, uq, us, n, experts, inter, dim, offsets,
+                                  mtiles, scale_fmt, cs))
     return st;
-  if (int st = grouped_scatter_run(uq, us, w2_e4m3, w2_s, o, perm, n, E, dim, inter, offsets, mtiles, cs))
+  if (int st = grouped_scatter_run(uq, us, w2_e4m3, w2_s, o, perm, n, experts, dim, inter, offsets, mtiles, cs))
     return st;
   // One thread per 8-element output vector (grid-stride past 2^30 CTAs).
   const long long vecs = T * (dim / 8);
   const int grid = static_cast<int>((vecs + 255) / 256 < (1LL << 30) ? (vecs + 255) / 256 : (1LL << 30));
-  moe_combine_kernel<<<grid, 256, 0, cs>>>(static_cast<const uint4*>(o), topk_idx, topk_w, static_cast<int>(T),
-                                           static_cast<int>(topk), static_cast<int>(E), static_cast<int>(dim),
+  moe_combine_kernel<<<grid, 256, 0, cs>>>(static_cast<const uint4*>(o), ridx, rw, static_cast<int>(T),
+                                           static_cast<int>(slots), static_cast<int>(topk),
+                                           static_cast<int>(experts), static_cast<int>(dim),
                                            static_cast<uint4*>(y_bf16));
   return launch_status();
 }

@@ -251,20 +251,30 @@ FP8BLK_API int fp8blk_moe_gate(const float *logits, const float *bias, int64_t T
  *                    topk_w[t, j] * bf16(FFN_{topk_idx[t, j]}(x[t])) ),
  * FFN_e(x) = w2_e(act_quant(bf16(silu(bf16(w1_e x))) * bf16(w3_e x))) with the
  * rounding of fp8blk_swiglu_gemm, accumulation of the sum in fp32.
+ * Shared experts (8.4 steps 6 and 8: the shared MLP runs on every token and
+ * the layer returns y + z): with n_shared > 0 the stacked weights hold the E
+ * routed experts followed by n_shared shared experts of the same shape; every
+ * token also goes through each of them with weight 1, and the row becomes
+ *     bf16( y[t] + z[t] ),  z[t] = bf16( sum over shared s of bf16(FFN_{E+s}(x[t])) ),
+ * in the same grouped launches as the routed rows. (A shared MLP of width
+ * n * inter, as in the 16B and 236B configs, is the sum of n experts of width
+ * inter up to the rounding of that sum.)
  * x: e4m3 [T, dim] + x_s [T, dim/128] (x quantised once per token: act_quant
  * is per row, so it commutes with routing). topk_idx int32 / topk_w fp32
- * [T, topk]. Stacked expert weights: w1, w3 e4m3 [E*inter, dim] with scales
- * [E*inter/128, dim/128]; w2 e4m3 [E*dim, inter] with scales [E*dim/128,
- * inter/128]. y: bf16 [T, dim]. dim % 256 == 0, inter % 128 == 0, E <= 1024.
+ * [T, topk], routed ids in [0, E). Stacked expert weights (K = E + n_shared):
+ * w1, w3 e4m3 [K*inter, dim] with scales [K*inter/128, dim/128]; w2 e4m3
+ * [K*dim, inter] with scales [K*dim/128, inter/128]. y: bf16 [T, dim].
+ * dim % 256 == 0, inter % 128 == 0, E + n_shared <= 1024.
  * Experts that receive no token read none of their weights.
- * Workspace: fp8blk_moe_workspace_bytes(T, topk, E, dim, inter), 256-aligned.
+ * Workspace: fp8blk_moe_workspace_bytes(T, topk, E, dim, inter, n_shared), 256-aligned.
  */
-FP8BLK_API size_t fp8blk_moe_workspace_bytes(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t inter);
+FP8BLK_API size_t fp8blk_moe_workspace_bytes(int64_t T, int64_t topk, int64_t E, int64_t dim, int64_t inter,
+                                             int64_t n_shared);
 FP8BLK_API int fp8blk_moe_grouped_gemm(const void *x_e4m3, const float *x_s, const int32_t *topk_idx,
                                        const float *topk_w, const void *w1_e4m3, const float *w1_s,
                                        const void *w3_e4m3, const float *w3_s, const void *w2_e4m3,
                                        const float *w2_s, void *y_bf16, int64_t T, int64_t topk, int64_t E,
-                                       int64_t dim, int64_t inter, int scale_fmt, void *workspace,
+                                       int64_t dim, int64_t inter, int64_t n_shared, int scale_fmt, void *workspace,
                                        size_t workspace_bytes, fp8blk_stream_t stream);
 
 /*

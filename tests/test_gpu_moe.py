@@ -240,3 +240,28 @@ def test_moe_full_size_sampled_tokens():
     assert_chain_close(dev_to_bits(y)[tokens], np.array(ref), np.array(allow), rms=rms, frac=0.99,
                        what="moe sampled tokens")
     assert fb.last_device_error() == 0
+
+
+@pytest.mark.parametrize("T,E,dim,inter,k", [(64, 8, 256, 256, 2), (33, 5, 256, 128, 3), (200, 3, 512, 256, 1)])
+def test_moe_shared_expert(T, E, dim, inter, k):
+    """One shared expert stacked after the E routed ones: every token also goes
+    through it (weight 1) in the same grouped launches, and the row is
+    bf16(y + z) (Guide 8.4 steps 6 and 8). Tolerance: the routed and shared
+    chains' allowances plus one bf16 step of y and of z (each is rounded once
+    before the sum)."""
+    xq, xs, _, _, w1q, w1s, w3q, w3s, w2q, w2s = moe_problem(T, E + 1, dim, inter, k, 950 + T)
+    idx, wts = synthetic.moe_routing(T, E, k, 951 + T)
+    p = (xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s)
+    y = fb.moe_grouped_gemm(to_dev_q(xq), to_dev(xs), to_dev(idx), to_dev(wts), to_dev_q(w1q), to_dev(w1s),
+                            to_dev_q(w3q), to_dev(w3s), to_dev_q(w2q), to_dev(w2s), E, n_shared=1)
+    ref = synthetic.bf16_bits_to_f32(oracle.moe_tokens(*p, range(T), n_shared=1)).astype(np.float64)
+    bi, bd = inter // 128, dim // 128
+    routed = (xq, xs, idx, wts, w1q[:E * inter], w1s[:E * bi], w3q[:E * inter], w3s[:E * bi], w2q[:E * dim],
+              w2s[:E * bd])
+    ref_r, allow_r = moe_reference(routed, range(T), E)
+    z, uq, us = oracle.ffn_rows(xq, xs, w1q[E * inter:], w1s[E * bi:], w3q[E * inter:], w3s[E * bi:],
+                                w2q[E * dim:], w2s[E * bd:], range(T), return_u=True)
+    allow_z = 2.0 ** -7 * np.abs(z) + flip_allowance(uq, us, dequant_weight(w2q[E * dim:], w2s[E * bd:]))
+    allow = allow_r + allow_z + 2.0 ** -8 * (np.abs(ref_r) + np.abs(z))
+    assert_chain_close(dev_to_bits(y), ref, allow, what=f"moe + shared expert T={T} E={E}")
+    assert fb.last_device_error() == 0
