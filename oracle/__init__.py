@@ -81,6 +81,7 @@ def lib():
             L.orc_expert_ffn_u.restype = i32
             L.orc_moe_token.argtypes = [vp, vp, vp, vp, i64, i64] + [vp] * 6 + [i64, i64, i32, i64, i64, vp]
             L.orc_moe_token.restype = i32
+            L.orc_mla_absorb.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
             L.orc_moe_gate.argtypes = [vp, vp, i64, i64, i64, i64, i64, i32, ctypes.c_float, i32, vp, vp]
             L.orc_moe_gate.restype = i32
             L.orc_e4m3_encode_array.argtypes = [vp, i64, vp]
@@ -302,3 +303,18 @@ def moe_gate(logits, bias, n_groups: int, topk_groups: int, topk: int, sigmoid: 
     if rc:
         raise ValueError("gate shape outside the rules")
     return idx, w
+
+
+# ---- MLA absorb projections ------------------------------------------------------
+
+def mla_absorb(inp_bits, wq, ws, H: int, dn: int, dv: int, mode: str):
+    """mode "qk": q_nope bf16 bits [T, H, dn] -> bf16 bits [T, H, C];
+    mode "v": x bf16 bits [T, H, C] -> bf16 bits [T, H, dv]. wq e4m3 codes
+    [H*(dn+dv), C] with block scales ws [H*(dn+dv)/128, C/128]."""
+    inp = _c(inp_bits, np.uint16)
+    wq, ws = _c(wq, np.uint8), _c(ws, np.float32)
+    C = wq.shape[1]
+    T = inp.shape[0]
+    out = np.empty((T, H, C if mode == "qk" else dv), np.uint16)
+    lib().orc_mla_absorb(_ptr(inp), _ptr(wq), _ptr(ws), T, H, dn, dv, C, 0 if mode == "qk" else 1, _ptr(out))
+    return out

@@ -29,6 +29,11 @@
  *        steps 2-5: per expert, the tokens routed to it, weighted by their
  *        gate weight, summed into y.
  *   [ML] same guide, 1.2 module map (MLP / Expert): w2(silu(w1 x) * w3 x).
+ *   [MA] same guide, 8.3 MLA forward, steps 5 and 7 ("absorb"): q_nope is
+ *        folded through wkv_b's no-positional rows, einsum("bshd,hdc->bshc"),
+ *        and the attention output is projected to V through its last v rows,
+ *        einsum("bshc,hdc->bshd"); wkv_b stored FP8 is used as its
+ *        weight_dequant (8.5.2: fp32 code times block scale, stored bf16).
  *   [GT] same guide, 8.4 (the Gate: with n_groups > 1 the scores are viewed as
  *        groups, a group's score is its max without a bias and the sum of its
  *        top two with one, the top topk_groups groups are kept and the rest
@@ -421,6 +426,46 @@ int orc_moe_token(const uint8_t *xq, const float *xs,
     }
     free(acc); free(accs); free(o);
     return 0;
+}
+
+/* ---- MLA absorb projections [MA] ------------------------------------------ */
+
+/* wkv_b: e4m3 [H*(dn+dv), C] with block scales [H*(dn+dv)/128, C/128]; head h
+ * owns rows h*(dn+dv) .. +dn (no-positional part) and the next dv rows (v).
+ * Weights are used as weight_dequant gives them: W = bf16(fp32(code) * s).
+ * mode 0 (qk): in = q_nope bf16 [T, H, dn], out[t,h,c] = bf16( sum_d q[t,h,d] * W[h*(dn+dv)+d, c] ), out [T, H, C];
+ * mode 1 (v):  in = x bf16 [T, H, C],      out[t,h,d] = bf16( sum_c x[t,h,c] * W[h*(dn+dv)+dn+d, c] ), out [T, H, dv].
+ * Sums in fp64 (exact products of two bf16 numbers), one bf16 rounding. */
+static double mla_w(const uint8_t *w, const float *ws, int64_t C, int64_t row, int64_t col)
+{
+    float f = (float)orc_e4m3_decode(w[row * C + col]) * ws[(row / ORC_BLOCK) * (C / ORC_BLOCK) + col / ORC_BLOCK];
+    return orc_bf16_decode(orc_bf16_encode((double)f));
+}
+
+void orc_mla_absorb(const uint16_t *in, const uint8_t *w, const float *ws, int64_t T, int64_t H, int64_t dn,
+                    int64_t dv, int64_t C, int mode, uint16_t *out)
+{
+    const int64_t hs = dn + dv;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t h = 0; h < H; ++h) {
+            if (mode == 0) {
+                const uint16_t *q = in + (t * H + h) * dn;
+                for (int64_t c = 0; c < C; ++c) {
+                    double acc = 0.0;
+                    for (int64_t d = 0; d < dn; ++d)
+                        acc += orc_bf16_decode(q[d]) * mla_w(w, ws, C, h * hs + d, c);
+                    out[(t * H + h) * C + c] = orc_bf16_encode(acc);
+                }
+            } else {
+                const uint16_t *x = in + (t * H + h) * C;
+                for (int64_t d = 0; d < dv; ++d) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < C; ++c)
+                        acc += orc_bf16_decode(x[c]) * mla_w(w, ws, C, h * hs + dn + d, c);
+                    out[(t * H + h) * dv + d] = orc_bf16_encode(acc);
+                }
+            }
+        }
 }
 
 /* ---- MoE gate: scores, group-limited top-k, weights [GT] ----------------- */
