@@ -65,6 +65,8 @@ WORKLOADS = {
     "moe_t4096_zipf": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=1.2, seed=synthetic.SEED_MOE)),
     "moe_t4096_uniform_shared": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, shared=1,
                                              seed=synthetic.SEED_MOE)),
+    "mla_absorb_m64": ("mla", dict(T=64, H=128, C=512, seed=synthetic.SEED_ATTN)),
+    "mla_absorb_m2048": ("mla", dict(T=2048, H=128, C=512, seed=synthetic.SEED_ATTN)),
     "moe_gate_t4096_e256": ("gate", dict(T=4096, E=256, groups=8, kept=4, k=8, route_scale=2.5,
                                          seed=synthetic.SEED_GATE)),
 }
@@ -605,6 +607,64 @@ def run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     }
 
 
+def run_mla(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
+    """The two MLA absorb projections of one layer (q_nope through wkv_b's
+    no-positional rows, the attention output through its v rows) with the FP8
+    wkv_b of the 671B config (128 heads, kv_lora 512): bf16 tensor-core
+    products of the dequantised weight."""
+    T, H, C, seed = shape["T"], shape["H"], shape["C"], shape["seed"]
+    dn = dv = 128
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
+    w_bytes = H * (dn + dv) * C
+    R = min(64, max(2, math.ceil(3 * l2 / w_bytes)))
+    w0, s0 = fb.weight_quant(synthetic.device_normal((H * (dn + dv), C), seed + 7, 0.02, dev))
+    qs = [w0] + [w0.clone() for _ in range(R - 1)]
+    q = synthetic.device_activations(T, H * dn, seed + 8, dev).view(T, H, dn)
+    x = synthetic.device_activations(T, H * C, seed + 9, dev).view(T, H, C)
+    oq = torch.empty((T, H, C), dtype=torch.bfloat16, device=dev)
+    ov = torch.empty((T, H, dv), dtype=torch.bfloat16, device=dev)
+
+    def step(i):
+        fb.mla_absorb(q, qs[i % R], s0, "qk", out=oq)
+        fb.mla_absorb(x, qs[i % R], s0, "v", out=ov)
+
+    for i in range(3):
+        step(i)
+    stream = torch.cuda.current_stream(dev)
+    g_warm = make_runs(step, warmup, 50, torch, args.eager)
+    g_main = make_runs(step, steps, 50, torch, args.eager)
+    for g in g_warm:
+        g.replay()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        el, t0, t1 = timed_replay(g_main, stream, torch)
+    assert fb.last_device_error(dev) == 0
+    b = w_bytes + (H * (dn + dv) // 128) * (C // 128) * 4 + 2 * T * H * (dn + C) * 2
+    flops = 2 * 2.0 * T * H * dn * C
+    el_max, units = reduce_over_ranks(el, steps * b, dev)
+    hbm_bound = flops / b < 300
+    per = el / steps
+    if hbm_bound:
+        value, unit = units / el_max / 1e9, "GB/s"
+        roof = {"bound": "hbm", "achieved": b / per / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": b / per / 1e9 / peaks["hbm"], "peak_source": f"hbm_gbs ({peaks['src']})"}
+    else:
+        value, unit = steps * flops * world / el_max / 1e12, "TFLOP/s"
+        roof = {"bound": "tensor", "achieved": flops / per / 1e12, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": flops / per / 1e12 / peaks["bf16"],
+                "peak_source": f"bf16_tflops ({peaks['src']}): the products are bf16"}
+    roof.update({"kernel": "mla_absorb_kernel (qk + v)", "traffic": None, "algorithmic_bytes_per_launch": b // 2,
+                 "kernel_us": per / 2 * 1e6})
+    return {
+        "value": value, "unit": unit, "ms_per_step": el_max / steps * 1e3, "clocks": clk.summary(t0, t1),
+        "gpu_launches": 2 * steps, "roofline": roof, "e2e": None,
+        "config": {"workload": args.workload, "T": T, "heads": H, "kv_lora": C, "qk_nope": dn, "v_head": dv,
+                   "l2": f"wkv_b rotates over {R} copies ({R * w_bytes / 1e6:.0f} MB > 3x L2)"},
+        "dtype": "bf16 x bf16(dequantised e4m3) -> f32 accumulate, bf16 out",
+    }
+
+
 def run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     """The 671B gate (sigmoid scores, per-expert bias, 8 groups with 4 kept,
     top-8, route_scale 2.5) on T tokens of fp32 logits, then the routing
@@ -753,7 +813,8 @@ def run_reference(args, kind, shape, steps, warmup):
 def main():
     args = parse()
     kind, shape = WORKLOADS[args.workload]
-    big = kind == "linear" and shape["M"] >= 2048 or kind in ("dequant", "ffn", "moe")
+    big = kind == "linear" and shape["M"] >= 2048 or kind in ("dequant", "ffn", "moe") or \
+        kind == "mla" and shape["T"] >= 2048
     steps = args.steps if args.steps is not None else (200 if big else 100000)
     warmup = args.warmup if args.warmup is not None else (10 if big else 1000)
     if warmup < 3:
@@ -783,6 +844,8 @@ def main():
         res = run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     elif kind == "gate":
         res = run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
+    elif kind == "mla":
+        res = run_mla(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     else:
         res = run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     cpu = None

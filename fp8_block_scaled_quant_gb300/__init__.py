@@ -322,6 +322,24 @@ def moe_permute(topk_idx: torch.Tensor, E: int):
     return counts, offsets, perm[: T * k]
 
 
+def mla_absorb(inp: torch.Tensor, wkv_b: torch.Tensor, wkv_b_s: torch.Tensor, mode: str,
+               out: torch.Tensor | None = None, dn: int = 128, dv: int = 128) -> torch.Tensor:
+    """MLA absorb projections with the FP8 wkv_b (e4m3 [H*(dn+dv), C] + block scales).
+    mode "qk": q_nope bf16 [T, H, dn] -> bf16 [T, H, C]; mode "v": x bf16 [T, H, C] -> bf16 [T, H, dv]."""
+    _need(inp, torch.bfloat16, "inp", ndim=3)
+    _need(wkv_b, torch.float8_e4m3fn, "wkv_b")
+    _need(wkv_b_s, torch.float32, "wkv_b_s")
+    T, H = inp.shape[0], inp.shape[1]
+    C = wkv_b.shape[1]
+    if out is None:
+        out = torch.empty((T, H, C if mode == "qk" else dv), dtype=torch.bfloat16, device=inp.device)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    name = "fp8blk_mla_absorb_qk" if mode == "qk" else "fp8blk_mla_absorb_v"
+    f = _set_types(name, [vp] * 4 + [i64] * 5 + [vp])
+    _check(f(_ptr(inp), _ptr(wkv_b), _ptr(wkv_b_s), _ptr(out), T, H, dn, dv, C, _stream(inp.device)), name)
+    return out
+
+
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 
 

@@ -216,6 +216,27 @@ FP8BLK_API int fp8blk_moe_permute(const int32_t *topk_idx, int64_t T, int64_t to
                                   fp8blk_stream_t stream);
 
 /*
+ * MLA "absorb" projections with the FP8 wkv_b ("Administrator & Developer
+ * Guide", 8.3 steps 5 and 7, attn_impl "absorb"). wkv_b: e4m3 [H*(dn+dv), C]
+ * with 128x128 block scales wkv_b_s fp32 [H*(dn+dv)/128, C/128]; head h owns
+ * rows h*(dn+dv) .. +dn (no-positional part) and the dv rows after them (v).
+ * W is wkv_b as weight_dequant gives it: bf16(fp32(code) * block scale).
+ *   qk: q_nope bf16 [T, H, dn] -> out bf16 [T, H, C],
+ *       out[t,h,c] = bf16( sum over d < dn of q_nope[t,h,d] * W[h*(dn+dv) + d, c] );
+ *   v:  x bf16 [T, H, C] -> out bf16 [T, H, dv],
+ *       out[t,h,d] = bf16( sum over c < C of x[t,h,c] * W[h*(dn+dv) + dn + d, c] ).
+ * Products of bf16 numbers summed in fp32 (tensor cores, bf16 inputs). Shapes:
+ * dn == dv == 128 (every config's qk_nope_head_dim and v_head_dim), C % 128 == 0
+ * (kv_lora_rank), H >= 1, T >= 0; else FP8BLK_ERR_SHAPE. Activations, weights
+ * and outputs 16-byte aligned, scales 4-byte aligned. No workspace.
+ */
+FP8BLK_API int fp8blk_mla_absorb_qk(const void *q_nope_bf16, const void *wkv_b_e4m3, const float *wkv_b_s,
+                                    void *out_bf16, int64_t T, int64_t H, int64_t dn, int64_t dv, int64_t C,
+                                    fp8blk_stream_t stream);
+FP8BLK_API int fp8blk_mla_absorb_v(const void *x_bf16, const void *wkv_b_e4m3, const float *wkv_b_s, void *out_bf16,
+                                   int64_t T, int64_t H, int64_t dn, int64_t dv, int64_t C, fp8blk_stream_t stream);
+
+/*
  * MoE gate ("Administrator & Developer Guide", 8.4 the Gate and 3.3 per-config
  * fields; "Repository overview" page, MoE data flow: scores, optional group
  * masking, top-k indices, the original scores, normalize, route_scale).

@@ -1,0 +1,82 @@
+"""GPU parity of the MLA absorb projections against the CPU oracle.
+
+Both sides use the dequantised weight bf16(fp32(code) * scale) and bf16
+activations. The oracle sums the exact products in fp64; the tensor cores sum
+them in fp32. Tolerance per element: one bf16 step of the result (2^-8 |ref|)
+plus 1e-3 of the output's rms for sums that cancel."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_quant_gb300 as fb
+import oracle
+import synthetic
+from helpers import bits_to_dev_bf16, dev_to_bits
+
+pytestmark = pytest.mark.gpu
+DN = DV = 128
+
+
+def close(got_bits, ref_bits, rms=None, what=""):
+    got = synthetic.bf16_bits_to_f32(got_bits).astype(np.float64)
+    ref = synthetic.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    if rms is None:
+        rms = float(np.sqrt(np.mean(ref ** 2)))
+    bad = np.abs(got - ref) > 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside, e.g. {got[bad][:4]} vs {ref[bad][:4]}"
+
+
+def weights(H, C, seed):
+    return oracle.weight_quant(synthetic.weights(H * (DN + DV), C, seed))
+
+
+def dev_w(wq, ws):
+    return torch.from_numpy(wq).cuda().view(torch.float8_e4m3fn), torch.from_numpy(ws).cuda()
+
+
+@pytest.mark.parametrize("T,H,C", [(5, 3, 256), (130, 2, 512), (1, 4, 512), (257, 1, 128)])
+@pytest.mark.parametrize("mode", ["qk", "v"])
+def test_mla_full_compare(T, H, C, mode):
+    wq, ws = weights(H, C, 300 + T + H)
+    width = DN if mode == "qk" else C
+    a = synthetic.activations(T, H * width, 301 + T)
+    out = fb.mla_absorb(bits_to_dev_bf16(a).view(T, H, width), *dev_w(wq, ws), mode)
+    ref = oracle.mla_absorb(a, wq, ws, H, DN, DV, mode)
+    close(dev_to_bits(out), ref, what=f"mla {mode} T={T} H={H} C={C}")
+    assert fb.last_device_error() == 0
+
+
+@pytest.mark.parametrize("T", [64, 2048])
+@pytest.mark.parametrize("mode", ["qk", "v"])
+def test_mla_full_size_sampled(T, mode):
+    """128 heads, kv_lora 512 (the 671B MLA); the oracle recomputes sampled
+    tokens of sampled heads (a sub-problem with only those heads' weights)."""
+    H, C = 128, 512
+    wq, ws = weights(H, C, 400 + T)
+    width = DN if mode == "qk" else C
+    a = synthetic.activations(T, H * width, 401 + T)
+    out = dev_to_bits(fb.mla_absorb(bits_to_dev_bf16(a).view(T, H, width), *dev_w(wq, ws), mode))
+    tokens = np.array(sorted({0, 1, T // 2, T - 1}))
+    heads = np.array([0, 63, 127])
+    rows = np.concatenate([np.arange(h * (DN + DV), (h + 1) * (DN + DV)) for h in heads])
+    srows = np.concatenate([np.arange(2 * h, 2 * h + 2) for h in heads])
+    sub = a.reshape(T, H, width)[tokens][:, heads].reshape(len(tokens), -1)
+    ref = oracle.mla_absorb(sub, wq[rows], ws[srows], len(heads), DN, DV, mode)
+    got = out[tokens][:, heads]
+    rms = float(np.sqrt(np.mean(synthetic.bf16_bits_to_f32(out).astype(np.float64) ** 2)))
+    close(got, ref, rms=rms, what=f"mla {mode} sampled T={T}")
+    assert fb.last_device_error() == 0
+
+
+def test_mla_argument_errors():
+    L = fb.lib()
+    x = torch.zeros((4, 2, 128), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((512, 256), dtype=torch.float8_e4m3fn, device="cuda")
+    s = torch.ones((4, 2), dtype=torch.float32, device="cuda")
+    y = torch.zeros((4, 2, 256), dtype=torch.bfloat16, device="cuda")
+    p = lambda t: t.data_ptr()
+    assert L.fp8blk_mla_absorb_qk(p(x), p(w), p(s), p(y), 4, 2, 64, 128, 256, None) == 2     # dn != 128
+    assert L.fp8blk_mla_absorb_qk(p(x), p(w), p(s), p(y), 4, 2, 128, 128, 200, None) == 2    # C % 128
+    assert L.fp8blk_mla_absorb_qk(None, p(w), p(s), p(y), 4, 2, 128, 128, 256, None) == 1
+    assert L.fp8blk_mla_absorb_qk(p(x) + 2, p(w), p(s), p(y), 4, 2, 128, 128, 256, None) == 3
+    assert L.fp8blk_mla_absorb_v(None, None, None, None, 0, 2, 128, 128, 256, None) == 0     # T == 0
