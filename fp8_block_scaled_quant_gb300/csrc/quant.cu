@@ -66,9 +66,12 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint4* __re
                                                                float* __restrict__ s, int64_t nblocks,
                                                                bool ue8m0, bool trigger) {
   // Launched programmatically, this kernel may start before the previous one
-  // on the stream ends: x is read only after that kernel has completed.
-  griddep_wait();
+  // on the stream ends: x is read only after that kernel has completed. The
+  // next kernel (the GEMM that reads q and s only after its own dependency
+  // wait, which follows this kernel's completion and so the previous one's)
+  // may launch at once and start streaming its weights meanwhile.
   if (trigger) griddep_launch_dependents();
+  griddep_wait();
   const int sub = threadIdx.x & 15;
   const int half = (threadIdx.x >> 4) & 1;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kAqThreads + threadIdx.x) >> 5;

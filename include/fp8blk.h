@@ -33,9 +33,11 @@
  *     same stream start early (programmatic dependent launch). That kernel
  *     may begin loading its WEIGHT operands (w, w1, w3, w2) before the
  *     previous one has finished; it reads activations and scales, and writes
- *     anything, only after. So a weight operand must not be the output of the
- *     library call issued just before it on the same stream. Kernels of other
- *     libraries are ordered as usual.
+ *     anything, only after. Inside fp8blk_linear / fp8blk_ffn the GEMM's
+ *     weight loads may even start while the library call before is still
+ *     running. So a weight operand must not be the output of either of the
+ *     two library calls issued just before it on the same stream. Kernels of
+ *     other libraries are ordered as usual.
  */
 #ifndef FP8BLK_H
 #define FP8BLK_H
