@@ -416,10 +416,12 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
 
 
 def run_e2e(shape, dev, torch, fb, qs, ss, n, hbm_bound, step_bytes, flops):
-    """End to end through fp8blk_linear_host: each step copies X from pinned
-    host memory, runs the layer, and copies Y back; timed on the stream and by
-    the wall clock (the larger counts). The weight rotates over the same
-    copies as the device-timed leg, so no step finds its weight in L2."""
+    """End to end through fp8blk_linear_host on pinned host buffers: each step's
+    X comes from host memory and its Y lands in host memory (the layer's
+    kernels read and write the pinned buffers over the chip-to-chip link);
+    timed on the stream and by the wall clock (the larger counts). The weight
+    rotates over the same copies as the device-timed leg, so no step finds its
+    weight in L2."""
     M, N, K = shape["M"], shape["N"], shape["K"]
     xh = [synthetic.device_activations(M, K, shape["seed"] + 7 + i, dev, shape["frac"]).cpu().pin_memory()
           for i in range(4)]

@@ -225,9 +225,10 @@ def linear(x: torch.Tensor, w: torch.Tensor, w_s: torch.Tensor, scale_fmt: int =
 
 def linear_host(x_host: torch.Tensor, w: torch.Tensor, w_s: torch.Tensor, y_host: torch.Tensor,
                 scale_fmt: int = SCALE_FP32, ws: torch.Tensor | None = None) -> torch.Tensor:
-    """The FP8 linear layer on host (preferably pinned) bf16 buffers: enqueues the
-    copy in, the layer, and the copy out on the current stream of w's device.
-    y_host is valid after that stream is synchronised."""
+    """The FP8 linear layer on host bf16 buffers, enqueued on the current stream of
+    w's device: pinned buffers are read and written in place by the kernels,
+    pageable ones are copied in and out. y_host is valid after that stream is
+    synchronised."""
     if x_host.is_cuda or y_host.is_cuda:
         raise Fp8BlkError("x_host and y_host must be host tensors")
     if x_host.dtype != torch.bfloat16 or y_host.dtype != torch.bfloat16:

@@ -170,6 +170,16 @@ extern "C" int fp8blk_linear_host(const void* x_host, const void* w_e4m3, const 
   uint8_t* xd = ws;
   uint8_t* yd = ws + align256(xb);
   uint8_t* lws = yd + align256(yb);
+  // Pinned host buffers the device can address (every page-locked allocation
+  // on a unified-address system such as a Grace + GB300 node): the layer reads
+  // x from and writes y to them directly over the chip-to-chip link, with no
+  // staging copies, so its kernels stay one chain of dependent launches.
+  void* xm = nullptr;
+  void* ym = nullptr;
+  if (cudaHostGetDevicePointer(&xm, const_cast<void*>(x_host), 0) == cudaSuccess &&
+      cudaHostGetDevicePointer(&ym, y_host, 0) == cudaSuccess && is_aligned(xm, 16) && is_aligned(ym, 16))
+    return fp8blk_linear(xm, w_e4m3, w_s, ym, M, N, K, scale_fmt, lws, workspace_bytes - (lws - ws), stream);
+  cudaGetLastError();  // an unregistered buffer is not an error here: copy it instead
   if (K > 0 && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
   if (int st = fp8blk_linear(xd, w_e4m3, w_s, yd, M, N, K, scale_fmt, lws, workspace_bytes - (lws - ws), stream))
     return st;

@@ -155,12 +155,14 @@ FP8BLK_API int fp8blk_linear(const void *x_bf16, const void *w_e4m3, const float
                   int64_t K, int scale_fmt, void *workspace, size_t workspace_bytes, fp8blk_stream_t stream);
 
 /*
- * The same layer with the activation and the result in HOST memory: copies
- * x_host (bf16 [M, K]) to the device workspace, runs fp8blk_linear, and copies
- * y back to y_host (bf16 [M, N]), all enqueued on `stream`. Host buffers
- * should be page-locked (cudaHostAlloc / pinned) for the copies to be
- * asynchronous; y_host is valid once the stream has been synchronised. The
- * weight stays on the device. Workspace: fp8blk_linear_host_workspace_bytes.
+ * The same layer with the activation and the result in HOST memory
+ * (x_host bf16 [M, K], y_host bf16 [M, N]), enqueued on `stream`; y_host is
+ * valid once the stream has been synchronised. The weight stays on the device.
+ * Page-locked buffers the device can address (cudaHostAlloc / pinned memory on
+ * a unified-address system), 16-byte aligned, are read and written in place by
+ * the layer's kernels (no staging copies). Any other buffer is copied to the
+ * workspace and back (page-locked memory keeps those copies asynchronous).
+ * Workspace: fp8blk_linear_host_workspace_bytes.
  */
 FP8BLK_API size_t fp8blk_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
 FP8BLK_API int fp8blk_linear_host(const void *x_host_bf16, const void *w_e4m3, const float *w_s, void *y_host_bf16,

@@ -210,11 +210,18 @@ def test_linear_matches_quant_then_gemm():
     assert_gemm_close(dev_to_bits(y), oracle.gemm(xq, xs, wq, ws))
 
 
-def test_linear_host_buffers():
-    x, w, xq, xs, wq, ws = host_problem(8, 10944, 2048, 22, 0.01)
+@pytest.mark.parametrize("M", [1, 8, 64])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_linear_host_buffers(M, pinned):
+    """Host x and y: pinned buffers are read and written in place by the
+    kernels, pageable ones go through staging copies; both give the device
+    layer's bits."""
+    x, w, xq, xs, wq, ws = host_problem(M, 10944, 2048, 22, 0.01)
     q, s = fb.weight_quant(torch.from_numpy(w).cuda())
-    xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
-    yh = torch.empty((8, 10944), dtype=torch.bfloat16).pin_memory()
+    xh = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16)
+    yh = torch.empty((M, 10944), dtype=torch.bfloat16)
+    if pinned:
+        xh, yh = xh.pin_memory(), yh.pin_memory()
     fb.linear_host(xh, q, s, yh)
     torch.cuda.current_stream().synchronize()
     y = fb.linear(bits_to_dev_bf16(x), q, s)
