@@ -51,6 +51,9 @@ WORKLOADS = {
     "pr1_linear_16x320x256": ("linear", dict(M=16, N=320, K=256, frac=0.0, seed=synthetic.SEED_PR1)),
     "prefill_gemm_w1": ("linear", dict(M=4096, N=18432, K=7168, frac=0.0, seed=synthetic.SEED_PREFILL)),
     "prefill_gemm_w2": ("linear", dict(M=4096, N=7168, K=18432, frac=0.0, seed=synthetic.SEED_PREFILL)),
+    # power-of-two (UE8M0) scales on activations and weights: the tensor core applies them
+    "prefill_gemm_w1_ue8m0": ("linear", dict(M=4096, N=18432, K=7168, frac=0.0, seed=synthetic.SEED_PREFILL, fmt=1)),
+    "prefill_gemm_w2_ue8m0": ("linear", dict(M=4096, N=7168, K=18432, frac=0.0, seed=synthetic.SEED_PREFILL, fmt=1)),
     "attn_wq_b_m2048": ("linear", dict(M=2048, N=24576, K=1536, frac=0.0, seed=synthetic.SEED_ATTN)),
     "attn_wkv_b_m2048": ("linear", dict(M=2048, N=32768, K=512, frac=0.0, seed=synthetic.SEED_ATTN)),
     "attn_wq_a_m2048": ("linear", dict(M=2048, N=1536, K=7168, frac=0.0, seed=synthetic.SEED_ATTN)),
@@ -61,7 +64,10 @@ WORKLOADS = {
     "attn_wkv_a_m64": ("linear", dict(M=64, N=576, K=7168, frac=0.0, seed=synthetic.SEED_ATTN)),
     "weight_dequant_18432x7168": ("dequant", dict(N=18432, K=7168, seed=synthetic.SEED_ATTN)),
     "prefill_ffn_4096": ("ffn", dict(M=4096, dim=7168, inter=18432, seed=synthetic.SEED_PREFILL)),
+    "prefill_ffn_4096_ue8m0": ("ffn", dict(M=4096, dim=7168, inter=18432, seed=synthetic.SEED_PREFILL, fmt=1)),
     "moe_t4096_uniform": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, seed=synthetic.SEED_MOE)),
+    "moe_t4096_uniform_ue8m0": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, fmt=1,
+                                            seed=synthetic.SEED_MOE)),
     "moe_t4096_zipf": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=1.2, seed=synthetic.SEED_MOE)),
     "moe_t4096_uniform_shared": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, shared=1,
                                              seed=synthetic.SEED_MOE)),
@@ -313,19 +319,20 @@ def timed_replay(graphs, stream, torch):
 
 def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     M, N, K, frac, seed = shape["M"], shape["N"], shape["K"], shape["frac"], shape["seed"]
+    fmt = shape.get("fmt", 0)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
     w_bytes = N * K
     R = max(2, math.ceil(3 * l2 / w_bytes))
     R = min(R, 64)
     w = synthetic.device_normal((N, K), seed + 1, 0.02, dev)
-    q0, s0 = fb.weight_quant(w)
+    q0, s0 = fb.weight_quant(w, fmt)
     del w
     qs = [q0] + [q0.clone() for _ in range(R - 1)]
     ss = [s0] + [s0.clone() for _ in range(R - 1)]
     xs = [synthetic.device_activations(M, K, seed + i, dev, outlier_frac=frac) for i in range(R)]
     ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    aqs = [fb.act_quant(x) for x in xs]   # for the GEMM-only pass
+    aqs = [fb.act_quant(x, fmt) for x in xs]   # for the GEMM-only pass
     ws = fb.workspace(fb.linear_workspace_bytes(M, N, K), dev, "bench")
     gws = fb.workspace(fb.gemm_workspace_bytes(M, N, K), dev, "bench_gemm")
     aq_buf = [(torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev),
@@ -333,15 +340,15 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
 
     def step(i):
         r = i % R
-        fb.linear(xs[r], qs[r], ss[r], out=ys[r], ws=ws)
+        fb.linear(xs[r], qs[r], ss[r], scale_fmt=fmt, out=ys[r], ws=ws)
 
     def gemm_only(i):
         r = i % R
-        fb.fp8_gemm(aqs[r][0], aqs[r][1], qs[r], ss[r], out=ys[r], ws=gws)
+        fb.fp8_gemm(aqs[r][0], aqs[r][1], qs[r], ss[r], scale_fmt=fmt, out=ys[r], ws=gws)
 
     def aq_only(i):
         r = i % R
-        fb.act_quant(xs[r], q=aq_buf[r][0], s=aq_buf[r][1])
+        fb.act_quant(xs[r], fmt, q=aq_buf[r][0], s=aq_buf[r][1])
 
     for i in range(3):   # eager warm-up: sets kernel attributes, loads modules
         step(i)
@@ -377,6 +384,8 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     gemm_s = el_gemm / steps
     kern_s, kern_b = (el / steps, step_bytes) if fused else (gemm_s, gemm_b)
     kern_name = "fp8blk_linear (act_quant fused into the GEMM)" if fused else "fp8_gemm"
+    if fmt and not fused and M > 128:
+        kern_name += " (UE8M0 scales applied by the tensor core)"
     if hbm_bound:
         metric_val = units / el_max / 1e9
         unit = "GB/s"
@@ -407,7 +416,9 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
         "kernels_us": {"linear_step": el / steps * 1e6, "act_quant_alone": el_aq / steps * 1e6,
                        "fp8_gemm_alone": gemm_s * 1e6},
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "outlier_channels": frac,
-                   "x": "bf16 N(0,1)", "w": "e4m3 from N(0,0.02), fp32 128x128 block scales",
+                   "x": "bf16 N(0,1)",
+                   "w": "e4m3 from N(0,0.02), " + ("power-of-two (UE8M0)" if fmt else "fp32") + " 128x128 block scales",
+                   "scale_fmt": "ue8m0" if fmt else "fp32",
                    "l2": f"weights rotate over {R} copies ({R * w_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
                    "launch": "host loop" if args.eager else f"CUDA graphs of {chunk} steps"},
         "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
@@ -423,13 +434,14 @@ def run_e2e(shape, dev, torch, fb, qs, ss, n, hbm_bound, step_bytes, flops):
     rotates over the same copies as the device-timed leg, so no step finds its
     weight in L2."""
     M, N, K = shape["M"], shape["N"], shape["K"]
+    fmt = shape.get("fmt", 0)
     xh = [synthetic.device_activations(M, K, shape["seed"] + 7 + i, dev, shape["frac"]).cpu().pin_memory()
           for i in range(4)]
     yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(4)]
     ws = fb.workspace(fb.linear_host_workspace_bytes(M, N, K), dev, "bench_e2e")
     R = len(qs)
     for i in range(3):
-        fb.linear_host(xh[i % 4], qs[i % R], ss[i % R], yh[i % 4], ws=ws)
+        fb.linear_host(xh[i % 4], qs[i % R], ss[i % R], yh[i % 4], scale_fmt=fmt, ws=ws)
     stream = torch.cuda.current_stream(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -437,7 +449,7 @@ def run_e2e(shape, dev, torch, fb, qs, ss, n, hbm_bound, step_bytes, flops):
     t0 = time.time()
     start.record(stream)
     for i in range(n):
-        fb.linear_host(xh[i % 4], qs[i % R], ss[i % R], yh[i % 4], ws=ws)
+        fb.linear_host(xh[i % 4], qs[i % R], ss[i % R], yh[i % 4], scale_fmt=fmt, ws=ws)
     end.record(stream)
     torch.cuda.synchronize()
     wall = time.time() - t0
@@ -453,24 +465,25 @@ def run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     """Dense SwiGLU FFN: act_quant(x), the fused w1/w3 GEMM (SwiGLU + act_quant
     epilogue), the w2 GEMM. Tensor-bound: 3 * 2 * M * dim * inter flops."""
     M, dim, inter, seed = shape["M"], shape["dim"], shape["inter"], shape["seed"]
+    fmt = shape.get("fmt", 0)
     x = synthetic.device_activations(M, dim, seed, dev)
     sets = []
     for c in range(2):   # two weight copies: 792 MB > 3x L2 between consecutive steps
         ws_ = [synthetic.device_normal(sh, seed + 10 + i, 0.02, dev) for i, sh in
                enumerate([(inter, dim), (inter, dim), (dim, inter)])]
-        sets.append([fb.weight_quant(w) for w in ws_])
+        sets.append([fb.weight_quant(w, fmt) for w in ws_])
         del ws_
     y = torch.empty((M, dim), dtype=torch.bfloat16, device=dev)
-    xq, xs = fb.act_quant(x)
+    xq, xs = fb.act_quant(x, fmt)
     wsp = fb.workspace(0, dev, "ffn")
 
     def step(i):
         (q1, s1), (q3, s3), (q2, s2) = sets[i % 2]
-        fb.ffn(x, q1, s1, q3, s3, q2, s2, out=y)
+        fb.ffn(x, q1, s1, q3, s3, q2, s2, scale_fmt=fmt, out=y)
 
     def swiglu_only(i):
         (q1, s1), (q3, s3), _ = sets[i % 2]
-        fb.swiglu_gemm(xq, xs, q1, s1, q3, s3)
+        fb.swiglu_gemm(xq, xs, q1, s1, q3, s3, scale_fmt=fmt)
 
     for i in range(3):
         step(i)
@@ -503,6 +516,7 @@ def run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
                      "kernel_us": el_swi / steps * 1e6},
         "e2e": None, "kernels_us": {"swiglu_gemm": el_swi / steps * 1e6},
         "config": {"workload": args.workload, "M": M, "dim": dim, "inter": inter,
+                   "scale_fmt": "ue8m0" if fmt else "fp32",
                    "l2": "two weight sets (792 MB) alternate between steps"},
         "dtype": "e4m3 x e4m3 -> f32 accumulate; SwiGLU in fp32/bf16; e4m3 re-quantisation",
     }
@@ -519,15 +533,16 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     HBM-bound on the touched experts' weights at this token count."""
     T, E, dim, inter, k, seed = (shape[n] for n in ("T", "E", "dim", "inter", "k", "seed"))
     ns = shape.get("shared", 0)
+    fmt = shape.get("fmt", 0)
     x = synthetic.device_activations(T, dim, seed, dev)
-    xq, xs = fb.act_quant(x)
+    xq, xs = fb.act_quant(x, fmt)
     idx_np, w_np = synthetic.moe_routing(T, E, k, seed, zipf_s=shape["zipf"])
     idx = torch.from_numpy(idx_np).to(dev)
     wts = torch.from_numpy(w_np).to(dev)
     stacks = []
     for which in range(3):
         sh = (inter, dim) if which < 2 else (dim, inter)
-        qs, ss = zip(*[fb.weight_quant(synthetic.device_normal(sh, seed * 100000 + 3 * e + which, 0.02, dev))
+        qs, ss = zip(*[fb.weight_quant(synthetic.device_normal(sh, seed * 100000 + 3 * e + which, 0.02, dev), fmt)
                        for e in range(E + ns)])
         stacks.append((torch.cat(qs), torch.cat(ss)))
         del qs, ss
@@ -535,7 +550,7 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     (q1, s1), (q3, s3), (q2, s2) = stacks
 
     def step(i):
-        fb.moe_grouped_gemm(xq, xs, idx, wts, q1, s1, q3, s3, q2, s2, E, out=y, n_shared=ns)
+        fb.moe_grouped_gemm(xq, xs, idx, wts, q1, s1, q3, s3, q2, s2, E, scale_fmt=fmt, out=y, n_shared=ns)
 
     for i in range(3):
         step(i)
@@ -566,6 +581,7 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
         "e2e": None,
         "config": {"workload": args.workload, "T": T, "E": E, "dim": dim, "inter": inter, "topk": k,
                    "routing": "Zipf(1.2)" if shape["zipf"] else "uniform", "shared_experts": ns,
+                   "scale_fmt": "ue8m0" if fmt else "fp32",
                    "experts_touched": touched,
                    "l2": f"{touched} experts' weights ({moe_weight_bytes(touched, dim, inter) / 1e9:.2f} GB) per step"},
         "dtype": "e4m3 x e4m3 -> f32 accumulate; SwiGLU in fp32/bf16; e4m3 re-quantisation",

@@ -52,6 +52,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "fp8blk.h"
@@ -190,8 +192,19 @@ constexpr int pow2_at_least(int v, int floor_) {
 #endif
 
 template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_, int MODE_ = kEpiBf16, bool GROUPED_ = false,
-          bool FUSED_ = false, int CLUSTER_ = 1>
+          bool FUSED_ = false, int CLUSTER_ = 1, bool MX_ = false>
 struct Cfg {
+  // MX: power-of-two (UE8M0) scales applied by the tensor core itself
+  // (tcgen05.mma kind::mxf8f6f4.block_scale). The scale of a K block is the
+  // same number for every 32-element MMA slice in it, so one UE8M0 scale per
+  // operand row and slice gives exactly a_s * w_s * partial, and the fp32
+  // accumulator stays in TMEM over the whole K range: no per-block promotion.
+  // A scale-writer warpgroup (warps 4-7) turns the fp32 scales into UE8M0
+  // bytes in a TMEM ring (16 columns per slot: 4 of activation-row scales, 8
+  // of weight-row scales; each 32-bit column holds the scales of 4 K blocks,
+  // chosen by the MMA's sf_id); the epilogue (warps 8-15) only drains the
+  // finished accumulator.
+  static constexpr bool MX = MX_;
   // CLUSTER = 2: two CTAs with adjacent 128-row lane tiles and the same column
   // tile form a cluster. Each loads its own lane tile and one half of the
   // shared column tile, multicast into both, so every CTA reads 2/3 of the
@@ -222,10 +235,14 @@ struct Cfg {
   // 128 accumulators next to 64 freshly loaded TMEM columns. The launch holds
   // kThreads x 168 registers; the split hands out exactly that many.
   static constexpr bool kSplitRegs = !SWAP && !FUSED && EPI_WARPS == 8 && kCpt == 128;
-  static constexpr int kEpiWarp0 = kSplitRegs ? 4 : 2;  // first epilogue warp
+  static constexpr int kSfWarp0 = 4;                             // MX: first scale-writer warp
+  static constexpr int kEpiWarp0 = MX ? 8 : kSplitRegs ? 4 : 2;  // first epilogue warp
   static constexpr int kThreads = (kEpiWarp0 + EPI_WARPS) * 32;
-  static constexpr int kLaunchRegs = 168;
-  static constexpr int kRegsLow = 56, kRegsHigh = 224;
+  static constexpr int kLaunchRegs = MX ? 128 : 168;
+  static constexpr int kRegsLow = 56, kRegsHigh = MX ? 200 : 224;
+  // MX scale ring: slots of 16 TMEM columns after the accumulator, 4 K blocks each.
+  static constexpr int kSfSlots = MX ? 8 : 0;
+  static constexpr int kSfCol0 = P * BN;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = FUSED ? kABytes : kABytes + kBBytes;
@@ -233,8 +250,8 @@ struct Cfg {
   // L2 before the dependency wait, so the whole weight tile streams from DRAM
   // while the previous kernel finishes.
   static constexpr int kL2Ahead = SWAP ? FP8BLK_DECODE_L2_AHEAD : 0;
-  static constexpr int kTmemCols = pow2_at_least(P * BN, 32);
-  static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16;
+  static constexpr int kTmemCols = pow2_at_least(P * BN + 16 * kSfSlots, 32);
+  static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16 + 2 * kSfSlots * 8;
   static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + kGroupBytes + kXchgBytes;
 
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -248,7 +265,10 @@ struct Cfg {
                 "non-swapped tiles: a column group lies inside one weight block");
   static_assert(!SWAP || kGroups == 1, "swapped tiles: one column group");
   static_assert(P * BN <= 512, "TMEM has 512 columns");
-  static_assert(!kSplitRegs || (128 * kRegsLow + EPI_WARPS * 32 * kRegsHigh <= kThreads * kLaunchRegs &&
+  static_assert(kSfCol0 + 16 * kSfSlots <= 512, "TMEM has 512 columns");
+  static_assert(!MX || (!SWAP && !FUSED && BN == 256 && P == 1 && EPI_WARPS == 8 && kSplitRegs),
+                "MX: 128 x 256 tiles with activation rows as lanes, one accumulator");
+  static_assert(!kSplitRegs || (kEpiWarp0 * 32 * kRegsLow + EPI_WARPS * 32 * kRegsHigh <= kThreads * kLaunchRegs &&
                                 kThreads * kLaunchRegs <= 65536),
                 "the register split must fit the registers the CTA is launched with");
   static_assert(CLUSTER == 1 || (CLUSTER == 2 && !SWAP && !GROUPED && !FUSED && BN == 256),
@@ -466,6 +486,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   int* grp_rows = reinterpret_cast<int*>(tail + C::kBarBytes);
   int* grp_mtiles = grp_rows + (kMaxGroups + 4);
   float* xchg = reinterpret_cast<float*>(tail + C::kBarBytes + C::kGroupBytes);
+  // MX scale ring: sf_full (the four scale writers have stored a slot),
+  // sf_empty (the MMAs that read a slot have completed).
+  uint64_t* sf_full = reinterpret_cast<uint64_t*>(tail + (2 * C::STAGES + 2 * C::P + 3) * 8 + 16);
+  uint64_t* sf_empty = sf_full + C::kSfSlots;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Cluster rank, and the index of the schedule this CTA (pair) walks.
@@ -491,6 +515,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(epi_bar, C::EPI_WARPS);
     mbar_init(act_ready, C::EPI_WARPS);
+    for (int q = 0; q < C::kSfSlots; ++q) {
+      mbar_init(&sf_full[q], 4);
+      mbar_init(&sf_empty[q], 1);
+    }
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -650,6 +678,67 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    if constexpr (C::MX) {
+    // ---------------- MMA issuer, tensor-core scaling ----------------
+    // One accumulator per unit: the first MMA of the unit overwrites it, every
+    // later one adds. A K block waits for its operands and, at the start of
+    // each group of 4 K blocks, for its scale slot; the slot is released
+    // after the group's MMAs, the accumulator after the unit's last.
+    const bool leader = elect_one_sync();
+    Sched sch(prm, worker, grouped_tiles, krank);
+    Unit u;
+    int st = 0, sfs = 0;
+    uint32_t ph = 0, sfph = 0, tph = 0;
+    bool ok = true;
+    const uint32_t sf0 = tmem_base + static_cast<uint32_t>(C::kSfCol0);
+    while (ok && sch.next(u)) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[0], tph ^ 1u, abort_flag, prm.err, kDevErrTimeoutMma))) {
+        ok = false;
+        break;
+      }
+      for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        const int g = kb - u.kb0;
+        const bool last = kb + 1 == u.kb1;
+        const bool slot_end = (g & 3) == 3 || last;
+        bool w = mbar_wait(&full[st], ph, abort_flag, prm.err, kDevErrTimeoutMma);
+        if ((g & 3) == 0) w = w && mbar_wait(&sf_full[sfs], sfph, abort_flag, prm.err, kDevErrTimeoutMma);
+        if (!__all_sync(0xFFFFFFFFu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_addr = smem_u32(smem + st * C::kStageBytes);
+        const uint64_t ad = sdesc_kmajor_sw128(a_addr);
+        const uint64_t bd = sdesc_kmajor_sw128(a_addr + C::kABytes);
+        const uint32_t idesc = idesc_mx_e4m3(128, C::BN, static_cast<uint32_t>(g & 3));
+        const uint32_t sfa = sf0 + static_cast<uint32_t>(sfs * 16);
+        if (leader) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_mx_e4m3(tmem_base, ad + 2 * k, bd + 2 * k, idesc, sfa, sfa + 4, (g > 0 || k > 0) ? 1u : 0u);
+          if constexpr (C::CLUSTER > 1) mma_commit_multicast(&empty[st], 0x3);
+          else mma_commit(&empty[st]);
+          if (slot_end) mma_commit(&sf_empty[sfs]);
+          if (last) mma_commit(&tfull[0]);
+        }
+        __syncwarp();
+        if (++st == C::STAGES) {
+          st = 0;
+          ph ^= 1u;
+        }
+        if (slot_end && ++sfs == C::kSfSlots) {
+          sfs = 0;
+          sfph ^= 1u;
+        }
+      }
+      tph ^= 1u;
+    }
+    if (leader) {
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr, prm.err, kDevErrTimeoutDrain);
+    }
+    __syncwarp();
+    } else {
     // ---------------- MMA issuer ----------------
     // The whole warp walks the schedule and waits; one elected lane issues the
     // MMAs and commits, so the warp stays converged around the tcgen05 issue
@@ -731,6 +820,79 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_wait(drain, 0, nullptr, prm.err, kDevErrTimeoutDrain);
     }
     __syncwarp();
+    }
+  } else if (warp >= C::kSfWarp0) {
+    if constexpr (C::MX) {
+      // ---------------- scale writer (MX) ----------------
+      // For each group of 4 K blocks of a unit: the UE8M0 byte (the fp32
+      // exponent field of a power-of-two scale) of every activation row's and
+      // every weight row's scale, byte j for K block j of the group, stored
+      // the same way into each of the four TMEM lane quarters: lane l, column
+      // i holds operand row 32 i + l (columns 0-3 activation rows, 4-11 the
+      // 256 weight rows, one weight block per 128 rows). K blocks past the
+      // unit and rows past the matrix get 127 (a scale of 1).
+      const int quarter = warp & 3;
+      const uint32_t t_sf = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(C::kSfCol0);
+      griddep_wait();  // the activation scales come from the previous kernel
+      bool bad = false;
+      auto pack = [&](const float* src, int nk) -> uint32_t {
+        uint32_t w = 0x7F7F7F7Fu;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (j < nk) {
+            const uint32_t b = __float_as_uint(__ldg(src + j));
+            const uint32_t e = b >> 23;  // sign bit set: e >= 256
+            bad |= (b & 0x007FFFFFu) != 0u || e == 0u || e >= 255u;
+            w = (w & ~(0xFFu << (8 * j))) | ((e & 0xFFu) << (8 * j));
+          }
+        }
+        return w;
+      };
+      Sched sch(prm, worker, grouped_tiles, krank);
+      Unit u;
+      int sfs = 0;
+      uint32_t sfph = 0;
+      bool ok = true;
+      while (ok && sch.next(u)) {
+        const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
+        for (int k0 = u.kb0; k0 < u.kb1; k0 += 4) {
+          const int nk = u.kb1 - k0 < 4 ? u.kb1 - k0 : 4;
+          uint32_t wa[4], wb[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = 32 * i + lane;
+            wa[i] = r < t.lane_valid ? pack(prm.a_s + static_cast<size_t>(t.lane_y + r) * prm.Kb + k0, nk)
+                                     : 0x7F7F7F7Fu;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            // SwiGLU tiles: rows [0,64) w1, [64,128) w3, [128,192) w1, [192,256) w3, one block of each.
+            const float* ws = (C::MODE == kEpiSwiGLU && (i & 2)) ? prm.w3_s : prm.w_s;
+            const int nb = C::MODE == kEpiSwiGLU ? t.wblock : t.wblock + (i >> 2);
+            wb[i] = (C::GROUPED || C::MODE == kEpiSwiGLU || nb < prm.n_wblocks)
+                        ? pack(ws + static_cast<size_t>(nb) * prm.Kb + k0, nk)
+                        : 0x7F7F7F7Fu;
+          }
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait(&sf_empty[sfs], sfph ^ 1u, abort_flag, prm.err, kDevErrTimeoutEpilogue))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          tmem_st_32x32b_x4(t_sf + static_cast<uint32_t>(sfs * 16), wa);
+          tmem_st_32x32b_x8(t_sf + static_cast<uint32_t>(sfs * 16 + 4), wb);
+          tmem_wait_st();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sf_full[sfs]);
+          if (++sfs == C::kSfSlots) {
+            sfs = 0;
+            sfph ^= 1u;
+          }
+        }
+      }
+      if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(prm.err, kDevErrBadScale);
+    }
   }
   } else {
     if constexpr (C::kSplitRegs) setmaxnreg_inc<C::kRegsHigh>();
@@ -876,6 +1038,26 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     while (ok && sch.next(u)) {
       const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
       float acc[C::kCpt];
+      if constexpr (C::MX) {
+        // The unit's accumulator is complete in TMEM (scaled by the tensor
+        // core): read this thread's 128 columns, then free it for the next unit.
+        if (!mbar_wait(&tfull[0], pph, abort_flag, prm.err, kDevErrTimeoutEpilogue)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int h = 0; h < C::kCpt / 64; ++h) {
+          uint32_t v[64];
+          tmem_ld_32x32b_x64(t_lane + static_cast<uint32_t>(group * C::kCpt + h * 64), v);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) acc[h * 64 + i] = __uint_as_float(v[i]);
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[0]);
+        pph ^= 1u;
+      } else {
 #pragma unroll
       for (int i = 0; i < C::kCpt; ++i) acc[i] = 0.0f;
       ScaleRaw pipe[kAhead];
@@ -1000,6 +1182,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       }
       if (!ok) break;
+      }
       FP8BLK_TIC(t2);
       if (ksplit > 1) {
         // Split-K cluster: park the partial in this CTA's (now idle) stage
@@ -1169,6 +1352,23 @@ using CfgSwiGLU = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false>;
 using CfgSwiGLUC2 = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false, false, 2>;
 using CfgSwiGLUGrouped = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, true>;
 using CfgScatterGrouped = Cfg<256, false, 4, 2, 8, kEpiScatter, true>;
+// The same large-M tiles with power-of-two scales applied by the tensor core
+// (one TMEM accumulator per tile, no promotion).
+using CfgN256MX = Cfg<256, false, 4, 1, 8, kEpiBf16, false, false, 1, true>;
+using CfgN256C2MX = Cfg<256, false, 4, 1, 8, kEpiBf16, false, false, 2, true>;
+using CfgSwiGLUMX = Cfg<256, false, 4, 1, 8, kEpiSwiGLU, false, false, 1, true>;
+using CfgSwiGLUC2MX = Cfg<256, false, 4, 1, 8, kEpiSwiGLU, false, false, 2, true>;
+using CfgSwiGLUGroupedMX = Cfg<256, false, 4, 1, 8, kEpiSwiGLU, true, false, 1, true>;
+using CfgScatterGroupedMX = Cfg<256, false, 4, 1, 8, kEpiScatter, true, false, 1, true>;
+
+// UE8M0 scales take the tensor-core scaled kernels (MX) when the environment
+// variable FP8BLK_UE8M0_MMA is "1" at the call; otherwise the per-block
+// promotion, which computes the same numbers.
+bool mx_for(int scale_fmt) {
+  if (scale_fmt != FP8BLK_SCALE_UE8M0) return false;
+  const char* v = getenv("FP8BLK_UE8M0_MMA");
+  return v && v[0] == '1' && v[1] == 0;
+}
 // Decode linear with the act_quant fused in (M <= 16): weights-only stages.
 using CfgF16S8 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, true>;
 using CfgF16S4 = Cfg<16, true, 4, 8, 4, kEpiBf16, false, true>;
@@ -1182,12 +1382,28 @@ struct Plan {
   int tiles_lane, tiles_col;
   int grid, dp_waves, sk_tiles;
   long long sk_iters;
+  int whole_tiles;  // > 0: that many tiles, whole and round-robin (no stream-K, no counters)
 };
+
+// Arrival counters of the stream-K fixup: a fixed region at the start of
+// every GEMM workspace, so that when one workspace serves GEMMs of different
+// shapes, no plan's partial slots (which follow the region) overlap another
+// plan's counters. A plan with more tiles than counters runs whole tiles.
+constexpr size_t kCounterBytes = 64 * 1024;
+constexpr long long kMaxCounters = static_cast<long long>(kCounterBytes / sizeof(int));
 
 // Data-parallel waves while at least two full waves remain, stream-K for the rest.
 void plan_schedule(Plan& pl, int64_t Kb, int sm_count) {
   const long long tiles = static_cast<long long>(pl.tiles_lane) * pl.tiles_col;
   const int G = sm_count;
+  if (tiles * pl.cluster > kMaxCounters) {
+    pl.grid = G;
+    pl.dp_waves = 0;
+    pl.sk_tiles = 0;
+    pl.sk_iters = 0;
+    pl.whole_tiles = static_cast<int>(tiles);
+    return;
+  }
   if (tiles >= 2LL * G) {
     pl.grid = G;
     pl.dp_waves = static_cast<int>(tiles / G - 1);
@@ -1284,10 +1500,9 @@ Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count, int pai
 
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
-// Workspace: one arrival counter per output tile, then two partial slots per CTA.
-size_t plan_counter_bytes(const Plan& pl) {
-  return align256(static_cast<size_t>(pl.tiles_lane) * pl.tiles_col * pl.cluster * sizeof(int));
-}
+// Workspace: the counter region (one arrival counter per output tile), then
+// two partial slots per CTA.
+size_t plan_counter_bytes(const Plan&) { return kCounterBytes; }
 
 size_t plan_workspace(const Plan& pl) {
   return plan_counter_bytes(pl) + static_cast<size_t>(2) * pl.grid * pl.cluster * pl.bn * 128 * sizeof(float);
@@ -1460,6 +1675,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   prm.dp_waves = pl.dp_waves;
   prm.sk_tiles = pl.sk_tiles;
   prm.sk_iters = pl.sk_iters;
+  prm.whole_tiles = pl.whole_tiles;
   prm.ksplit = pl.ksplit;
   prm.vec_store = (N % 8 == 0 && is_aligned(c, 16)) ? 1 : 0;
   prm.ldc = static_cast<int>(N);
@@ -1476,8 +1692,11 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     return FP8BLK_ERR_CUDA;
 
   if (!pl.swap) {
-    if (pl.cluster == 2) return launch<CfgN256C2>(d, ml, mc, mc, prm, stream);
-    if (pl.bn == 256) return launch<CfgN256>(d, ml, mc, mc, prm, stream);
+    const bool mx = mx_for(scale_fmt);
+    if (pl.cluster == 2)
+      return mx ? launch<CfgN256C2MX>(d, ml, mc, mc, prm, stream) : launch<CfgN256C2>(d, ml, mc, mc, prm, stream);
+    if (pl.bn == 256)
+      return mx ? launch<CfgN256MX>(d, ml, mc, mc, prm, stream) : launch<CfgN256>(d, ml, mc, mc, prm, stream);
     return launch<CfgN128E8>(d, ml, mc, mc, prm, stream);
   }
   switch (pl.bn) {
@@ -1581,12 +1800,16 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
   prm.dp_waves = pl.dp_waves;
   prm.sk_tiles = pl.sk_tiles;
   prm.sk_iters = pl.sk_iters;
+  prm.whole_tiles = pl.whole_tiles;
   prm.ue8m0 = scale_fmt == FP8BLK_SCALE_UE8M0;
   CUtensorMap ml, m1, m3;
   if (!make_kmajor_map(&ml, xq, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128) ||
       !make_kmajor_map(&m1, w1, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64) ||
       !make_kmajor_map(&m3, w3, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64))
     return FP8BLK_ERR_CUDA;
+  if (mx_for(scale_fmt))
+    return pl.cluster == 2 ? launch<CfgSwiGLUC2MX>(d, ml, m1, m3, prm, stream)
+                           : launch<CfgSwiGLUMX>(d, ml, m1, m3, prm, stream);
   if (pl.cluster == 2) return launch<CfgSwiGLUC2>(d, ml, m1, m3, prm, stream);
   return launch<CfgSwiGLU>(d, ml, m1, m3, prm, stream);
 }
@@ -1621,6 +1844,7 @@ int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const f
       !make_kmajor_map(&m1, w1, static_cast<uint64_t>(E * inter), static_cast<uint64_t>(K), 64) ||
       !make_kmajor_map(&m3, w3, static_cast<uint64_t>(E * inter), static_cast<uint64_t>(K), 64))
     return FP8BLK_ERR_CUDA;
+  if (mx_for(scale_fmt)) return launch<CfgSwiGLUGroupedMX>(d, ml, m1, m3, prm, stream);
   return launch<CfgSwiGLUGrouped>(d, ml, m1, m3, prm, stream);
 }
 
@@ -1628,7 +1852,7 @@ int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const f
 // times weight rows [e*dim, (e+1)*dim) of w2 [E*dim, inter]; dim % 256 == 0.
 int grouped_scatter_run(const void* uq, const float* us, const void* w2, const float* w2s, void* out,
                         const int* perm, int64_t rows, int64_t E, int64_t dim, int64_t inter, const int* grp_rows,
-                        const int* grp_mtiles, cudaStream_t stream) {
+                        const int* grp_mtiles, int scale_fmt, cudaStream_t stream) {
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
   GemmParams prm{};
@@ -1651,6 +1875,7 @@ int grouped_scatter_run(const void* uq, const float* us, const void* w2, const f
   if (!make_kmajor_map(&ml, uq, static_cast<uint64_t>(rows), static_cast<uint64_t>(inter), 128) ||
       !make_kmajor_map(&mc, w2, static_cast<uint64_t>(E * dim), static_cast<uint64_t>(inter), 256))
     return FP8BLK_ERR_CUDA;
+  if (mx_for(scale_fmt)) return launch<CfgScatterGroupedMX>(d, ml, mc, mc, prm, stream);
   return launch<CfgScatterGrouped>(d, ml, mc, mc, prm, stream);
 }
 

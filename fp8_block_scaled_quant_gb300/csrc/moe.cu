@@ -42,7 +42,7 @@ int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const f
                        const int* grp_rows, const int* grp_mtiles, int scale_fmt, cudaStream_t stream);
 int grouped_scatter_run(const void* uq, const float* us, const void* w2, const float* w2s, void* out,
                         const int* perm, int64_t rows, int64_t E, int64_t dim, int64_t inter, const int* grp_rows,
-                        const int* grp_mtiles, cudaStream_t stream);
+                        const int* grp_mtiles, int scale_fmt, cudaStream_t stream);
 
 namespace {
 
@@ -675,7 +675,8 @@ extern "C" int fp8blk_moe_grouped_gemm(const void* x_e4m3, const float* x_s, con
   if (int st = grouped_swiglu_run(xg, xgs, w1_e4m3, w1_s, w3_e4m3, w3_s, uq, us, n, experts, inter, dim, offsets,
                                   mtiles, scale_fmt, cs))
     return st;
-  if (int st = grouped_scatter_run(uq, us, w2_e4m3, w2_s, o, perm, n, experts, dim, inter, offsets, mtiles, cs))
+  if (int st = grouped_scatter_run(uq, us, w2_e4m3, w2_s, o, perm, n, experts, dim, inter, offsets, mtiles,
+                                   scale_fmt, cs))
     return st;
   // One thread per 8-element output vector (grid-stride past 2^30 CTAs).
   const long long vecs = T * (dim / 8);

@@ -17,6 +17,7 @@ enum : unsigned {
   kDevErrTimeoutEpilogue = 1u << 2,
   kDevErrTimeoutDrain = 1u << 3,
   kDevErrBadSchedule = 1u << 4,
+  kDevErrBadScale = 1u << 7,  // a UE8M0-format scale that is not a positive normal power of two
 };
 
 // A wait on an mbarrier gives up after this long (ns of %globaltimer). Every
@@ -214,6 +215,36 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: e4m3 A and B,
+// both K-major, fp32 accumulation, UE8M0 scale factors (bit 23), and the byte
+// `sf_id` of each 32-bit scale-factor column selected for A (bits 29-30) and
+// B (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4)                              // B scale-factor byte
+         | (0u << 7) | (0u << 10)                  // A, B format: e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (1u << 23)                              // scale factors are UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)   // M / 16
+         | (sf_id << 29);                          // A scale-factor byte
+}
+
+// D[tmem] (+)= (A * 2^(sfa - 127)) (B * 2^(sfb - 127))^T for one 32-byte K
+// slice, one UE8M0 scale per operand row (scale_vec::1X). For M = 128 and
+// N <= 256 the scale of operand row r is read from TMEM lane r % 32, column
+// sf_tmem + r / 32, byte sf_id; the lane is taken in the lane quarter of the
+// accumulator row being computed (so a layout written identically into all
+// four quarters serves every row).
+__device__ __forceinline__ void mma_mx_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T for one 32-byte K slice; issued by one thread.
 __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -345,6 +376,24 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)
       : "r"(taddr)
       : "memory");
 }
+
+// ---- registers -> TMEM ---------------------------------------------------------
+// Each thread writes its own lane (the warp's 32-lane quarter), N consecutive
+// 32-bit columns. tmem_wait_st() waits until this thread's stores are done.
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id `id` (1..15).
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {

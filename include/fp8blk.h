@@ -131,11 +131,20 @@ FP8BLK_API int fp8blk_weight_dequant(const void *q_e4m3, const float *s, int64_t
  * c:   bf16 [M, N]. 16-byte alignment and N % 8 == 0 take the vector store path.
  * K must be a multiple of 128; N need not be (the last weight block is
  * partial: rows past N contribute nothing). K == 0 writes zeros.
- * scale_fmt only states the scale format (both formats use the same math).
+ * scale_fmt: FP8BLK_SCALE_FP32 or FP8BLK_SCALE_UE8M0 (same arithmetic).
+ * Under UE8M0 every a_s and w_s must be a positive normal power of two (as
+ * fp8blk_act_quant and fp8blk_weight_quant give them under UE8M0). GEMMs with
+ * M > 128 on 128 x 256 tiles (the FFN, expert and large prefill GEMMs) can
+ * then let the tensor core apply the scales itself (block-scaled MMA,
+ * one UE8M0 exponent per operand row and 32-wide K slice), and a scale that
+ * is not such a power of two sets device error bit 0x80 (its outputs are
+ * undefined). That path is taken while the environment variable
+ * FP8BLK_UE8M0_MMA is "1"; otherwise UE8M0 uses the per-block promotion.
  * workspace: device memory of at least fp8blk_gemm_workspace_bytes(M, N, K),
- * 256-byte aligned, ZERO-FILLED before its first use; every call returns it
- * to that state (its tile counters end at zero). One workspace serves one
- * stream at a time.
+ * 256-byte aligned. Its first 64 KB hold the tile counters: ZERO-FILLED
+ * before the first use, and every call leaves them at zero; the rest is
+ * scratch whose contents do not matter. One workspace serves one stream at a
+ * time, for GEMMs of any shape.
  */
 FP8BLK_API size_t fp8blk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 FP8BLK_API int fp8blk_gemm(const void *a_e4m3, const float *a_s, const void *w_e4m3, const float *w_s, void *c_bf16,

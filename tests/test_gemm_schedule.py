@@ -11,6 +11,9 @@ CTAs race on one slot."""
 import pytest
 
 
+MAX_COUNTERS = 64 * 1024 // 4   # the workspace's fixed counter region, one int32 per tile
+
+
 def make_plan(M, N, K, sms, pairs=None):
     """pairs: co-resident CTA pairs of the cluster kernel (default sms // 2;
     0 disables clusters). With pairs, large-M tiles of 128 x 256 run as
@@ -42,6 +45,9 @@ def make_plan(M, N, K, sms, pairs=None):
         cluster, workers = 2, pairs
         tl = (tl + 1) // 2
     tiles = tl * tc
+    if tiles * cluster > MAX_COUNTERS:   # more tiles than the counter region holds: whole tiles only
+        return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=workers, dp=0, sk_tiles=0, sk_iters=0, Kb=Kb,
+                    tiles=tiles, cluster=cluster, ksplit=1, whole=tiles)
     if tiles >= 2 * workers:
         grid = workers
         dp = tiles // workers - 1
@@ -61,6 +67,10 @@ def units(p, c):
         yield (c // ks, r * Kb // ks, (r + 1) * Kb // ks, 0, 1)
         return
     G, Kb, S = p["grid"], p["Kb"], p["sk_iters"]
+    if p.get("whole"):       # round-robin whole tiles (mirror of the whole_tiles branch)
+        for t in range(c, p["whole"], G):
+            yield (t, 0, Kb, 0, 1)
+        return
     for j in range(p["dp"]):
         yield (c + j * G, 0, Kb, 0, 1)
     it, it_end = c * S // G, (c + 1) * S // G
@@ -84,6 +94,7 @@ SHAPES = [
     (2048, 1536, 7168), (2048, 576, 7168), (2048, 24576, 1536), (2048, 32768, 512),
     (129, 130, 128), (300, 700, 384), (1, 1, 128), (128, 129, 2048), (33, 4000, 128),
     (5000, 100, 256),
+    (40000, 60000, 256),   # more tiles than counters: whole tiles, round-robin
 ]
 
 

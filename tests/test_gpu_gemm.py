@@ -100,6 +100,31 @@ def test_gemm_deterministic_and_workspace_restored():
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
 
 
+def test_gemm_workspace_shared_by_plans_of_different_shapes():
+    """One workspace serves GEMMs of different shapes. A small stream-K GEMM
+    (15 tiles, each cut into parts) fills its partial slots; a larger one
+    (cluster-pair tiles with a stream-K tail) then counts part arrivals in the
+    same buffer. Its output must equal, bit for bit, the output on a fresh
+    workspace, and the counters must end at zero."""
+    dev = torch.device("cuda")
+    small, big = (300, 576, 1024), (1300, 7000, 640)
+    ops = []
+    for i, (M, N, K) in enumerate((small, big)):
+        a, a_s = fb.act_quant(synthetic.device_activations(M, K, 61 + i, dev))
+        q, s = fb.weight_quant(synthetic.device_normal((N, K), 71 + i, 0.02, dev))
+        ops.append((a, a_s, q, s, fb.gemm_workspace_bytes(M, N, K)))
+    a, a_s, q, s, nb = ops[1]
+    want = fb.fp8_gemm(a, a_s, q, s, ws=torch.zeros(nb, dtype=torch.uint8, device=dev))
+    shared = torch.zeros(max(o[4] for o in ops), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        a1, a1_s, q1, s1, nb1 = ops[0]
+        fb.fp8_gemm(a1, a1_s, q1, s1, ws=shared[:nb1])
+        got = fb.fp8_gemm(a, a_s, q, s, ws=shared[:nb])
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert torch.count_nonzero(shared[:64 * 1024]) == 0
+    assert fb.last_device_error() == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(64, 576, 7168), (4096, 7168, 18432)])
 def test_gemm_split_paths_deterministic(M, N, K):
     """Split-K clusters (few weight tiles) and stream-K cluster pairs reduce
@@ -153,16 +178,17 @@ def test_gemm_unaligned_output_scalar_stores():
 
 # ---- full-size workloads, sampled ------------------------------------------------
 
-def sampled_check(M, N, K, seed, frac=0.0, n_random=48):
+def sampled_check(M, N, K, seed, frac=0.0, n_random=48, fmt=fb.SCALE_FP32):
     """Device-generated inputs at full size; the oracle recomputes sampled
     outputs from host copies of the same bf16 / fp32 inputs (quantising the
     needed rows and weight blocks itself)."""
     dev = torch.device("cuda")
+    ue = fmt == fb.SCALE_UE8M0
     x = synthetic.device_activations(M, K, seed, dev, outlier_frac=frac)
     w = synthetic.device_normal((N, K), seed + 1, 0.02, dev)
-    a, a_s = fb.act_quant(x)
-    q, s = fb.weight_quant(w)
-    c = fb.fp8_gemm(a, a_s, q, s)
+    a, a_s = fb.act_quant(x, fmt)
+    q, s = fb.weight_quant(w, fmt)
+    c = fb.fp8_gemm(a, a_s, q, s, scale_fmt=fmt)
     g = np.random.Generator(np.random.PCG64(seed))
     ms = np.concatenate([[0, M - 1, min(127, M - 1), min(128, M - 1)], g.integers(0, M, n_random)])
     ns = np.concatenate([[0, N - 1, min(127, N - 1), min(255, N - 1)], g.integers(0, N, n_random)])
@@ -170,12 +196,12 @@ def sampled_check(M, N, K, seed, frac=0.0, n_random=48):
     ms, ns = ms.ravel(), ns.ravel()
     rows = np.unique(ms)
     xb = dev_to_bits(x[torch.from_numpy(rows).to(dev)])
-    xq, xs = oracle.act_quant(xb)
+    xq, xs = oracle.act_quant(xb, ue)
     assert np.array_equal(dev_to_bits(a[torch.from_numpy(rows).to(dev)]), xq)
     blocks = np.unique(ns // 128)
     wq_parts, ws_parts = [], []
     for b in blocks:
-        qo, so = oracle.weight_quant(w[b * 128:(b + 1) * 128].cpu().numpy())
+        qo, so = oracle.weight_quant(w[b * 128:(b + 1) * 128].cpu().numpy(), ue)
         assert np.array_equal(dev_to_bits(q[b * 128:(b + 1) * 128]), qo)
         wq_parts.append(np.pad(qo, ((0, 128 - qo.shape[0]), (0, 0))))
         ws_parts.append(so)
@@ -197,6 +223,31 @@ def sampled_check(M, N, K, seed, frac=0.0, n_random=48):
                                    (64, 24576, 1536), (64, 32768, 512), (64, 576, 7168)])
 def test_gemm_full_size_sampled(M, N, K):
     sampled_check(M, N, K, 4000 + M % 97 + N % 89, frac=0.01)
+
+
+@pytest.mark.parametrize("M,N,K", [(1300, 7000, 640), (4096, 18432, 7168), (4096, 7168, 18432)])
+def test_gemm_ue8m0_tensor_core_scaling_sampled(M, N, K, monkeypatch):
+    """Power-of-two scales on 128 x 256 tiles: the tensor core applies the
+    UE8M0 scales itself (block-scaled MMA, one accumulator over the whole K
+    range). 1300 x 7000 x 640: cluster pairs, a ragged row tile, a partial
+    weight block, stream-K parts, 5 K blocks (a scale group of 4 and one of
+    1); 7168 and 18432: 14 and 36 scale groups through the 8-slot ring."""
+    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
+    sampled_check(M, N, K, 5000 + M % 97 + N % 89, frac=0.01, fmt=fb.SCALE_UE8M0)
+    assert fb.last_device_error() == 0
+
+
+def test_gemm_ue8m0_flags_scales_that_are_not_powers_of_two(monkeypatch):
+    """Under UE8M0 the tensor core takes only the exponent of each scale: fp32
+    weight scales that are not powers of two set the device error bit 1 << 7."""
+    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
+    dev = torch.device("cuda")
+    a, a_s = fb.act_quant(synthetic.device_activations(1300, 640, 91, dev), fb.SCALE_UE8M0)
+    q, s = fb.weight_quant(synthetic.device_normal((7000, 640), 92, 0.02, dev))
+    assert fb.last_device_error() == 0
+    fb.fp8_gemm(a, a_s, q, s, scale_fmt=fb.SCALE_UE8M0)
+    assert fb.last_device_error() & (1 << 7)
+    assert fb.last_device_error() == 0
 
 
 def test_linear_matches_quant_then_gemm():

@@ -65,8 +65,12 @@ def oracle_u(xq, xs, w1q, w1s, w3q, w3s, ue8m0=False):
 
 
 @pytest.mark.parametrize("M,dim,inter", [(5, 256, 384), (130, 512, 256), (300, 256, 1024)])
-@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0])
-def test_swiglu_gemm_matches_oracle_chain(M, dim, inter, fmt):
+@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-mma"])
+def test_swiglu_gemm_matches_oracle_chain(M, dim, inter, fmt, monkeypatch):
+    """ue8m0-mma: UE8M0 scales applied by the tensor core (block-scaled MMA)."""
+    if fmt == "ue8m0-mma":
+        monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
+        fmt = fb.SCALE_UE8M0
     ue = fmt == fb.SCALE_UE8M0
     x = synthetic.activations(M, dim, 600 + M)
     xq, xs = oracle.act_quant(x, ue)
@@ -176,8 +180,12 @@ def run_moe(p, E, fmt=fb.SCALE_FP32):
 
 @pytest.mark.parametrize("T,E,dim,inter,k,zipf", [(64, 8, 256, 256, 2, 0.0), (96, 16, 512, 384, 4, 1.2),
                                                   (33, 5, 256, 128, 3, 0.0), (300, 4, 256, 256, 1, 0.0)])
-@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0])
-def test_moe_full_compare(T, E, dim, inter, k, zipf, fmt):
+@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-mma"])
+def test_moe_full_compare(T, E, dim, inter, k, zipf, fmt, monkeypatch):
+    """ue8m0-mma: both grouped GEMMs with UE8M0 scales applied by the tensor core."""
+    if fmt == "ue8m0-mma":
+        monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
+        fmt = fb.SCALE_UE8M0
     p = moe_problem(T, E, dim, inter, k, 800 + T + E, zipf, fmt == fb.SCALE_UE8M0)
     y = run_moe(p, E, fmt)
     ref, allow = moe_reference(p, range(T), E, ue8m0=fmt == fb.SCALE_UE8M0)
