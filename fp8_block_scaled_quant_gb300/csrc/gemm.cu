@@ -251,8 +251,10 @@ struct Cfg {
   // while the previous kernel finishes.
   static constexpr int kL2Ahead = SWAP ? FP8BLK_DECODE_L2_AHEAD : 0;
   static constexpr int kTmemCols = pow2_at_least(P * BN + 16 * kSfSlots, 32);
-  static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16 + 2 * kSfSlots * 8;
-  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + kGroupBytes + kXchgBytes;
+  static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16 + (2 * kSfSlots + (MX ? 1 : 0)) * 8;
+  // MX: the scale writers' exchange of activation-row scale words, double-buffered.
+  static constexpr int kSfxBytes = MX ? 2 * 128 * 4 : 0;
+  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + kGroupBytes + kXchgBytes + kSfxBytes;
 
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(MODE == kEpiBf16 || !SWAP, "SwiGLU and scatter epilogues use activation rows as lanes");
@@ -490,6 +492,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   // sf_empty (the MMAs that read a slot have completed).
   uint64_t* sf_full = reinterpret_cast<uint64_t*>(tail + (2 * C::STAGES + 2 * C::P + 3) * 8 + 16);
   uint64_t* sf_empty = sf_full + C::kSfSlots;
+  uint64_t* wr_bar = sf_empty + C::kSfSlots;  // the four scale writers, once per scale group
+  uint32_t* sfx = reinterpret_cast<uint32_t*>(tail + C::kBarBytes + C::kGroupBytes + C::kXchgBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Cluster rank, and the index of the schedule this CTA (pair) walks.
@@ -519,6 +523,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&sf_full[q], 4);
       mbar_init(&sf_empty[q], 1);
     }
+    if constexpr (C::MX) mbar_init(wr_bar, 4);
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -831,65 +836,100 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // i holds operand row 32 i + l (columns 0-3 activation rows, 4-11 the
       // 256 weight rows, one weight block per 128 rows). K blocks past the
       // unit and rows past the matrix get 127 (a scale of 1).
+      // Thread (quarter q, lane l) loads the scales of activation row 32 q + l
+      // (one group ahead, so the loads overlap the previous group's stores);
+      // the four warps exchange the packed row words through shared memory.
+      // Lanes 0-7 load the tile's weight-block scales (block l / 4, K block
+      // l % 4), packed by shuffles.
       const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;
       const uint32_t t_sf = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(C::kSfCol0);
       griddep_wait();  // the activation scales come from the previous kernel
       bool bad = false;
-      auto pack = [&](const float* src, int nk) -> uint32_t {
-        uint32_t w = 0x7F7F7F7Fu;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (j < nk) {
-            const uint32_t b = __float_as_uint(__ldg(src + j));
-            const uint32_t e = b >> 23;  // sign bit set: e >= 256
-            bad |= (b & 0x007FFFFFu) != 0u || e == 0u || e >= 255u;
-            w = (w & ~(0xFFu << (8 * j))) | ((e & 0xFFu) << (8 * j));
-          }
-        }
-        return w;
+      auto ue8m0 = [&](float v) -> uint32_t {
+        const uint32_t b = __float_as_uint(v);
+        const uint32_t e = b >> 23;  // sign bit set: e >= 256
+        bad |= (b & 0x007FFFFFu) != 0u || e == 0u || e >= 255u;
+        return e & 0xFFu;
       };
       Sched sch(prm, worker, grouped_tiles, krank);
       Unit u;
-      int sfs = 0;
-      uint32_t sfph = 0;
+      TileInfo t{};
+      bool have = sch.next(u);
+      if (have) t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
+      int k0 = have ? u.kb0 : 0;
+      float ra[4], rw = 1.0f;
+      auto fetch = [&]() {
+        const int nk = u.kb1 - k0 < 4 ? u.kb1 - k0 : 4;
+        const float* src = prm.a_s + static_cast<size_t>(t.lane_y + row) * prm.Kb + k0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ra[j] = (row < t.lane_valid && j < nk) ? __ldg(src + j) : 1.0f;
+        rw = 1.0f;
+        if (lane < 8) {
+          const int jb = lane & 3, blk = lane >> 2;
+          // SwiGLU tiles: rows [0,64) w1, [64,128) w3, [128,192) w1, [192,256) w3, one block of each.
+          const float* ws = (C::MODE == kEpiSwiGLU && blk) ? prm.w3_s : prm.w_s;
+          const int nb = C::MODE == kEpiSwiGLU ? t.wblock : t.wblock + blk;
+          if (jb < nk && (C::GROUPED || C::MODE == kEpiSwiGLU || nb < prm.n_wblocks))
+            rw = __ldg(ws + static_cast<size_t>(nb) * prm.Kb + k0 + jb);
+        }
+      };
+      if (have) fetch();
+      int sfs = 0, xb = 0;
+      uint32_t sfph = 0, xph = 0;
       bool ok = true;
-      while (ok && sch.next(u)) {
-        const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
-        for (int k0 = u.kb0; k0 < u.kb1; k0 += 4) {
-          const int nk = u.kb1 - k0 < 4 ? u.kb1 - k0 : 4;
-          uint32_t wa[4], wb[8];
+      while (ok && have) {
+        uint32_t wrow = 0;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = 32 * i + lane;
-            wa[i] = r < t.lane_valid ? pack(prm.a_s + static_cast<size_t>(t.lane_y + r) * prm.Kb + k0, nk)
-                                     : 0x7F7F7F7Fu;
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            // SwiGLU tiles: rows [0,64) w1, [64,128) w3, [128,192) w1, [192,256) w3, one block of each.
-            const float* ws = (C::MODE == kEpiSwiGLU && (i & 2)) ? prm.w3_s : prm.w_s;
-            const int nb = C::MODE == kEpiSwiGLU ? t.wblock : t.wblock + (i >> 2);
-            wb[i] = (C::GROUPED || C::MODE == kEpiSwiGLU || nb < prm.n_wblocks)
-                        ? pack(ws + static_cast<size_t>(nb) * prm.Kb + k0, nk)
-                        : 0x7F7F7F7Fu;
-          }
-          if (!__all_sync(0xFFFFFFFFu,
-                          mbar_wait(&sf_empty[sfs], sfph ^ 1u, abort_flag, prm.err, kDevErrTimeoutEpilogue))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          tmem_st_32x32b_x4(t_sf + static_cast<uint32_t>(sfs * 16), wa);
-          tmem_st_32x32b_x8(t_sf + static_cast<uint32_t>(sfs * 16 + 4), wb);
-          tmem_wait_st();
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sf_full[sfs]);
-          if (++sfs == C::kSfSlots) {
-            sfs = 0;
-            sfph ^= 1u;
+        for (int j = 0; j < 4; ++j) wrow |= ue8m0(ra[j]) << (8 * j);
+        const uint32_t wbyte = ue8m0(rw);
+        // Advance to the next group and start its loads.
+        k0 += 4;
+        if (k0 >= u.kb1) {
+          have = sch.next(u);
+          if (have) {
+            t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
+            k0 = u.kb0;
           }
         }
+        if (have) fetch();
+        // Exchange the row words (bounded mbarrier over the four warps).
+        sfx[xb * 128 + row] = wrow;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(wr_bar);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(wr_bar, xph, abort_flag, prm.err, kDevErrTimeoutEpilogue))) {
+          ok = false;
+          break;
+        }
+        xph ^= 1u;
+        uint32_t wa[4], wb[8], blkw[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wa[i] = sfx[xb * 128 + 32 * i + lane];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          blkw[b] = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) blkw[b] |= __shfl_sync(0xFFFFFFFFu, wbyte, 4 * b + j) << (8 * j);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wb[i] = blkw[C::MODE == kEpiSwiGLU ? ((i >> 1) & 1) : (i >> 2)];
+        if (!__all_sync(0xFFFFFFFFu,
+                        mbar_wait(&sf_empty[sfs], sfph ^ 1u, abort_flag, prm.err, kDevErrTimeoutEpilogue))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        tmem_st_32x32b_x4(t_sf + static_cast<uint32_t>(sfs * 16), wa);
+        tmem_st_32x32b_x8(t_sf + static_cast<uint32_t>(sfs * 16 + 4), wb);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[sfs]);
+        if (++sfs == C::kSfSlots) {
+          sfs = 0;
+          sfph ^= 1u;
+        }
+        xb ^= 1;
       }
       if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(prm.err, kDevErrBadScale);
     }
@@ -1361,13 +1401,13 @@ using CfgSwiGLUC2MX = Cfg<256, false, 4, 1, 8, kEpiSwiGLU, false, false, 2, true
 using CfgSwiGLUGroupedMX = Cfg<256, false, 4, 1, 8, kEpiSwiGLU, true, false, 1, true>;
 using CfgScatterGroupedMX = Cfg<256, false, 4, 1, 8, kEpiScatter, true, false, 1, true>;
 
-// UE8M0 scales take the tensor-core scaled kernels (MX) when the environment
-// variable FP8BLK_UE8M0_MMA is "1" at the call; otherwise the per-block
-// promotion, which computes the same numbers.
+// UE8M0 scales take the tensor-core scaled kernels (MX) unless the
+// environment variable FP8BLK_UE8M0_MMA is "0" at the call; that keeps the
+// per-block promotion, which computes the same numbers.
 bool mx_for(int scale_fmt) {
   if (scale_fmt != FP8BLK_SCALE_UE8M0) return false;
   const char* v = getenv("FP8BLK_UE8M0_MMA");
-  return v && v[0] == '1' && v[1] == 0;
+  return !(v && v[0] == '0' && v[1] == 0);
 }
 // Decode linear with the act_quant fused in (M <= 16): weights-only stages.
 using CfgF16S8 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, true>;

@@ -134,12 +134,12 @@ FP8BLK_API int fp8blk_weight_dequant(const void *q_e4m3, const float *s, int64_t
  * scale_fmt: FP8BLK_SCALE_FP32 or FP8BLK_SCALE_UE8M0 (same arithmetic).
  * Under UE8M0 every a_s and w_s must be a positive normal power of two (as
  * fp8blk_act_quant and fp8blk_weight_quant give them under UE8M0). GEMMs with
- * M > 128 on 128 x 256 tiles (the FFN, expert and large prefill GEMMs) can
- * then let the tensor core apply the scales itself (block-scaled MMA,
+ * M > 128 on 128 x 256 tiles (the FFN, expert and large prefill GEMMs) then
+ * let the tensor core apply the scales itself (block-scaled MMA,
  * one UE8M0 exponent per operand row and 32-wide K slice), and a scale that
  * is not such a power of two sets device error bit 0x80 (its outputs are
- * undefined). That path is taken while the environment variable
- * FP8BLK_UE8M0_MMA is "1"; otherwise UE8M0 uses the per-block promotion.
+ * undefined). Setting the environment variable FP8BLK_UE8M0_MMA to "0"
+ * keeps the per-block promotion for UE8M0 as well.
  * workspace: device memory of at least fp8blk_gemm_workspace_bytes(M, N, K),
  * 256-byte aligned. Its first 64 KB hold the tile counters: ZERO-FILLED
  * before the first use, and every call leaves them at zero; the rest is

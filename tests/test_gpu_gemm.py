@@ -225,14 +225,16 @@ def test_gemm_full_size_sampled(M, N, K):
     sampled_check(M, N, K, 4000 + M % 97 + N % 89, frac=0.01)
 
 
+@pytest.mark.parametrize("mma", ["1", "0"])
 @pytest.mark.parametrize("M,N,K", [(1300, 7000, 640), (4096, 18432, 7168), (4096, 7168, 18432)])
-def test_gemm_ue8m0_tensor_core_scaling_sampled(M, N, K, monkeypatch):
+def test_gemm_ue8m0_tensor_core_scaling_sampled(M, N, K, mma, monkeypatch):
     """Power-of-two scales on 128 x 256 tiles: the tensor core applies the
     UE8M0 scales itself (block-scaled MMA, one accumulator over the whole K
     range). 1300 x 7000 x 640: cluster pairs, a ragged row tile, a partial
     weight block, stream-K parts, 5 K blocks (a scale group of 4 and one of
-    1); 7168 and 18432: 14 and 36 scale groups through the 8-slot ring."""
-    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
+    1); 7168 and 18432: 14 and 36 scale groups through the 8-slot ring.
+    mma "0": the same problems through the per-block promotion."""
+    monkeypatch.setenv("FP8BLK_UE8M0_MMA", mma)
     sampled_check(M, N, K, 5000 + M % 97 + N % 89, frac=0.01, fmt=fb.SCALE_UE8M0)
     assert fb.last_device_error() == 0
 

@@ -65,11 +65,12 @@ def oracle_u(xq, xs, w1q, w1s, w3q, w3s, ue8m0=False):
 
 
 @pytest.mark.parametrize("M,dim,inter", [(5, 256, 384), (130, 512, 256), (300, 256, 1024)])
-@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-mma"])
+@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-promotion"])
 def test_swiglu_gemm_matches_oracle_chain(M, dim, inter, fmt, monkeypatch):
-    """ue8m0-mma: UE8M0 scales applied by the tensor core (block-scaled MMA)."""
-    if fmt == "ue8m0-mma":
-        monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
+    """UE8M0 scales are applied by the tensor core (block-scaled MMA);
+    ue8m0-promotion: the same scales through the per-block promotion."""
+    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "0" if fmt == "ue8m0-promotion" else "1")
+    if fmt == "ue8m0-promotion":
         fmt = fb.SCALE_UE8M0
     ue = fmt == fb.SCALE_UE8M0
     x = synthetic.activations(M, dim, 600 + M)
@@ -180,11 +181,12 @@ def run_moe(p, E, fmt=fb.SCALE_FP32):
 
 @pytest.mark.parametrize("T,E,dim,inter,k,zipf", [(64, 8, 256, 256, 2, 0.0), (96, 16, 512, 384, 4, 1.2),
                                                   (33, 5, 256, 128, 3, 0.0), (300, 4, 256, 256, 1, 0.0)])
-@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-mma"])
+@pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-promotion"])
 def test_moe_full_compare(T, E, dim, inter, k, zipf, fmt, monkeypatch):
-    """ue8m0-mma: both grouped GEMMs with UE8M0 scales applied by the tensor core."""
-    if fmt == "ue8m0-mma":
-        monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
+    """UE8M0: both grouped GEMMs with the scales applied by the tensor core;
+    ue8m0-promotion: the same scales through the per-block promotion."""
+    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "0" if fmt == "ue8m0-promotion" else "1")
+    if fmt == "ue8m0-promotion":
         fmt = fb.SCALE_UE8M0
     p = moe_problem(T, E, dim, inter, k, 800 + T + E, zipf, fmt == fb.SCALE_UE8M0)
     y = run_moe(p, E, fmt)
