@@ -230,15 +230,29 @@ def barrier():
 _COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
 
 
-def kernel_source_digest() -> str:
-    """Digest of the kernel sources' code: comments and whitespace removed, so
-    an edit to a comment keeps a profile's traffic record valid and any change
-    to the code invalidates it. (A string literal holding "//" would lose its
-    tail here; the sources have none that matters to the digest.)"""
+# The library sources whose code makes up each recorded kernel: the kernel,
+# the device helpers it includes and the host code that plans its launch.
+# None: every source (a workload of several kernels).
+KERNEL_SOURCES = {
+    "fp8_gemm": ("gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
+    "swiglu_gemm": ("gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
+    "linear_fused": ("api.cu", "gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
+    "weight_dequant": ("quant.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
+    "moe_step": None,
+}
+
+
+def kernel_source_digest(kernel: str | None = None) -> str:
+    """Digest of the code of the sources that make up `kernel` (all sources if
+    None): comments and whitespace removed, so an edit to a comment keeps a
+    profile's traffic record valid and any change to that code invalidates it.
+    (A string literal holding "//" would lose its tail here; the sources have
+    none that matters to the digest.)"""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_quant_gb300", "csrc")
+    files = KERNEL_SOURCES.get(kernel) if kernel else None
     for name in sorted(os.listdir(csrc)):
-        if not name.endswith((".cu", ".cuh", ".h")):
+        if not name.endswith((".cu", ".cuh", ".h")) or (files is not None and name not in files):
             continue
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             code = "".join(_COMMENT.sub(" ", f.read()).split())
@@ -248,11 +262,11 @@ def kernel_source_digest() -> str:
 
 def recorded_traffic(workload: str, kernel: str):
     """dram bytes per launch recorded in profiles/*.md by an ncu capture of this
-    workload, if the kernel sources are unchanged since (else None)."""
+    workload, if the kernel's sources are unchanged since (else None)."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(kernel)
     for name in sorted(os.listdir(pdir)):
         if not name.endswith(".md"):
             continue

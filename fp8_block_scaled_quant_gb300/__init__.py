@@ -287,6 +287,11 @@ def swiglu_gemm(x: torch.Tensor, x_s: torch.Tensor, w1: torch.Tensor, w1_s: torc
     return u, us
 
 
+def ffn_workspace_bytes(M: int, dim: int, inter: int) -> int:
+    i64 = ctypes.c_int64
+    return int(_set_types("fp8blk_ffn_workspace_bytes", [i64, i64, i64], ctypes.c_size_t)(M, dim, inter))
+
+
 def ffn(x: torch.Tensor, w1, w1_s, w3, w3_s, w2, w2_s, scale_fmt: int = SCALE_FP32,
         out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
     """Dense SwiGLU FFN with FP8 Linears: x bf16 [M, dim] -> bf16 [M, dim]."""
@@ -294,7 +299,7 @@ def ffn(x: torch.Tensor, w1, w1_s, w3, w3_s, w2, w2_s, scale_fmt: int = SCALE_FP
     M, dim = x.shape
     inter = w1.shape[0]
     vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
-    nb = _set_types("fp8blk_ffn_workspace_bytes", [i64, i64, i64], sz)(M, dim, inter)
+    nb = ffn_workspace_bytes(M, dim, inter)
     if ws is None:
         ws = workspace(nb, x.device, "ffn")
     if out is None:

@@ -112,12 +112,14 @@ extern "C" int fp8blk_last_device_error(fp8blk_stream_t stream, unsigned* bits) 
   return v ? FP8BLK_ERR_TIMEOUT : FP8BLK_OK;
 }
 
-// Workspace of the linear layer: [x_q e4m3 M*K][x_s fp32 M*K/128][GEMM workspace],
-// each part 256-byte aligned.
+// Workspace of the linear layer: [GEMM workspace][x_q e4m3 M*K][x_s fp32 M*K/128],
+// each part 256-byte aligned. The GEMM workspace comes first so that its tile
+// counters sit at the same offset whatever the shape: one workspace can serve
+// layers of different shapes.
 extern "C" size_t fp8blk_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return 0;
-  return align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / kBlock) * 4) +
-         gemm_workspace_bytes(M, N, K);
+  return align256(gemm_workspace_bytes(M, N, K)) + align256(static_cast<size_t>(M) * K) +
+         align256(static_cast<size_t>(M) * (K / kBlock) * 4);
 }
 
 extern "C" int fp8blk_linear(const void* x_bf16, const void* w_e4m3, const float* w_s, void* y_bf16, int64_t M,
@@ -138,21 +140,22 @@ extern "C" int fp8blk_linear(const void* x_bf16, const void* w_e4m3, const float
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   const size_t need = fp8blk_linear_workspace_bytes(M, N, K);
   if (workspace_bytes < need) return FP8BLK_ERR_WORKSPACE;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint8_t* xq = ws;
-  float* xs = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(M) * K));
-  uint8_t* gws = ws + align256(static_cast<size_t>(M) * K) + align256(static_cast<size_t>(M) * (K / kBlock) * 4);
+  uint8_t* gws = static_cast<uint8_t*>(workspace);
+  const size_t gbytes = align256(gemm_workspace_bytes(M, N, K));
+  uint8_t* xq = gws + gbytes;
+  float* xs = reinterpret_cast<float*>(xq + align256(static_cast<size_t>(M) * K));
   if (int st = act_quant_launch(x_bf16, M, K, xq, xs, scale_fmt, reinterpret_cast<cudaStream_t>(stream), true))
     return st;
-  return gemm_run(xq, xs, w_e4m3, w_s, y_bf16, M, N, K, scale_fmt, gws, workspace_bytes - (gws - ws),
+  return gemm_run(xq, xs, w_e4m3, w_s, y_bf16, M, N, K, scale_fmt, gws, gbytes,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
-// Host variant: [x bf16 M*K][y bf16 M*N][linear workspace].
+// Host variant: [linear workspace][x bf16 M*K][y bf16 M*N] (the linear
+// workspace first, for the same reason).
 extern "C" size_t fp8blk_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return 0;
-  return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * N * 2) +
-         fp8blk_linear_workspace_bytes(M, N, K);
+  return align256(fp8blk_linear_workspace_bytes(M, N, K)) + align256(static_cast<size_t>(M) * K * 2) +
+         align256(static_cast<size_t>(M) * N * 2);
 }
 
 extern "C" int fp8blk_linear_host(const void* x_host, const void* w_e4m3, const float* w_s, void* y_host,
@@ -165,11 +168,11 @@ extern "C" int fp8blk_linear_host(const void* x_host, const void* w_e4m3, const 
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   if (workspace_bytes < fp8blk_linear_host_workspace_bytes(M, N, K)) return FP8BLK_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* lws = static_cast<uint8_t*>(workspace);
+  const size_t lbytes = align256(fp8blk_linear_workspace_bytes(M, N, K));
   const size_t xb = static_cast<size_t>(M) * K * 2, yb = static_cast<size_t>(M) * N * 2;
-  uint8_t* xd = ws;
-  uint8_t* yd = ws + align256(xb);
-  uint8_t* lws = yd + align256(yb);
+  uint8_t* xd = lws + lbytes;
+  uint8_t* yd = xd + align256(xb);
   // Pinned host buffers the device can address (every page-locked allocation
   // on a unified-address system such as a Grace + GB300 node): the layer reads
   // x from and writes y to them directly over the chip-to-chip link, with no
@@ -178,10 +181,10 @@ extern "C" int fp8blk_linear_host(const void* x_host, const void* w_e4m3, const 
   void* ym = nullptr;
   if (cudaHostGetDevicePointer(&xm, const_cast<void*>(x_host), 0) == cudaSuccess &&
       cudaHostGetDevicePointer(&ym, y_host, 0) == cudaSuccess && is_aligned(xm, 16) && is_aligned(ym, 16))
-    return fp8blk_linear(xm, w_e4m3, w_s, ym, M, N, K, scale_fmt, lws, workspace_bytes - (lws - ws), stream);
+    return fp8blk_linear(xm, w_e4m3, w_s, ym, M, N, K, scale_fmt, lws, lbytes, stream);
   cudaGetLastError();  // an unregistered buffer is not an error here: copy it instead
   if (K > 0 && cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
-  if (int st = fp8blk_linear(xd, w_e4m3, w_s, yd, M, N, K, scale_fmt, lws, workspace_bytes - (lws - ws), stream))
+  if (int st = fp8blk_linear(xd, w_e4m3, w_s, yd, M, N, K, scale_fmt, lws, lbytes, stream))
     return st;
   if (cudaMemcpyAsync(y_host, yd, yb, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
   return FP8BLK_OK;

@@ -527,15 +527,22 @@ extern "C" int fp8blk_swiglu_gemm(const void* x_e4m3, const float* x_s, const vo
                     workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
-// FFN workspace: [x_q M*dim][x_s M*dim/128][u_q M*inter][u_s M*inter/128]
-// [w1/w3 GEMM workspace][w2 GEMM workspace]. The two GEMM workspaces are
-// separate: each keeps its tile counters at zero between calls, and neither
-// may write partial sums where the other keeps its counters.
+// FFN workspace: [GEMM workspace][x_q M*dim][x_s M*dim/128][u_q M*inter]
+// [u_s M*inter/128]. The w1/w3 GEMM and the w2 GEMM share the GEMM workspace,
+// which comes first so that its tile counters sit at the same offset whatever
+// the shape. Sharing is safe: each GEMM touches the workspace only after its
+// dependency wait, so the w2 GEMM starts on it once the w1/w3 GEMM has
+// completed and left its counters at zero.
+static size_t ffn_gemm_bytes(int64_t M, int64_t dim, int64_t inter) {
+  const size_t a = swiglu_workspace_bytes(M, inter, dim), b = gemm_workspace_bytes(M, dim, inter);
+  return align256(a > b ? a : b);
+}
+
 extern "C" size_t fp8blk_ffn_workspace_bytes(int64_t M, int64_t dim, int64_t inter) {
   if (M < 0 || dim < 0 || inter < 0) return 0;
-  return align256(static_cast<size_t>(M) * dim) + align256(static_cast<size_t>(M) * (dim / kBlock) * 4) +
-         align256(static_cast<size_t>(M) * inter) + align256(static_cast<size_t>(M) * (inter / kBlock) * 4) +
-         align256(swiglu_workspace_bytes(M, inter, dim)) + gemm_workspace_bytes(M, dim, inter);
+  return ffn_gemm_bytes(M, dim, inter) + align256(static_cast<size_t>(M) * dim) +
+         align256(static_cast<size_t>(M) * (dim / kBlock) * 4) + align256(static_cast<size_t>(M) * inter) +
+         align256(static_cast<size_t>(M) * (inter / kBlock) * 4);
 }
 
 extern "C" int fp8blk_ffn(const void* x_bf16, const void* w1_e4m3, const float* w1_s, const void* w3_e4m3,
@@ -548,7 +555,9 @@ extern "C" int fp8blk_ffn(const void* x_bf16, const void* w1_e4m3, const float* 
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   if (workspace_bytes < fp8blk_ffn_workspace_bytes(M, dim, inter)) return FP8BLK_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* p = static_cast<uint8_t*>(workspace);
+  uint8_t* gws = static_cast<uint8_t*>(workspace);
+  const size_t gbytes = ffn_gemm_bytes(M, dim, inter);
+  uint8_t* p = gws + gbytes;
   uint8_t* xq = p;
   p += align256(static_cast<size_t>(M) * dim);
   float* xs = reinterpret_cast<float*>(p);
@@ -556,14 +565,10 @@ extern "C" int fp8blk_ffn(const void* x_bf16, const void* w1_e4m3, const float* 
   uint8_t* uq = p;
   p += align256(static_cast<size_t>(M) * inter);
   float* us = reinterpret_cast<float*>(p);
-  p += align256(static_cast<size_t>(M) * (inter / kBlock) * 4);
-  const size_t g1 = align256(swiglu_workspace_bytes(M, inter, dim));
-  uint8_t* g2p = p + g1;
-  const size_t rest = workspace_bytes - (g2p - static_cast<uint8_t*>(workspace));
   if (int st = act_quant_launch(x_bf16, M, dim, xq, xs, scale_fmt, cs, true)) return st;
-  if (int st = swiglu_run(xq, xs, w1_e4m3, w1_s, w3_e4m3, w3_s, uq, us, M, inter, dim, scale_fmt, p, g1, cs))
+  if (int st = swiglu_run(xq, xs, w1_e4m3, w1_s, w3_e4m3, w3_s, uq, us, M, inter, dim, scale_fmt, gws, gbytes, cs))
     return st;
-  return gemm_run(uq, us, w2_e4m3, w2_s, y_bf16, M, dim, inter, scale_fmt, g2p, rest, cs);
+  return gemm_run(uq, us, w2_e4m3, w2_s, y_bf16, M, dim, inter, scale_fmt, gws, gbytes, cs);
 }
 
 namespace {

@@ -156,8 +156,9 @@ FP8BLK_API int fp8blk_gemm(const void *a_e4m3, const float *a_s, const void *w_e
  * "fp8" branch of linear()): y = fp8_gemm(act_quant(x), w) with x bf16 [M, K],
  * w e4m3 [N, K] with scales w_s [ceil(N/128), K/128], y bf16 [M, N].
  * The quantised activation lives in the workspace:
- *     fp8blk_linear_workspace_bytes(M, N, K) bytes, 256-byte aligned, zero-filled
- * before first use (as for fp8blk_gemm).
+ *     fp8blk_linear_workspace_bytes(M, N, K) bytes, 256-byte aligned, its first
+ * 64 KB zero-filled before first use (as for fp8blk_gemm); one workspace
+ * serves layers of any shape, one stream at a time.
  */
 FP8BLK_API size_t fp8blk_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 FP8BLK_API int fp8blk_linear(const void *x_bf16, const void *w_e4m3, const float *w_s, void *y_bf16, int64_t M, int64_t N,
@@ -189,8 +190,8 @@ FP8BLK_API int fp8blk_linear_host(const void *x_host_bf16, const void *w_e4m3, c
  * [inter/128, dim/128]; u_q: e4m3 [M, inter] (16-byte aligned); u_s: fp32
  * [M, inter/128]. dim % 128 == 0, inter % 128 == 0. The act_quant of u happens
  * in the GEMM's epilogue (u never reaches memory in bf16).
- * Workspace: fp8blk_swiglu_workspace_bytes(M, inter, dim), zero-filled before
- * first use, left zero-filled.
+ * Workspace: fp8blk_swiglu_workspace_bytes(M, inter, dim), laid out and kept
+ * as fp8blk_gemm's (first 64 KB zero-filled before first use, left so).
  */
 FP8BLK_API size_t fp8blk_swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t dim);
 FP8BLK_API int fp8blk_swiglu_gemm(const void *x_e4m3, const float *x_s, const void *w1_e4m3, const float *w1_s,
@@ -202,7 +203,8 @@ FP8BLK_API int fp8blk_swiglu_gemm(const void *x_e4m3, const float *x_s, const vo
  * Dense SwiGLU FFN (the guide's MLP with FP8 Linears): y = w2(u) with
  * u from fp8blk_swiglu_gemm on act_quant(x). x: bf16 [M, dim]; w2: e4m3
  * [dim, inter] + scales [dim/128, inter/128]; y: bf16 [M, dim].
- * Workspace: fp8blk_ffn_workspace_bytes(M, dim, inter), zero-filled before first use.
+ * Workspace: fp8blk_ffn_workspace_bytes(M, dim, inter), first 64 KB zero-filled
+ * before first use (left so); one workspace serves FFNs of any shape.
  */
 FP8BLK_API size_t fp8blk_ffn_workspace_bytes(int64_t M, int64_t dim, int64_t inter);
 FP8BLK_API int fp8blk_ffn(const void *x_bf16, const void *w1_e4m3, const float *w1_s, const void *w3_e4m3,

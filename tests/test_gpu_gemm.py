@@ -125,6 +125,28 @@ def test_gemm_workspace_shared_by_plans_of_different_shapes():
     assert fb.last_device_error() == 0
 
 
+def test_linear_workspace_shared_by_layers_of_different_shapes():
+    """The linear layer's workspace keeps the GEMM's tile counters at offset 0
+    whatever the shape, so one workspace serves layers of different shapes
+    (a small stream-K layer, then a larger one): bit-equal to fresh workspaces."""
+    dev = torch.device("cuda")
+    shapes = [(300, 576, 1024), (1300, 7000, 640)]
+    layers = []
+    for i, (M, N, K) in enumerate(shapes):
+        x = synthetic.device_activations(M, K, 81 + i, dev)
+        q, s = fb.weight_quant(synthetic.device_normal((N, K), 91 + i, 0.02, dev))
+        nb = fb.linear_workspace_bytes(M, N, K)
+        want = fb.linear(x, q, s, ws=torch.zeros(nb, dtype=torch.uint8, device=dev))
+        layers.append((x, q, s, nb, want))
+    shared = torch.zeros(max(l[3] for l in layers), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        for x, q, s, nb, want in layers:
+            got = fb.linear(x, q, s, ws=shared[:nb])
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert torch.count_nonzero(shared[:64 * 1024]) == 0
+    assert fb.last_device_error() == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(64, 576, 7168), (4096, 7168, 18432)])
 def test_gemm_split_paths_deterministic(M, N, K):
     """Split-K clusters (few weight tiles) and stream-K cluster pairs reduce

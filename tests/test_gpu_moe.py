@@ -112,6 +112,30 @@ def test_ffn_full_compare(M, dim, inter):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
+def test_ffn_workspace_shared_by_layers_of_different_shapes():
+    """The FFN's two GEMMs share one GEMM workspace at offset 0 of the FFN
+    workspace, so one workspace serves FFNs of different shapes: bit-equal to
+    fresh workspaces, counters back at zero."""
+    dev = torch.device("cuda")
+    shapes = [(300, 256, 1024), (1300, 512, 1024)]
+    layers = []
+    for i, (M, dim, inter) in enumerate(shapes):
+        x = synthetic.device_activations(M, dim, 111 + i, dev)
+        qs = [fb.weight_quant(synthetic.device_normal(sh, 121 + 3 * i + j, 0.02, dev))
+              for j, sh in enumerate([(inter, dim), (inter, dim), (dim, inter)])]
+        args = (x, qs[0][0], qs[0][1], qs[1][0], qs[1][1], qs[2][0], qs[2][1])
+        nb = fb.ffn_workspace_bytes(M, dim, inter)
+        want = fb.ffn(*args, ws=torch.zeros(nb, dtype=torch.uint8, device=dev))
+        layers.append((args, nb, want))
+    shared = torch.zeros(max(l[1] for l in layers), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        for args, nb, want in layers:
+            got = fb.ffn(*args, ws=shared[:nb])
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    assert torch.count_nonzero(shared[:64 * 1024]) == 0
+    assert fb.last_device_error() == 0
+
+
 def test_ffn_full_size_sampled_rows():
     """The prefill FFN (x [4096, 7168], inter 18432) on the device; the oracle
     recomputes two whole output rows (one per end of the row range)."""
