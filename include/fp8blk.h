@@ -343,9 +343,13 @@ FP8BLK_API int fp8blk_gemm_noalloc(const void *a_e4m3, const float *a_s, const v
 
 /*
  * Debug: synchronises `stream`, then returns and clears the device error
- * word of the current device (0 when no kernel gave up waiting). A non-zero
- * value means a kernel hit its wait limit and returned early: its outputs are
- * undefined and the workspace must be zero-filled again before reuse.
+ * word of the current device (0 when no kernel reported a problem). Bits
+ * 0x01-0x08: a GEMM role gave up waiting (producer, MMA, epilogue, drain);
+ * 0x20: an expert id outside [0, E) (MoE); 0x40: an MLA kernel gave up
+ * waiting; 0x80: a UE8M0-format scale that is not a positive normal power of
+ * two. After a wait gave up, that kernel returned early: its outputs are
+ * undefined and the workspace's first 64 KB must be zero-filled again before
+ * reuse. The function returns FP8BLK_ERR_TIMEOUT when any bit is set.
  */
 FP8BLK_API int fp8blk_last_device_error(fp8blk_stream_t stream, unsigned *device_error_bits);
 
