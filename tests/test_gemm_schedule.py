@@ -14,10 +14,12 @@ import pytest
 MAX_COUNTERS = 64 * 1024 // 4   # the workspace's fixed counter region, one int32 per tile
 
 
-def make_plan(M, N, K, sms, pairs=None):
+def make_plan(M, N, K, sms, pairs=None, split_k=True):
     """pairs: co-resident CTA pairs of the cluster kernel (default sms // 2;
     0 disables clusters). With pairs, large-M tiles of 128 x 256 run as
-    cluster pairs: the schedule's lane index counts pairs of 128-row tiles."""
+    cluster pairs: the schedule's lane index counts pairs of 128-row tiles.
+    split_k=False: no split-K clusters (their capacity is unknown, as when
+    the library plans without a device)."""
     if pairs is None:
         pairs = sms // 2
     Kb = K // 128
@@ -29,7 +31,7 @@ def make_plan(M, N, K, sms, pairs=None):
         if bn <= 64 and tiles <= sms and 2 * tiles >= sms:   # decode: one CTA per whole weight tile
             return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tiles, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
                         tiles=tiles, cluster=1, ksplit=1)
-        if 2 * tiles < sms:          # few tiles: split-K clusters of ks CTAs per tile
+        if split_k and 2 * tiles < sms:   # few tiles: split-K clusters of ks CTAs per tile
             for ks in (8, 4, 2):      # (co-resident clusters assumed: sms // ks)
                 if Kb >= 2 * ks and tiles * ks <= sms:
                     return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tiles * ks, dp=1, sk_tiles=0, sk_iters=0,
