@@ -842,9 +842,28 @@ def run_reference(args, kind, shape, steps, warmup):
 
 # ---------------------------------------------------------------------------
 
+def reaches_cluster_multicast(kind, shape) -> bool:
+    """True if the workload can run a GEMM kernel that loads with TMA
+    cluster multicast: the CTA-pair plans of dense GEMMs with M > 128 (and the
+    dense SwiGLU GEMM of the FFN). Decode-sized GEMMs (M <= 128, weights as the
+    MMA's M operand), the grouped expert GEMMs, dequant, the gate and the MLA
+    kernels never do."""
+    return (kind == "linear" and shape["M"] > 128) or kind == "ffn"
+
+
 def main():
     args = parse()
     kind, shape = WORKLOADS[args.workload]
+    world, rank, _ = dist_env()
+    if (world > 1 or args.gpus > 1) and args.impl == "ours" and reaches_cluster_multicast(kind, shape):
+        # Cluster-multicast kernels run only in single-GPU processes: refuse
+        # before the library is loaded or any GPU is touched.
+        if rank == 0:
+            print(json.dumps({"impl": "ours", "workload": args.workload, "unavailable":
+                              "one GPU by design: this workload's GEMMs use cluster-multicast TMA loads, "
+                              "which run only in single-GPU calls; multi-GPU replicas are offered for the "
+                              "decode-sized, expert, dequant, gate and MLA workloads"}))
+        return 0
     big = kind == "linear" and shape["M"] >= 2048 or kind in ("dequant", "ffn", "moe") or \
         kind == "mla" and shape["T"] >= 2048
     steps = args.steps if args.steps is not None else (200 if big else 100000)
