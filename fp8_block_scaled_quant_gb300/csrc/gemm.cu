@@ -1678,8 +1678,11 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M)));
 }
 
-int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
-             int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+// The argument checks of fp8_gemm, in order: FP8BLK_OK when they pass (an
+// empty problem, M == 0 or N == 0, passes without its pointers being looked
+// at; K == 0 needs only c).
+int gemm_check_args(const void* a, const float* a_s, const void* w, const float* w_s, const void* c, int64_t M,
+                    int64_t N, int64_t K, int scale_fmt) {
   if (scale_fmt != FP8BLK_SCALE_FP32 && scale_fmt != FP8BLK_SCALE_UE8M0) return FP8BLK_ERR_ARG;
   if (M < 0 || N < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
   if (M > (int64_t{1} << 31) - 1 || N > (int64_t{1} << 31) - 1 || K > (int64_t{1} << 31) - 1)
@@ -1687,10 +1690,18 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   if (M == 0 || N == 0) return FP8BLK_OK;
   if (!c) return FP8BLK_ERR_NULL;
   if (!is_aligned(c, 2)) return FP8BLK_ERR_ALIGN;
-  if (K == 0) return cuda_status(cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * 2, stream));
+  if (K == 0) return FP8BLK_OK;
   if (!a || !a_s || !w || !w_s) return FP8BLK_ERR_NULL;
   if (!is_aligned(a, 16) || !is_aligned(w, 16) || !is_aligned(a_s, 4) || !is_aligned(w_s, 4))
     return FP8BLK_ERR_ALIGN;
+  return FP8BLK_OK;
+}
+
+int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
+             int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (int st = gemm_check_args(a, a_s, w, w_s, c, M, N, K, scale_fmt)) return st;
+  if (M == 0 || N == 0) return FP8BLK_OK;
+  if (K == 0) return cuda_status(cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * 2, stream));
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
   const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
@@ -1955,8 +1966,6 @@ int noalloc_scratch(int dev, void** out) {
   return nd.status;
 }
 
-// Bytes at the start of a plan's workspace that hold the tile counters.
-
 }  // namespace
 }  // namespace fp8blk
 
@@ -1965,19 +1974,20 @@ extern "C" int fp8blk_gemm_noalloc(const void* a_e4m3, const float* a_s, const v
                                    fp8blk_stream_t stream) {
   using namespace fp8blk;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const int64_t lim = (int64_t{1} << 31) - 1;
-  if (M > 0 && N > 0 && K > 0 && K % kBlock == 0 && M <= lim && N <= lim && K <= lim) {
-    const DevInfo* d;
-    if (int st = current_device(&d)) return st;
-    const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
-    if (plan_workspace(pl) > FP8BLK_NOALLOC_SCRATCH_BYTES) return FP8BLK_ERR_TOO_LARGE;
-    void* scratch = nullptr;
-    if (int st = noalloc_scratch(d->device, &scratch)) return st;
-    if (cudaMemsetAsync(scratch, 0, plan_counter_bytes(pl), cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
-    return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, scratch, FP8BLK_NOALLOC_SCRATCH_BYTES, cs);
-  }
-  // Empty, zero-K and invalid problems need no scratch: same answers as fp8blk_gemm.
-  return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, nullptr, 0, cs);
+  // fp8blk_gemm's argument checks come first, so a rejected call returns the
+  // same status as fp8blk_gemm would and neither clears nor launches anything.
+  if (int st = gemm_check_args(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt)) return st;
+  // Empty and zero-K problems need no scratch.
+  if (M == 0 || N == 0 || K == 0)
+    return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, nullptr, 0, cs);
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
+  if (plan_workspace(pl) > FP8BLK_NOALLOC_SCRATCH_BYTES) return FP8BLK_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  if (int st = noalloc_scratch(d->device, &scratch)) return st;
+  if (cudaMemsetAsync(scratch, 0, plan_counter_bytes(pl), cs) != cudaSuccess) return FP8BLK_ERR_CUDA;
+  return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, scratch, FP8BLK_NOALLOC_SCRATCH_BYTES, cs);
 }
 
 extern "C" size_t fp8blk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {

@@ -325,7 +325,9 @@ FP8BLK_API int fp8blk_moe_grouped_gemm(const void *x_e4m3, const float *x_s, con
  * allocation while it executes, a latency-critical loop that must never
  * reach cudaMalloc/cudaFree (cudaFree synchronises the device), or a caller
  * that is handed device pointers but has no allocator of its own.
- * - Size limit: problems whose scratch need (fp8blk_gemm_workspace_bytes)
+ * - Arguments are checked first, exactly as fp8blk_gemm checks them (same
+ *   statuses, same order); a call that fails them touches nothing.
+ * - Size limit: then, problems whose scratch need (fp8blk_gemm_workspace_bytes)
  *   exceeds FP8BLK_NOALLOC_SCRATCH_BYTES return FP8BLK_ERR_TOO_LARGE and
  *   launch nothing. On a 152-SM GB300 every M <= 32 fits, for any N and K.
  * - The first call on a device looks up the buffer's device address; make that

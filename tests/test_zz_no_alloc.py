@@ -5,11 +5,15 @@ Its scratch is a buffer the library keeps in device memory, shared by every
 call on the device.
 
 Checked through the C ABI against fp8blk_gemm (the entry point that takes a
-workspace), within the GEMM tolerance the other tests use, on two calls in a
-row with different problems -- the second call must not see the first call's
-leftovers in the shared buffer -- and on a repeat of the first problem.
-Problems that need more scratch than the buffer holds are refused on the
-host. This file is collected last; it passes alone and after the others."""
+workspace). Both run the same plan and the same kernels, whose partial sums
+are added in a fixed order, so the outputs must be bit-identical. The calls
+come in a row on the shared buffer: a problem whose plan splits tiles
+stream-K (partial sums written to the buffer's slots, tile counters
+incremented and reset), then problems with other plans, then the first
+problem again -- no call may see another's leftovers. Problems that need
+more scratch than the buffer holds are refused on the host, after the same
+argument checks as fp8blk_gemm. This file is collected last; it passes alone
+and after the others."""
 import ctypes
 
 import numpy as np
@@ -18,11 +22,14 @@ import torch
 
 import fp8_block_scaled_quant_gb300 as fb
 import synthetic
-from helpers import gemm_tol
+from test_gemm_schedule import make_plan, units
 
 pytestmark = pytest.mark.gpu
 
+ERR_NULL = 1
+ERR_ARG = 8
 ERR_TOO_LARGE = 9
+SCRATCH = 8 << 20
 
 
 def noalloc_fn():
@@ -48,36 +55,49 @@ def call_noalloc(f, a, a_s, q, s, out):
     return f(a.data_ptr(), a_s.data_ptr(), q.data_ptr(), s.data_ptr(), out.data_ptr(), M, N, K, 0, stream)
 
 
-def assert_close(got, ref):
-    g = got.float().cpu().numpy().astype(np.float64)
-    r = ref.float().cpu().numpy().astype(np.float64)
-    assert np.all(np.abs(g - r) <= gemm_tol(r))
+def assert_same_bits(got, ref):
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
 
 
-def test_noalloc_matches_gemm_on_two_calls_in_a_row():
+def test_stream_k_shape_writes_partials():
+    """The first problem below really runs stream-K with split tiles (plan
+    mirror at this GPU's SM count), within the scratch."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = make_plan(8, 24576, 1536, sms)
+    assert p["swap"] and p["ksplit"] == 1 and not p.get("whole") and p["sk_tiles"] > 0
+    assert any(u[4] > 1 for c in range(p["grid"]) for u in units(p, c)), "no tile is split"
+    assert fb.gemm_workspace_bytes(8, 24576, 1536) <= SCRATCH
+
+
+def test_noalloc_matches_gemm_on_calls_in_a_row():
     f = noalloc_fn()
-    p1 = problem(8, 10944, 2048, 31)      # decode-shaped: stream-K partials in the scratch
-    p2 = problem(16, 320, 256, 32)        # another plan on the same scratch
-    ref1 = fb.fp8_gemm(*p1)
-    ref2 = fb.fp8_gemm(*p2)
-    out1 = torch.empty((8, 10944), dtype=torch.bfloat16, device="cuda")
-    out2 = torch.empty((16, 320), dtype=torch.bfloat16, device="cuda")
-    assert call_noalloc(f, *p1, out1) == 0
-    assert call_noalloc(f, *p2, out2) == 0
+    shapes = [(8, 24576, 1536), (8, 10944, 2048), (64, 10944, 2048), (16, 320, 256)]
+    probs = [problem(M, N, K, 31 + i) for i, (M, N, K) in enumerate(shapes)]
+    refs = [fb.fp8_gemm(*p) for p in probs]
+    outs = [torch.empty_like(r) for r in refs]
+    for p, o in zip(probs, outs):
+        assert call_noalloc(f, *p, o) == 0
+    again = torch.empty_like(refs[0])
+    assert call_noalloc(f, *probs[0], again) == 0
     torch.cuda.synchronize()
-    assert_close(out1, ref1)
-    assert_close(out2, ref2)
-    out3 = torch.empty_like(out1)
-    assert call_noalloc(f, *p1, out3) == 0
-    torch.cuda.synchronize()
-    assert_close(out3, ref1)
+    for o, r in zip(outs, refs):
+        assert_same_bits(o, r)
+    assert_same_bits(again, refs[0])
     assert fb.last_device_error() == 0
 
 
-def test_noalloc_refuses_problems_beyond_its_scratch():
+def test_noalloc_checks_arguments_then_size():
     f = noalloc_fn()
     M, N, K = 4096, 18432, 7168
-    assert fb.gemm_workspace_bytes(M, N, K) > (8 << 20)
-    # refused on the host before any pointer is read or kernel launched
-    assert f(None, None, None, None, None, M, N, K, 0, None) == ERR_TOO_LARGE
+    assert fb.gemm_workspace_bytes(M, N, K) > SCRATCH
+    buf = torch.zeros(256, dtype=torch.uint8, device="cuda")   # aligned, never read: the call is refused
+    p = buf.data_ptr()
+    stream = torch.cuda.current_stream().cuda_stream
+    # argument errors come first, as in fp8blk_gemm
+    assert f(None, None, None, None, None, M, N, K, 0, stream) == ERR_NULL
+    assert f(p, p, p, p, p, M, N, K, 7, stream) == ERR_ARG
+    # then the size: refused on the host, nothing launched or cleared
+    assert f(p, p, p, p, p, M, N, K, 0, stream) == ERR_TOO_LARGE
+    torch.cuda.synchronize()
+    assert int(buf.sum()) == 0
     assert b"fp8blk_gemm" in fb.lib().fp8blk_status_string(ERR_TOO_LARGE)
