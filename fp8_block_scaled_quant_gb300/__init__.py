@@ -20,7 +20,7 @@ import threading
 import torch
 
 __all__ = [
-    "SCALE_FP32", "SCALE_UE8M0", "BLOCK", "lib", "lib_path", "header_functions", "Fp8BlkError",
+    "SCALE_FP32", "SCALE_UE8M0", "SCALE_PROMOTE", "BLOCK", "lib", "lib_path", "header_functions", "Fp8BlkError",
     "act_quant", "weight_quant", "weight_dequant", "fp8_gemm", "linear", "linear_host",
     "gemm_workspace_bytes", "linear_workspace_bytes", "linear_host_workspace_bytes", "last_device_error",
     "swiglu_gemm", "ffn", "moe_permute", "moe_workspace_bytes", "moe_grouped_gemm",
@@ -28,6 +28,7 @@ __all__ = [
 
 SCALE_FP32 = 0
 SCALE_UE8M0 = 1
+SCALE_PROMOTE = 0x10   # | SCALE_UE8M0: GEMMs keep the per-block promotion
 BLOCK = 128
 
 _PKG = os.path.dirname(os.path.abspath(__file__))

@@ -52,8 +52,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <stdlib.h>
-
 #include <mutex>
 
 #include "fp8blk.h"
@@ -1401,14 +1399,10 @@ using CfgSwiGLUC2MX = Cfg<256, false, 4, 1, 8, kEpiSwiGLU, false, false, 2, true
 using CfgSwiGLUGroupedMX = Cfg<256, false, 4, 1, 8, kEpiSwiGLU, true, false, 1, true>;
 using CfgScatterGroupedMX = Cfg<256, false, 4, 1, 8, kEpiScatter, true, false, 1, true>;
 
-// UE8M0 scales take the tensor-core scaled kernels (MX) unless the
-// environment variable FP8BLK_UE8M0_MMA is "0" at the call; that keeps the
-// per-block promotion, which computes the same numbers.
-bool mx_for(int scale_fmt) {
-  if (scale_fmt != FP8BLK_SCALE_UE8M0) return false;
-  const char* v = getenv("FP8BLK_UE8M0_MMA");
-  return !(v && v[0] == '0' && v[1] == 0);
-}
+// UE8M0 scales take the tensor-core scaled kernels (MX) unless the call adds
+// FP8BLK_SCALE_PROMOTE; that keeps the per-block promotion, which computes the
+// same numbers in another summation order.
+bool mx_for(int scale_fmt) { return scale_fmt_mx(scale_fmt); }
 // Decode linear with the act_quant fused in (M <= 16): weights-only stages.
 using CfgF16S8 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, true>;
 using CfgF16S4 = Cfg<16, true, 4, 8, 4, kEpiBf16, false, true>;
@@ -1683,7 +1677,7 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 // at; K == 0 needs only c).
 int gemm_check_args(const void* a, const float* a_s, const void* w, const float* w_s, const void* c, int64_t M,
                     int64_t N, int64_t K, int scale_fmt) {
-  if (scale_fmt != FP8BLK_SCALE_FP32 && scale_fmt != FP8BLK_SCALE_UE8M0) return FP8BLK_ERR_ARG;
+  if (!scale_fmt_valid(scale_fmt)) return FP8BLK_ERR_ARG;
   if (M < 0 || N < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
   if (M > (int64_t{1} << 31) - 1 || N > (int64_t{1} << 31) - 1 || K > (int64_t{1} << 31) - 1)
     return FP8BLK_ERR_SHAPE;
@@ -1760,7 +1754,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
 
 namespace {
 
-bool scale_fmt_ok(int f) { return f == FP8BLK_SCALE_FP32 || f == FP8BLK_SCALE_UE8M0; }
+bool scale_fmt_ok(int f) { return scale_fmt_valid(f); }
 
 }  // namespace
 
@@ -1798,7 +1792,7 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
   prm.tiles_col = 1;
   prm.whole_tiles = prm.n_wblocks;
   prm.grid = prm.n_wblocks < d->sm_count ? prm.n_wblocks : d->sm_count;
-  prm.ue8m0 = scale_fmt == FP8BLK_SCALE_UE8M0;
+  prm.ue8m0 = scale_fmt_ue8m0(scale_fmt);
   CUtensorMap ml;
   if (!make_kmajor_map(&ml, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128)) return FP8BLK_ERR_CUDA;
   *used = true;
@@ -1852,7 +1846,7 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
   prm.sk_tiles = pl.sk_tiles;
   prm.sk_iters = pl.sk_iters;
   prm.whole_tiles = pl.whole_tiles;
-  prm.ue8m0 = scale_fmt == FP8BLK_SCALE_UE8M0;
+  prm.ue8m0 = scale_fmt_ue8m0(scale_fmt);
   CUtensorMap ml, m1, m3;
   if (!make_kmajor_map(&ml, xq, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128) ||
       !make_kmajor_map(&m1, w1, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64) ||
@@ -1889,7 +1883,7 @@ int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const f
   prm.E = static_cast<int>(E);
   prm.tiles_col = static_cast<int>(inter / 128);
   prm.grid = d->sm_count;
-  prm.ue8m0 = scale_fmt == FP8BLK_SCALE_UE8M0;
+  prm.ue8m0 = scale_fmt_ue8m0(scale_fmt);
   CUtensorMap ml, m1, m3;
   if (!make_kmajor_map(&ml, xg, static_cast<uint64_t>(rows), static_cast<uint64_t>(K), 128) ||
       !make_kmajor_map(&m1, w1, static_cast<uint64_t>(E * inter), static_cast<uint64_t>(K), 64) ||

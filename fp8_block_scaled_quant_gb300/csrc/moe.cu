@@ -617,7 +617,7 @@ extern "C" int fp8blk_moe_grouped_gemm(const void* x_e4m3, const float* x_s, con
                                        const float* w2_s, void* y_bf16, int64_t T, int64_t topk, int64_t E,
                                        int64_t dim, int64_t inter, int64_t n_shared, int scale_fmt, void* workspace,
                                        size_t workspace_bytes, fp8blk_stream_t stream) {
-  if (scale_fmt != FP8BLK_SCALE_FP32 && scale_fmt != FP8BLK_SCALE_UE8M0) return FP8BLK_ERR_ARG;
+  if (!scale_fmt_valid(scale_fmt)) return FP8BLK_ERR_ARG;
   if (T < 0 || topk < 0 || n_shared < 0 || E <= 0 || E + n_shared > kMaxExperts || dim <= 0 || inter <= 0 ||
       dim % 256 || inter % kBlock)
     return FP8BLK_ERR_SHAPE;

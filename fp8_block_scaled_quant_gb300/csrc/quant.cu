@@ -270,7 +270,7 @@ namespace fp8blk {
 // reads only its weights before it waits for this one).
 int act_quant_launch(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, float* s, int scale_fmt,
                      cudaStream_t stream, bool trigger) {
-  if (scale_fmt != FP8BLK_SCALE_FP32 && scale_fmt != FP8BLK_SCALE_UE8M0) return FP8BLK_ERR_ARG;
+  if (!scale_fmt_valid(scale_fmt)) return FP8BLK_ERR_ARG;
   if (M < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
   if (M == 0 || K == 0) return FP8BLK_OK;
   if (!x_bf16 || !q_e4m3 || !s) return FP8BLK_ERR_NULL;
@@ -290,7 +290,7 @@ int act_quant_launch(const void* x_bf16, int64_t M, int64_t K, void* q_e4m3, flo
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cuda_status(cudaLaunchKernelEx(&cfg, act_quant_kernel, static_cast<const uint4*>(x_bf16),
-                                        static_cast<uint2*>(q_e4m3), s, nblocks, scale_fmt == FP8BLK_SCALE_UE8M0,
+                                        static_cast<uint2*>(q_e4m3), s, nblocks, scale_fmt_ue8m0(scale_fmt),
                                         trigger));
 }
 
@@ -303,7 +303,7 @@ extern "C" int fp8blk_act_quant(const void* x_bf16, int64_t M, int64_t K, void* 
 
 extern "C" int fp8blk_weight_quant(const float* w, int64_t N, int64_t K, void* q_e4m3, float* s, int scale_fmt,
                                    fp8blk_stream_t stream) {
-  if (scale_fmt != FP8BLK_SCALE_FP32 && scale_fmt != FP8BLK_SCALE_UE8M0) return FP8BLK_ERR_ARG;
+  if (!scale_fmt_valid(scale_fmt)) return FP8BLK_ERR_ARG;
   if (N < 0 || K < 0) return FP8BLK_ERR_SHAPE;
   if (N == 0 || K == 0) return FP8BLK_OK;
   if (!w || !q_e4m3 || !s) return FP8BLK_ERR_NULL;
@@ -314,7 +314,7 @@ extern "C" int fp8blk_weight_quant(const float* w, int64_t N, int64_t K, void* q
   if (int st = current_device(&d)) return st;
   dim3 grid(static_cast<unsigned>(nbk), static_cast<unsigned>(nbn));
   weight_quant_kernel<<<grid, kWqThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      w, static_cast<uint8_t*>(q_e4m3), s, N, K, nbk, scale_fmt == FP8BLK_SCALE_UE8M0);
+      w, static_cast<uint8_t*>(q_e4m3), s, N, K, nbk, scale_fmt_ue8m0(scale_fmt));
   return launch_status();
 }
 

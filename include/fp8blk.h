@@ -21,7 +21,8 @@
  *   - Block size is 128: activation scales are one fp32 per (row, 128
  *     columns), weight scales one fp32 per 128x128 block.
  *   - scale_fmt is FP8BLK_SCALE_FP32 (0) or FP8BLK_SCALE_UE8M0 (1, scales
- *     rounded up to a power of two and still stored as fp32).
+ *     rounded up to a power of two and still stored as fp32), optionally
+ *     with FP8BLK_SCALE_PROMOTE (below).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; 0 = the legacy
  *     default stream). Arguments are checked on the host before any launch;
  *     a failed check launches nothing and returns a non-zero status.
@@ -58,6 +59,17 @@ extern "C" {
 typedef struct CUstream_st *fp8blk_stream_t; /* identical to cudaStream_t */
 
 enum fp8blk_scale_fmt { FP8BLK_SCALE_FP32 = 0, FP8BLK_SCALE_UE8M0 = 1 };
+
+/*
+ * OR'ed into FP8BLK_SCALE_UE8M0 (scale_fmt = FP8BLK_SCALE_UE8M0 |
+ * FP8BLK_SCALE_PROMOTE): the GEMMs of this call keep the per-128-K promotion
+ * (each K block's tensor-core partial scaled by a_s * w_s and added in fp32
+ * registers) instead of letting the tensor core apply the power-of-two scales.
+ * Same arithmetic, another summation order. Per call, so callers in one
+ * process may choose differently. The quantising entry points accept it and
+ * quantise as FP8BLK_SCALE_UE8M0. Any other combination is FP8BLK_ERR_ARG.
+ */
+#define FP8BLK_SCALE_PROMOTE 0x10
 
 enum fp8blk_status {
   FP8BLK_OK = 0,
@@ -138,8 +150,8 @@ FP8BLK_API int fp8blk_weight_dequant(const void *q_e4m3, const float *s, int64_t
  * let the tensor core apply the scales itself (block-scaled MMA,
  * one UE8M0 exponent per operand row and 32-wide K slice), and a scale that
  * is not such a power of two sets device error bit 0x80 (its outputs are
- * undefined). Setting the environment variable FP8BLK_UE8M0_MMA to "0"
- * keeps the per-block promotion for UE8M0 as well.
+ * undefined). FP8BLK_SCALE_UE8M0 | FP8BLK_SCALE_PROMOTE keeps the per-block
+ * promotion for UE8M0 as well.
  * workspace: device memory of at least fp8blk_gemm_workspace_bytes(M, N, K),
  * 256-byte aligned. Its first 64 KB hold the tile counters: ZERO-FILLED
  * before the first use, and every call leaves them at zero; the rest is

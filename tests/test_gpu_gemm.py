@@ -205,7 +205,7 @@ def sampled_check(M, N, K, seed, frac=0.0, n_random=48, fmt=fb.SCALE_FP32):
     outputs from host copies of the same bf16 / fp32 inputs (quantising the
     needed rows and weight blocks itself)."""
     dev = torch.device("cuda")
-    ue = fmt == fb.SCALE_UE8M0
+    ue = (fmt & ~fb.SCALE_PROMOTE) == fb.SCALE_UE8M0
     x = synthetic.device_activations(M, K, seed, dev, outlier_frac=frac)
     w = synthetic.device_normal((N, K), seed + 1, 0.02, dev)
     a, a_s = fb.act_quant(x, fmt)
@@ -247,24 +247,24 @@ def test_gemm_full_size_sampled(M, N, K):
     sampled_check(M, N, K, 4000 + M % 97 + N % 89, frac=0.01)
 
 
-@pytest.mark.parametrize("mma", ["1", "0"])
+@pytest.mark.parametrize("mma", [True, False])
 @pytest.mark.parametrize("M,N,K", [(1300, 7000, 640), (4096, 18432, 7168), (4096, 7168, 18432)])
-def test_gemm_ue8m0_tensor_core_scaling_sampled(M, N, K, mma, monkeypatch):
+def test_gemm_ue8m0_tensor_core_scaling_sampled(M, N, K, mma):
     """Power-of-two scales on 128 x 256 tiles: the tensor core applies the
     UE8M0 scales itself (block-scaled MMA, one accumulator over the whole K
     range). 1300 x 7000 x 640: cluster pairs, a ragged row tile, a partial
     weight block, stream-K parts, 5 K blocks (a scale group of 4 and one of
     1); 7168 and 18432: 14 and 36 scale groups through the 8-slot ring.
-    mma "0": the same problems through the per-block promotion."""
-    monkeypatch.setenv("FP8BLK_UE8M0_MMA", mma)
-    sampled_check(M, N, K, 5000 + M % 97 + N % 89, frac=0.01, fmt=fb.SCALE_UE8M0)
+    mma False: the same problems through the per-block promotion (the
+    FP8BLK_SCALE_PROMOTE flag of the call)."""
+    fmt = fb.SCALE_UE8M0 if mma else fb.SCALE_UE8M0 | fb.SCALE_PROMOTE
+    sampled_check(M, N, K, 5000 + M % 97 + N % 89, frac=0.01, fmt=fmt)
     assert fb.last_device_error() == 0
 
 
-def test_gemm_ue8m0_flags_scales_that_are_not_powers_of_two(monkeypatch):
+def test_gemm_ue8m0_flags_scales_that_are_not_powers_of_two():
     """Under UE8M0 the tensor core takes only the exponent of each scale: fp32
     weight scales that are not powers of two set the device error bit 1 << 7."""
-    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "1")
     dev = torch.device("cuda")
     a, a_s = fb.act_quant(synthetic.device_activations(1300, 640, 91, dev), fb.SCALE_UE8M0)
     q, s = fb.weight_quant(synthetic.device_normal((7000, 640), 92, 0.02, dev))
@@ -313,7 +313,7 @@ def test_fused_decode_linear(M, N, K, fmt):
     8 weight stages up to K = 5888 and 4 beyond): same bits as act_quant +
     fp8_gemm on the same whole-tile schedule (N <= 128 * SMs), and within the
     GEMM tolerance of the oracle."""
-    ue = fmt == fb.SCALE_UE8M0
+    ue = (fmt & ~fb.SCALE_PROMOTE) == fb.SCALE_UE8M0
     x, w, xq, xs, wq, ws = host_problem(M, N, K, 3000 + M + N, 0.01, ue8m0=ue)
     xd = bits_to_dev_bf16(x)
     q, s = fb.weight_quant(torch.from_numpy(w).cuda(), fmt)

@@ -66,13 +66,12 @@ def oracle_u(xq, xs, w1q, w1s, w3q, w3s, ue8m0=False):
 
 @pytest.mark.parametrize("M,dim,inter", [(5, 256, 384), (130, 512, 256), (300, 256, 1024)])
 @pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-promotion"])
-def test_swiglu_gemm_matches_oracle_chain(M, dim, inter, fmt, monkeypatch):
+def test_swiglu_gemm_matches_oracle_chain(M, dim, inter, fmt):
     """UE8M0 scales are applied by the tensor core (block-scaled MMA);
     ue8m0-promotion: the same scales through the per-block promotion."""
-    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "0" if fmt == "ue8m0-promotion" else "1")
     if fmt == "ue8m0-promotion":
-        fmt = fb.SCALE_UE8M0
-    ue = fmt == fb.SCALE_UE8M0
+        fmt = fb.SCALE_UE8M0 | fb.SCALE_PROMOTE
+    ue = (fmt & ~fb.SCALE_PROMOTE) == fb.SCALE_UE8M0
     x = synthetic.activations(M, dim, 600 + M)
     xq, xs = oracle.act_quant(x, ue)
     w1q, w1s = oracle.weight_quant(synthetic.weights(inter, dim, 601 + M), ue)
@@ -206,15 +205,15 @@ def run_moe(p, E, fmt=fb.SCALE_FP32):
 @pytest.mark.parametrize("T,E,dim,inter,k,zipf", [(64, 8, 256, 256, 2, 0.0), (96, 16, 512, 384, 4, 1.2),
                                                   (33, 5, 256, 128, 3, 0.0), (300, 4, 256, 256, 1, 0.0)])
 @pytest.mark.parametrize("fmt", [fb.SCALE_FP32, fb.SCALE_UE8M0, "ue8m0-promotion"])
-def test_moe_full_compare(T, E, dim, inter, k, zipf, fmt, monkeypatch):
+def test_moe_full_compare(T, E, dim, inter, k, zipf, fmt):
     """UE8M0: both grouped GEMMs with the scales applied by the tensor core;
     ue8m0-promotion: the same scales through the per-block promotion."""
-    monkeypatch.setenv("FP8BLK_UE8M0_MMA", "0" if fmt == "ue8m0-promotion" else "1")
     if fmt == "ue8m0-promotion":
-        fmt = fb.SCALE_UE8M0
-    p = moe_problem(T, E, dim, inter, k, 800 + T + E, zipf, fmt == fb.SCALE_UE8M0)
+        fmt = fb.SCALE_UE8M0 | fb.SCALE_PROMOTE
+    ue = (fmt & ~fb.SCALE_PROMOTE) == fb.SCALE_UE8M0
+    p = moe_problem(T, E, dim, inter, k, 800 + T + E, zipf, ue)
     y = run_moe(p, E, fmt)
-    ref, allow = moe_reference(p, range(T), E, ue8m0=fmt == fb.SCALE_UE8M0)
+    ref, allow = moe_reference(p, range(T), E, ue8m0=ue)
     assert_chain_close(dev_to_bits(y), ref, allow, what=f"moe T={T} E={E}")
     assert fb.last_device_error() == 0
 
