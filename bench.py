@@ -224,7 +224,7 @@ def barrier():
 
 
 # ---------------------------------------------------------------------------
-# traffic figures recorded from ncu (profiles/), valid only for unchanged sources
+# traffic figures recorded from ncu captures, valid only for unchanged sources
 # ---------------------------------------------------------------------------
 
 _COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
@@ -261,21 +261,17 @@ def kernel_source_digest(kernel: str | None = None) -> str:
 
 
 def recorded_traffic(workload: str, kernel: str):
-    """dram bytes per launch recorded in profiles/*.md by an ncu capture of this
-    workload, if the kernel's sources are unchanged since (else None)."""
-    pdir = os.path.join(ROOT, "profiles")
-    if not os.path.isdir(pdir):
+    """DRAM bytes per launch that an ncu capture of this workload recorded in
+    profiles/traffic.json, if the kernel's sources are unchanged since (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
         return None
+    with open(path) as f:
+        records = json.load(f).get("records", [])
     digest = kernel_source_digest(kernel)
-    for name in sorted(os.listdir(pdir)):
-        if not name.endswith(".md"):
-            continue
-        with open(os.path.join(pdir, name)) as f:
-            text = f.read()
-        for m in re.finditer(r"^traffic: workload=(\S+) kernel=(\S+) bytes_per_launch=(\d+) sources=(\w+)",
-                             text, re.M):
-            if m.group(1) == workload and m.group(2) == kernel and m.group(4) == digest:
-                return int(m.group(3))
+    for r in records:
+        if r.get("workload") == workload and r.get("kernel") == kernel and r.get("sources") == digest:
+            return int(r["bytes_per_launch"])
     return None
 
 
