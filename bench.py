@@ -89,6 +89,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-other", action="store_true",
+                    help="skip the other_workloads key (prefill GEMM and MoE step, fp32 and UE8M0 scales)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step from the host instead of replaying CUDA graphs (for profilers)")
     return ap.parse_args()
@@ -311,6 +313,55 @@ def make_runs(fn_step, n_steps, chunk, torch, eager):
     return graph_chunks(fn_step, n_steps, chunk, torch)
 
 
+def upload_graphs(graphs, stream, torch) -> bool:
+    """Upload captured graphs to the device before they are timed, so that a
+    graph's first replay does not pay for its upload inside the timed region
+    (cuGraphUpload through the driver; False where it is not available)."""
+    import ctypes
+
+    try:
+        upload = ctypes.CDLL("libcuda.so.1").cuGraphUpload
+    except (OSError, AttributeError):
+        return False
+    upload.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    upload.restype = ctypes.c_int
+    ok = True
+    for g in graphs:
+        if not hasattr(g, "raw_cuda_graph_exec"):
+            return False
+        ok = upload(ctypes.c_void_p(g.raw_cuda_graph_exec()), ctypes.c_void_p(stream.cuda_stream)) == 0 and ok
+    torch.cuda.synchronize()
+    return ok
+
+
+SOAK_S = 2.0   # untimed replays right before each timed region, so clock samplers see the GPU under load
+
+
+def timed_runs(dev, stream, torch, main, extras=(), soak=None, soak_s=SOAK_S):
+    """Times `main` (graphs of exactly the --steps steps) and then each list of
+    graphs in `extras` (kernel-only passes), with nvidia-smi sampling clocks.
+    Before the timed region the `soak` graphs are replayed for soak_s seconds
+    (untimed), so that the clocks sampled -- by this process and by anyone
+    watching the GPU -- are those of the GPU under this load. Returns
+    (elapsed of main, [elapsed of each extra], clock summary over soak + main,
+    whether the graphs were uploaded before timing)."""
+    graphs = list(main) + [g for e in extras for g in e] + list(soak or [])
+    uploaded = upload_graphs(graphs, stream, torch)
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        ts = time.time()
+        if soak:
+            while time.time() - ts < soak_s:
+                for g in soak:
+                    g.replay()
+                torch.cuda.synchronize()
+        el, t0, t1 = timed_replay(main, stream, torch)
+        els = [timed_replay(e, stream, torch)[0] for e in extras]
+    clocks = clk.summary(ts, t1)
+    clocks["window"] = f"{soak_s if soak else 0:.1f} s of untimed replays of the step, then the timed region"
+    return el, els, clocks, uploaded
+
+
 def timed_replay(graphs, stream, torch):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -371,16 +422,12 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     g_main = make_runs(step, steps, chunk, torch, args.eager)
     g_gemm = make_runs(gemm_only, steps, chunk, torch, args.eager)
     g_aq = make_runs(aq_only, steps, chunk, torch, args.eager)
+    g_soak = make_runs(step, chunk, chunk, torch, args.eager)
     for g in g_warm:
         g.replay()
     torch.cuda.synchronize()
 
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.3)
-        el, t0, t1 = timed_replay(g_main, stream, torch)
-        el_gemm, _, _ = timed_replay(g_gemm, stream, torch)
-        el_aq, _, _ = timed_replay(g_aq, stream, torch)
-    clocks = clk.summary(t0, t1)
+    el, (el_gemm, el_aq), clocks, uploaded = timed_runs(dev, stream, torch, g_main, (g_gemm, g_aq), g_soak)
     assert fb.last_device_error(dev) == 0, "a kernel reported a wait timeout"
 
     # M <= 2: fp8blk_linear is one kernel (act_quant fused into the GEMM);
@@ -430,7 +477,8 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
                    "w": "e4m3 from N(0,0.02), " + ("power-of-two (UE8M0)" if fmt else "fp32") + " 128x128 block scales",
                    "scale_fmt": "ue8m0" if fmt else "fp32",
                    "l2": f"weights rotate over {R} copies ({R * w_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
-                   "launch": "host loop" if args.eager else f"CUDA graphs of {chunk} steps"},
+                   "launch": "host loop" if args.eager else
+                   f"CUDA graphs of up to {chunk} steps" + (", uploaded before timing" if uploaded else "")},
         "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
     }
     return out
@@ -503,12 +551,10 @@ def run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     g_warm = make_runs(step, warmup, 10, torch, args.eager)
     g_main = make_runs(step, steps, 10, torch, args.eager)
     g_swi = make_runs(swiglu_only, steps, 10, torch, args.eager)
+    g_soak = make_runs(step, 10, 10, torch, args.eager)
     for g in g_warm:
         g.replay()
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.3)
-        el, t0, t1 = timed_replay(g_main, stream, torch)
-        el_swi, _, _ = timed_replay(g_swi, stream, torch)
+    el, (el_swi,), clocks, _ = timed_runs(dev, stream, torch, g_main, (g_swi,), g_soak)
     assert fb.last_device_error(dev) == 0
     flops = 3 * 2.0 * M * dim * inter
     el_max, units = reduce_over_ranks(el, steps * flops, dev)
@@ -518,7 +564,7 @@ def run_ffn(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     del wsp
     return {
         "value": units / el_max / 1e12, "unit": "TFLOP/s", "ms_per_step": el_max / steps * 1e3,
-        "clocks": clk.summary(t0, t1), "gpu_launches": 3 * steps,
+        "clocks": clocks, "gpu_launches": 3 * steps,
         "roofline": {"bound": "tensor", "kernel": "fused w1/w3 GEMM + SwiGLU + act_quant", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "traffic": recorded_traffic(args.workload, "swiglu_gemm"),
@@ -568,11 +614,10 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     stream = torch.cuda.current_stream(dev)
     g_warm = make_runs(step, warmup, 10, torch, args.eager)
     g_main = make_runs(step, steps, 10, torch, args.eager)
+    g_soak = make_runs(step, 10, 10, torch, args.eager)
     for g in g_warm:
         g.replay()
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.3)
-        el, t0, t1 = timed_replay(g_main, stream, torch)
+    el, _, clocks, _ = timed_runs(dev, stream, torch, g_main, (), g_soak)
     assert fb.last_device_error(dev) == 0
     touched = int(np.unique(idx_np).size) + ns
     b = moe_weight_bytes(touched, dim, inter) + T * dim + T * (dim // 128) * 4 + T * dim * 2 + T * k * 8
@@ -582,7 +627,7 @@ def run_moe(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     return {
         "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
         "tflops": steps * flops / el / 1e12,
-        "clocks": clk.summary(t0, t1), "gpu_launches": (7 + (1 if ns else 0)) * steps,
+        "clocks": clocks, "gpu_launches": (7 + (1 if ns else 0)) * steps,
         "roofline": {"bound": "hbm", "kernel": f"whole routed-expert step ({7 + (1 if ns else 0)} kernels)",
                      "achieved": achieved,
                      "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
@@ -614,17 +659,16 @@ def run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     stream = torch.cuda.current_stream(dev)
     g_warm = make_runs(step, warmup, 20, torch, args.eager)
     g_main = make_runs(step, steps, 20, torch, args.eager)
+    g_soak = make_runs(step, 20, 20, torch, args.eager)
     for g in g_warm:
         g.replay()
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.3)
-        el, t0, t1 = timed_replay(g_main, stream, torch)
+    el, _, clocks, _ = timed_runs(dev, stream, torch, g_main, (), g_soak)
     b = dequant_bytes(N, K)
     el_max, units = reduce_over_ranks(el, steps * b, dev)
     achieved = b / (el / steps) / 1e9
     return {
         "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
-        "clocks": clk.summary(t0, t1), "gpu_launches": steps,
+        "clocks": clocks, "gpu_launches": steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm"], "traffic": recorded_traffic(args.workload, "weight_dequant"),
                      "peak_source": f"hbm_gbs ({peaks['src']})", "algorithmic_bytes_per_launch": b},
@@ -662,11 +706,10 @@ def run_mla(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     stream = torch.cuda.current_stream(dev)
     g_warm = make_runs(step, warmup, 50, torch, args.eager)
     g_main = make_runs(step, steps, 50, torch, args.eager)
+    g_soak = make_runs(step, 50, 50, torch, args.eager)
     for g in g_warm:
         g.replay()
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.3)
-        el, t0, t1 = timed_replay(g_main, stream, torch)
+    el, _, clocks, _ = timed_runs(dev, stream, torch, g_main, (), g_soak)
     assert fb.last_device_error(dev) == 0
     b = w_bytes + (H * (dn + dv) // 128) * (C // 128) * 4 + 2 * T * H * (dn + C) * 2
     flops = 2 * 2.0 * T * H * dn * C
@@ -685,7 +728,7 @@ def run_mla(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     roof.update({"kernel": "mla_absorb_kernel (qk + v)", "traffic": None, "algorithmic_bytes_per_launch": b // 2,
                  "kernel_us": per / 2 * 1e6})
     return {
-        "value": value, "unit": unit, "ms_per_step": el_max / steps * 1e3, "clocks": clk.summary(t0, t1),
+        "value": value, "unit": unit, "ms_per_step": el_max / steps * 1e3, "clocks": clocks,
         "gpu_launches": 2 * steps, "roofline": roof, "e2e": None,
         "config": {"workload": args.workload, "T": T, "heads": H, "kv_lora": C, "qk_nope": dn, "v_head": dv,
                    "l2": f"wkv_b rotates over {R} copies ({R * w_bytes / 1e6:.0f} MB > 3x L2)"},
@@ -720,12 +763,10 @@ def run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     g_warm = make_runs(step, warmup, 50, torch, args.eager)
     g_main = make_runs(step, steps, 50, torch, args.eager)
     g_gate = make_runs(gate, steps, 50, torch, args.eager)
+    g_soak = make_runs(step, 50, 50, torch, args.eager)
     for g in g_warm:
         g.replay()
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.3)
-        el, t0, t1 = timed_replay(g_main, stream, torch)
-        el_gate, _, _ = timed_replay(g_gate, stream, torch)
+    el, (el_gate,), clocks, _ = timed_runs(dev, stream, torch, g_main, (g_gate,), g_soak)
     assert fb.last_device_error(dev) == 0
     b_gate = T * E * 4 + E * 4 + T * k * 8            # logits, bias in; ids, weights out
     b_step = b_gate + T * k * 4 + T * k * 4 + (2 * E + 1) * 4   # + ids read by the permutation, perm, counts
@@ -733,7 +774,7 @@ def run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     achieved = b_gate / (el_gate / steps) / 1e9
     return {
         "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
-        "clocks": clk.summary(t0, t1), "gpu_launches": 4 * steps,
+        "clocks": clocks, "gpu_launches": 4 * steps,
         "kernels_us": {"gate_and_permute": el / steps * 1e6, "gate_alone": el_gate / steps * 1e6},
         "roofline": {"bound": "hbm", "kernel": "moe_gate", "achieved": achieved, "peak": peaks["hbm"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None,
@@ -786,39 +827,147 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(shape, kind, budget_s=10.0):
+def block_row_ranges(N: int, parts: int):
+    """Row ranges of whole 128-row weight blocks (the last one ragged), about
+    N / parts rows each: the oracle runs one range per host thread."""
+    nb = -(-N // 128)
+    parts = max(1, min(parts, nb))
+    edges = [min(N, (nb * i // parts) * 128) for i in range(parts + 1)]
+    return [(edges[i], edges[i + 1]) for i in range(parts) if edges[i + 1] > edges[i]]
+
+
+def oracle_gemm_threads(xq, xs, wq, ws, cores: int):
+    """The oracle's GEMM with the weight rows split over `cores` host threads
+    (the C oracle runs outside the interpreter lock), joined by columns."""
+    import concurrent.futures as cf
+
+    import oracle
+
+    ranges = block_row_ranges(wq.shape[0], cores)
+    with cf.ThreadPoolExecutor(len(ranges)) as ex:
+        parts = list(ex.map(lambda r: oracle.gemm(xq, xs, wq[r[0]:r[1]], ws[r[0] // 128:-(-r[1] // 128)]), ranges))
+    return np.concatenate(parts, axis=1)
+
+
+def oracle_dequant_threads(q, s, cores: int):
+    import concurrent.futures as cf
+
+    import oracle
+
+    ranges = block_row_ranges(q.shape[0], cores)
+    with cf.ThreadPoolExecutor(len(ranges)) as ex:
+        parts = list(ex.map(lambda r: oracle.weight_dequant(q[r[0]:r[1]], s[r[0] // 128:-(-r[1] // 128)]), ranges))
+    return np.concatenate(parts, axis=0)
+
+
+def oracle_linear_full(shape, cores: int):
+    """One full oracle step of the linear workload on `cores` host threads:
+    act_quant of all of X, then the fp64 GEMM over every weight row (the
+    weight is quantised once, outside the timed part). Returns (seconds,
+    algorithmic bytes)."""
+    import oracle
+
+    M, N, K = shape["M"], shape["N"], shape["K"]
+    key = ("full", M, N, K, shape["seed"])
+    if key not in _SAMPLE_CACHE:
+        x = synthetic.activations(M, K, shape["seed"], outlier_frac=shape["frac"])
+        w = synthetic.weights(N, K, shape["seed"] + 1)
+        _SAMPLE_CACHE[key] = (x,) + oracle.weight_quant(w)
+    x, wq, ws = _SAMPLE_CACHE[key]
+    t0 = time.perf_counter()
+    xq, xs = oracle.act_quant(x)
+    oracle_gemm_threads(xq, xs, wq, ws, cores)
+    return time.perf_counter() - t0, linear_bytes(M, N, K)
+
+
+def cpu_baseline(shape, kind, budget_s=5.0):
+    """The oracle (plain C, fp64) timed on this host's cores: the full decode
+    layer with its weight rows split over every core (the reported value),
+    the same layer single-threaded on a sample of rows, and one full run of
+    the oracle on the 16x320x256 workload, act_quant of the prefill input and
+    weight_dequant of an [18432, 7168] weight."""
     if kind != "linear":
         return None
+    import oracle
+
     M, N, K = shape["M"], shape["N"], shape["K"]
-    # size one sample to about 1-2 s: the oracle runs ~2.5e7 multiply-adds/s
-    n_cols = max(1, min(N, int(2.5e7 * 1.5 / (M * K))))
-    total_t, total_b, reps = 0.0, 0, 0
-    while total_t < budget_s or reps == 0:
+    cores = cpu_cores()
+    oracle_linear_full(shape, cores)                       # warm: inputs, library, threads
+    tt, tb, reps = 0.0, 0, 0
+    while tt < budget_s or reps == 0:
+        dt, b = oracle_linear_full(shape, cores)
+        tt, tb, reps = tt + dt, tb + b, reps + 1
+    allc = tb / tt / 1e9
+    # single-threaded, on a sample of weight rows sized to about 1 s per step
+    n_cols = max(1, min(N, int(4e7 / (M * K))))
+    st_t, st_b, st_reps = 0.0, 0, 0
+    while st_t < budget_s or st_reps == 0:
         dt, b = oracle_linear_sample(shape, n_cols)
-        total_t += dt
-        total_b += b
-        reps += 1
-    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x (act_quant of X[{M},{K}] + fp64 GEMM over {n_cols} of {N} weight rows), "
-                      f"{total_t:.1f} s single-threaded C"}
+        st_t, st_b, st_reps = st_t + dt, st_b + b, st_reps + 1
+    full = {}
+    x = synthetic.activations(16, 256, synthetic.SEED_PR1)
+    wq, ws = oracle.weight_quant(synthetic.weights(320, 256, synthetic.SEED_PR1))
+    t0 = time.perf_counter()
+    xq, xs = oracle.act_quant(x)
+    oracle.gemm(xq, xs, wq, ws)
+    full["pr1_linear_16x320x256 (1 thread)"] = time.perf_counter() - t0
+    x = synthetic.activations(4096, 7168, synthetic.SEED_PREFILL)
+    t0 = time.perf_counter()
+    oracle.act_quant(x)
+    full["act_quant_4096x7168 (1 thread)"] = time.perf_counter() - t0
+    del x
+    # every finite positive code, one power-of-two scale per block: dequant cost does not depend on values
+    q = np.random.default_rng(synthetic.SEED_ATTN).integers(0, 126, size=(18432, 7168), dtype=np.uint8)
+    s = np.full((144, 56), 2.0 ** -7, np.float32)
+    t0 = time.perf_counter()
+    oracle_dequant_threads(q, s, cores)
+    full[f"weight_dequant_18432x7168 ({cores} threads)"] = time.perf_counter() - t0
+    full[f"decode_linear_{M}x{N}x{K} ({cores} threads)"] = tt / reps
+    return {"value": allc, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x the full layer: act_quant of X[{M},{K}] + fp64 GEMM over all {N} weight rows "
+                      f"split over {cores} threads, {tt:.1f} s",
+            "single_thread": {"value": st_b / st_t / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{st_reps} x (act_quant of X[{M},{K}] + fp64 GEMM over {n_cols} of {N} "
+                                        f"weight rows), {st_t:.1f} s"},
+            "full_oracle_seconds": {k: round(v, 4) for k, v in full.items()},
+            "threads": "the C oracle unchanged, one call per range of 128-row weight blocks per host thread"}
 
 
 def run_reference(args, kind, shape, steps, warmup):
+    """The reference arm: the oracle on the host cores. Each step is the full
+    decode layer with its weight rows split over every core, or, when
+    warm-up + steps would take more than about a minute and a half that way,
+    a single-threaded sample of weight rows sized to fit."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
     if kind != "linear":
         print(json.dumps({"impl": "reference", "unavailable": "the oracle leg covers the linear workloads only"}))
         return 0
-    # size each step so that warm-up + steps take about a minute in all
     M, N, K = shape["M"], shape["N"], shape["K"]
-    per_step_s = 60.0 / max(1, steps + warmup)
-    n_cols = max(1, min(N, int(2.5e7 * per_step_s / (M * K))))
+    cores = cpu_cores()
+    oracle_linear_full(shape, cores)
+    probe, _ = oracle_linear_full(shape, cores)
+    full = probe * (steps + min(warmup, 3)) <= 90.0
+    if full:
+        def step():
+            return oracle_linear_full(shape, cores)
+        used = cores
+        sample = f"each step: the full layer, act_quant of X[{M},{K}] + fp64 GEMM over all {N} rows " \
+                 f"split over {cores} threads"
+    else:
+        per_step_s = 60.0 / max(1, steps + warmup)
+        n_cols = max(1, min(N, int(4e7 * per_step_s / (M * K))))
+
+        def step():
+            return oracle_linear_sample(shape, n_cols)
+        used = 1
+        sample = f"each step: act_quant of X[{M},{K}] + fp64 GEMM over {n_cols} of {N} rows, 1 thread"
     for _ in range(min(warmup, 3)):
-        oracle_linear_sample(shape, n_cols)
+        step()
     tt, tb = 0.0, 0
     for _ in range(steps):
-        dt, b = oracle_linear_sample(shape, n_cols)
+        dt, b = step()
         tt += dt
         tb += b
     val = tb / tt / 1e9
@@ -827,9 +976,9 @@ def run_reference(args, kind, shape, steps, warmup):
         "value": val, "unit": "GB/s", "impl": "reference", "n_gpus": 1, "steps": steps, "warmup": warmup,
         "ms_per_step": tt / steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "sample_cols": n_cols},
-        "cpu_baseline": {"value": val, "unit": "GB/s", "kind": "oracle", "cores": 1,
-                         "sample": f"each step: act_quant of X[{M},{K}] + fp64 GEMM over {n_cols} of {N} rows"},
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K,
+                   "sample": "full layer" if full else "sampled weight rows"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "kind": "oracle", "cores": used, "sample": sample},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -837,6 +986,35 @@ def run_reference(args, kind, shape, steps, warmup):
 
 
 # ---------------------------------------------------------------------------
+
+# Measured after the default workload and reported under "other_workloads":
+# the TFLOP/s half of the metric (the prefill GEMM, both scale formats) and
+# the MoE step (both scale formats), each a short run of its own.
+OTHER_WORKLOADS = ("prefill_gemm_w1", "prefill_gemm_w1_ue8m0", "moe_t4096_uniform", "moe_t4096_uniform_ue8m0")
+
+
+def run_other_workloads(args, dev, torch, fb, peaks, steps=20, warmup=3):
+    out = {}
+    runners = {"linear": run_linear, "moe": run_moe, "ffn": run_ffn}
+    for name in OTHER_WORKLOADS:
+        if name == args.workload:
+            continue
+        kind, shape = WORKLOADS[name]
+        sub = argparse.Namespace(**dict(vars(args), workload=name, no_e2e=True))
+        r = runners[kind](sub, shape, dev, torch, fb, peaks, steps, warmup, 0, 1)
+        roof = r["roofline"]
+        out[name] = {"value": r["value"], "unit": r["unit"], "ms_per_step": r["ms_per_step"], "steps": steps,
+                     "warmup": warmup, "clocks": r["clocks"],
+                     "roofline": {k: roof.get(k) for k in ("bound", "kernel", "achieved", "peak", "unit", "frac",
+                                                           "kernel_us", "traffic")},
+                     "config": r["config"]}
+        if "tflops" in r:
+            out[name]["tflops"] = r["tflops"]
+        del r
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
 
 def reaches_cluster_multicast(kind, shape) -> bool:
     """True if the workload can run a GEMM kernel that loads with TMA
@@ -895,6 +1073,9 @@ def main():
         res = run_mla(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
     else:
         res = run_dequant(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world)
+    other = None
+    if world == 1 and not args.no_other and args.workload == DEFAULT:
+        other = run_other_workloads(args, dev, torch, fb, peaks)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(shape, kind)
@@ -911,6 +1092,8 @@ def main():
         for extra in ("kernels_us", "tflops"):
             if extra in res:
                 line[extra] = res[extra]
+        if other is not None:
+            line["other_workloads"] = other
         print(json.dumps(line))
     if world > 1:
         dist.barrier()

@@ -42,6 +42,7 @@ void init_device(int dev) {
   d.cc_major = prop.major;
   d.cc_minor = prop.minor;
   d.smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+  d.smem_per_sm = static_cast<int>(prop.sharedMemPerMultiprocessor);
   if (prop.major != 10 || prop.minor != 3) {
     g_status[dev] = FP8BLK_ERR_ARCH;
     return;

@@ -99,6 +99,8 @@ struct GemmParams {
   int whole_tiles;     // > 0: that many whole tiles, round-robin over the CTAs (no stream-K)
   int ksplit;          // > 1: clusters of ksplit CTAs share one tile, each a K slice, reduced in DSMEM
   const __nv_bfloat16* x;  // fused decode linear: the bf16 activation [M, Kb * 128]
+  int lane_rows;       // swapped tiles: weight rows per tile (128, or fewer for weight slices)
+  int l2_ahead;        // swapped tiles: K blocks past the stage ring prefetched into L2 before the dependency wait
   int trace_id;        // phase-trace builds only: which of 8 trace slots this launch fills
 };
 
@@ -180,17 +182,13 @@ constexpr int pow2_at_least(int v, int floor_) {
   return p;
 }
 
-#ifndef FP8BLK_DECODE_L2_AHEAD
-#define FP8BLK_DECODE_L2_AHEAD 0
-#endif
-
 // TMEM columns per load (and per wait) in the register-split epilogue.
 #ifndef FP8BLK_SPLIT_LD
 #define FP8BLK_SPLIT_LD 64
 #endif
 
 template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_, int MODE_ = kEpiBf16, bool GROUPED_ = false,
-          bool FUSED_ = false, int CLUSTER_ = 1, bool MX_ = false>
+          bool FUSED_ = false, int CLUSTER_ = 1, bool MX_ = false, int LROWS_ = 128>
 struct Cfg {
   // MX: power-of-two (UE8M0) scales applied by the tensor core itself
   // (tcgen05.mma kind::mxf8f6f4.block_scale). The scale of a K block is the
@@ -241,18 +239,24 @@ struct Cfg {
   // MX scale ring: slots of 16 TMEM columns after the accumulator, 4 K blocks each.
   static constexpr int kSfSlots = MX ? 8 : 0;
   static constexpr int kSfCol0 = P * BN;
-  static constexpr int kABytes = 128 * 128;
+  // Weight slices (swapped tiles of fewer than 128 weight rows): a stage holds
+  // LROWS weight rows. The MMA still has M = 128 and reads 128 rows from the
+  // stage's start, past its weight rows; the lanes beyond the slice compute
+  // values nobody reads. Two such CTAs fit on one SM, so the next launch's
+  // CTAs start streaming their weights while this launch runs.
+  static constexpr int kLRows = SWAP ? LROWS_ : 128;
+  static constexpr int kABytes = kLRows * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = FUSED ? kABytes : kABytes + kBBytes;
-  // Decode tiles: weight chunks beyond the stage ring that are prefetched into
-  // L2 before the dependency wait, so the whole weight tile streams from DRAM
-  // while the previous kernel finishes.
-  static constexpr int kL2Ahead = SWAP ? FP8BLK_DECODE_L2_AHEAD : 0;
+  // Bytes after the ring that the last stage's 128-row MMA read may reach.
+  static constexpr int kRingPad = (kLRows < 128 && kStageBytes < 128 * 128) ? 128 * 128 - kStageBytes : 0;
+  static constexpr int kRingBytes = STAGES * kStageBytes + kRingPad;
+  static constexpr int kMinBlocks = kLRows < 128 ? 2 : 1;
   static constexpr int kTmemCols = pow2_at_least(P * BN + 16 * kSfSlots, 32);
   static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16 + (2 * kSfSlots + (MX ? 1 : 0)) * 8;
   // MX: the scale writers' exchange of activation-row scale words, double-buffered.
   static constexpr int kSfxBytes = MX ? 2 * 128 * 4 : 0;
-  static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + kGroupBytes + kXchgBytes + kSfxBytes;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kGroupBytes + kXchgBytes + kSfxBytes;
 
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(MODE == kEpiBf16 || !SWAP, "SwiGLU and scatter epilogues use activation rows as lanes");
@@ -274,6 +278,8 @@ struct Cfg {
   static_assert(CLUSTER == 1 || (CLUSTER == 2 && !SWAP && !GROUPED && !FUSED && BN == 256),
                 "clusters pair the 128-row lane tiles of dense large-M GEMMs");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kLRows % 8 == 0 && kLRows >= 8 && kLRows <= 128, "whole 8-row swizzle atoms per stage");
+  static_assert(kLRows == 128 || (SWAP && !GROUPED && CLUSTER == 1), "weight slices: swapped decode tiles");
 };
 
 // Where one output tile lives.
@@ -314,9 +320,10 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
     const int tl = (tile % p.tiles_lane) * C::CLUSTER + rank, tc = tile / p.tiles_lane;
     t.lane_y = tl * 128;
     if constexpr (C::SWAP) {
-      t.lane_valid = min(128, p.N - t.lane_y);
+      t.lane_y = tl * p.lane_rows;  // weight rows: 128-row tiles or slices of lane_rows
+      t.lane_valid = min(p.lane_rows, p.N - t.lane_y);
       t.col_y = tc * C::BN;
-      t.wblock = tl;
+      t.wblock = t.lane_y / 128;
       t.col0 = tc * C::BN;
     } else {
       t.lane_valid = min(128, p.M - t.lane_y);
@@ -355,7 +362,7 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
                                          int row, float* xchg, uint32_t unit_parity, Sync&& epi_sync) {
   if constexpr (C::SWAP) {
     const int n = t.lane_y + row;
-    if (n >= p.N) return true;
+    if (row >= t.lane_valid) return true;  // a slice's lanes past its rows (or rows past N)
 #pragma unroll
     for (int j = 0; j < C::kCpt; ++j) {
       const int m = t.col0 + j;
@@ -463,14 +470,14 @@ __host__ __device__ constexpr size_t fused_extra_bytes(int Kb, int BN) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::kThreads, 1)
+__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_lane, const __grid_constant__ CUtensorMap tmap_col,
                     const __grid_constant__ CUtensorMap tmap_col2, const GemmParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
   // Fused decode: the quantised activation (all K blocks, BN token rows each,
   // 128-byte swizzled like a TMA tile) and its scales follow the stage ring.
-  uint8_t* act_smem = smem + C::STAGES * C::kStageBytes;
+  uint8_t* act_smem = smem + C::kRingBytes;
   float* act_scale = reinterpret_cast<float*>(act_smem + static_cast<size_t>(prm.Kb) * C::BN * 128);
   uint8_t* tail = act_smem + (C::FUSED ? fused_extra_bytes(prm.Kb, C::BN) : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(tail);
@@ -501,6 +508,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int krank = ksplit > 1 ? static_cast<int>(blockIdx.x) % ksplit : 0;
   const int worker = static_cast<int>(blockIdx.x) / (ksplit > 1 ? ksplit : C::CLUSTER);
   if (threadIdx.x == 0) FP8BLK_STAMP(0);
+#ifdef FP8BLK_TRACE
+  if (threadIdx.x == 0) {
+    unsigned sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    FP8BLK_PUT(26, sm);
+  }
+#endif
   // The next kernel on the stream may begin its prologue (and its weight
   // loads) now; it waits for this one before touching anything we write.
   griddep_launch_dependents();
@@ -592,22 +606,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if constexpr (C::SWAP) tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, t.col_y);
         else tma_load_2d(sa, &tmap_lane, &full[st], kb * 128, t.lane_y);
       };
+      // Bytes a stage receives: a weight slice has lane_rows rows (the TMA box).
+      const uint32_t stage_tx =
+          C::SWAP ? static_cast<uint32_t>(prm.lane_rows * 128 + (C::FUSED ? 0 : C::kBBytes)) : C::kStageBytes;
       // Weights do not depend on the previous kernel on the stream: the first
-      // STAGES stages start loading them before the dependency wait; the
-      // activations follow once the previous kernel has completed.
+      // STAGES stages start loading them before the dependency wait, and the
+      // next l2_ahead K blocks are prefetched into L2; the activations follow
+      // once the previous kernel has completed.
+      const int l2_ahead = C::SWAP ? prm.l2_ahead : 0;
       int npre = 0;
       if constexpr (!C::GROUPED) {
         Sched pre(prm, worker, -1, krank);
         Unit u;
         int nl2 = 0;
-        while ((npre < C::STAGES || nl2 < C::kL2Ahead) && pre.next(u)) {
+        while ((npre < C::STAGES || nl2 < l2_ahead) && pre.next(u)) {
           const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
           for (int kb = u.kb0; kb < u.kb1; ++kb) {
             if (npre < C::STAGES) {
-              mbar_arrive_expect_tx(&full[npre], C::kStageBytes);
+              mbar_arrive_expect_tx(&full[npre], stage_tx);
               load_weights(npre, t, kb);
               ++npre;
-            } else if (nl2 < C::kL2Ahead) {
+            } else if (nl2 < l2_ahead) {
               if constexpr (C::SWAP) tma_prefetch_l2_2d(&tmap_lane, kb * 128, t.lane_y);
               ++nl2;
             } else {
@@ -639,7 +658,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               break;
             }
             FP8BLK_TOC(tw_empty, t0);
-            mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+            mbar_arrive_expect_tx(&full[st], stage_tx);
             load_weights(st, t, kb);
             load_acts(st, t, kb);
 #ifdef FP8BLK_TRACE
@@ -1050,7 +1069,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if (C::GROUPED || nb < prm.n_wblocks) r.w = __ldg(prm.w_s + static_cast<size_t>(nb) * prm.Kb + kb);
         }
       } else {
-        r.w = __ldg(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + kb);
+        // This lane's weight row: a slice can straddle two 128-row scale blocks.
+        const int n = t.lane_y + row;
+        if (n < prm.N) r.w = __ldg(prm.w_s + static_cast<size_t>(n >> 7) * prm.Kb + kb);
         if constexpr (!C::FUSED) {
 #pragma unroll
           for (int i = 0; i < kColRegs; ++i) {
@@ -1112,7 +1133,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int d = 0; d + 1 < kAhead; ++d) pipe[d] = pipe[d + 1];
         pipe[kAhead - 1] = load_scales(t, kb + kAhead, u.kb1);
         float sc_lo = 0.0f, sc_hi = 0.0f;
+        // Swapped tiles: sc_col[i] is the activation scale of token lane + 32 i
+        // (shuffled to the thread that owns each column), w_row this thread's
+        // own weight-row scale (rows of a slice can lie in two scale blocks).
         float sc_col[kAsRegs];
+        const float w_row = cur.w;
         if constexpr (!C::SWAP) {
           sc_lo = cur.a * cur.w;
           sc_hi = C::MODE == kEpiSwiGLU ? cur.a * cur.w3 : sc_lo;
@@ -1121,9 +1146,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int i = 0; i < kAsRegs; ++i) {
             const int j = lane + 32 * i;
             if constexpr (C::FUSED)
-              sc_col[i] = (j < C::kCpt) ? act_scale[kb * C::BN + j] * cur.w : 0.0f;
+              sc_col[i] = (j < C::kCpt) ? act_scale[kb * C::BN + j] : 0.0f;
             else
-              sc_col[i] = cur.col[i < kColRegs ? i : 0] * cur.w;
+              sc_col[i] = cur.col[i < kColRegs ? i : 0];
           }
         }
         FP8BLK_TIC(t0);
@@ -1188,7 +1213,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const float sc_h = (ch < C::kCpt / 32) ? sc_lo : sc_hi;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float sc = C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[(ch * 16 + i) / 32], (ch * 16 + i) % 32) : sc_h;
+              const float sc =
+                  C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[(ch * 16 + i) / 32], (ch * 16 + i) % 32) * w_row : sc_h;
               acc[ch * 16 + i] = fmaf(__uint_as_float(v[i]), sc, acc[ch * 16 + i]);
             }
           }
@@ -1200,7 +1226,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const float sc_h = (ch < C::kCpt / 64) ? sc_lo : sc_hi;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float sc = C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[ch], i) : sc_h;
+              const float sc = C::SWAP ? __shfl_sync(0xFFFFFFFFu, sc_col[ch], i) * w_row : sc_h;
               acc[ch * 32 + i] = fmaf(__uint_as_float(v[i]), sc, acc[ch * 32 + i]);
             }
           }
@@ -1384,6 +1410,15 @@ using CfgS32 = Cfg<32, true, (FP8BLK_DECODE_STAGES > 10 ? 10 : FP8BLK_DECODE_STA
 #endif
 using CfgS64 = Cfg<64, true, FP8BLK_S64_STAGES, 4, 4>;
 using CfgS128 = Cfg<128, true, 6, 4, 4>;
+// Weight slices for decode-sized M: up to kSliceRows weight rows per CTA and
+// all of K, one CTA per SM, stages small enough for two CTAs per SM.
+#ifndef FP8BLK_SLICES
+#define FP8BLK_SLICES 1
+#endif
+constexpr int kSliceRows = 80;
+using CfgSl16 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
+using CfgSl32 = Cfg<32, true, 7, 8, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
+using CfgSl64 = Cfg<64, true, 6, 4, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
 // Fused w1/w3 GEMM with the SwiGLU + act_quant epilogue (dense and grouped),
 // and the grouped GEMM whose rows are scattered back to token order.
 using CfgSwiGLU = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false>;
@@ -1406,11 +1441,16 @@ bool mx_for(int scale_fmt) { return scale_fmt_mx(scale_fmt); }
 // Decode linear with the act_quant fused in (M <= 16): weights-only stages.
 using CfgF16S8 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, true>;
 using CfgF16S4 = Cfg<16, true, 4, 8, 4, kEpiBf16, false, true>;
+using CfgF16Sl = Cfg<16, true, 6, 8, 4, kEpiBf16, false, true, 1, false, kSliceRows>;
 constexpr int kMaxDynSmem = 232448;
+#ifndef FP8BLK_SMEM_CARVEOUT
+#define FP8BLK_SMEM_CARVEOUT 100  // percent of the unified L1 / shared memory (-1: the driver's choice)
+#endif
 
 struct Plan {
   int bn;
   bool swap;
+  int lane_rows;  // swapped tiles: weight rows per tile (128, or a slice of 48..kSliceRows)
   int cluster;  // CTAs per schedule worker (2: lane-tile pairs); grid counts workers
   int ksplit;   // > 1: split-K clusters of that many CTAs per tile; grid counts CTAs
   int tiles_lane, tiles_col;
@@ -1465,9 +1505,24 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, 
   Plan pl{};
   pl.cluster = 1;
   pl.ksplit = 1;
+  pl.lane_rows = 128;
   if (M <= 128) {
     pl.swap = true;
     pl.bn = swap_bn(M);
+    // Weight slices: one CTA per SM, each an equal slice of 48..kSliceRows
+    // weight rows over all of K (so no SM idles, as 128-row tiles would leave
+    // some when N / 128 is below the SM count, and no partial sums to fix up).
+    if (FP8BLK_SLICES && pl.bn <= 64) {
+      const int64_t rows = ((N + sm_count - 1) / sm_count + 7) / 8 * 8;
+      if (rows >= 48 && rows <= kSliceRows) {
+        pl.lane_rows = static_cast<int>(rows);
+        pl.tiles_lane = static_cast<int>((N + rows - 1) / rows);
+        pl.tiles_col = 1;
+        pl.grid = pl.tiles_lane;
+        pl.whole_tiles = pl.tiles_lane;
+        return pl;
+      }
+    }
     pl.tiles_lane = static_cast<int>((N + 127) / 128);
     pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
     const long long tiles = static_cast<long long>(pl.tiles_lane) * pl.tiles_col;
@@ -1534,12 +1589,14 @@ Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count, int pai
 
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
-// Workspace: the counter region (one arrival counter per output tile), then
-// two partial slots per CTA.
+// Workspace: the counter region (one arrival counter per output tile), then,
+// for plans that cut tiles stream-K, two partial slots per CTA. Plans of whole
+// tiles, weight slices or split-K clusters write no partial sums to memory.
 size_t plan_counter_bytes(const Plan&) { return kCounterBytes; }
 
 size_t plan_workspace(const Plan& pl) {
-  return plan_counter_bytes(pl) + static_cast<size_t>(2) * pl.grid * pl.cluster * pl.bn * 128 * sizeof(float);
+  const size_t slots = pl.sk_tiles > 0 ? static_cast<size_t>(2) * pl.grid * pl.cluster * pl.bn * 128 * sizeof(float) : 0;
+  return plan_counter_bytes(pl) + slots;
 }
 
 template <class C>
@@ -1550,6 +1607,13 @@ int launch(const DevInfo* d, const CUtensorMap& ml, const CUtensorMap& mc, const
   const int smem_attr = C::FUSED ? kMaxDynSmem : C::kSmemBytes;
   if (d->device >= 64 || !attr_done[d->device]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_attr) != cudaSuccess)
+      return FP8BLK_ERR_CUDA;
+    // All of the unified L1 / shared memory as shared memory: the kernels
+    // stage through shared memory, and a CTA of the next launch can then sit
+    // beside a running one wherever their shared memory fits.
+    if (FP8BLK_SMEM_CARVEOUT >= 0 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, FP8BLK_SMEM_CARVEOUT) !=
+            cudaSuccess)
       return FP8BLK_ERR_CUDA;
     if constexpr (C::kSplitRegs) {
       // setmaxnreg.inc would wait forever if the build gave the kernel fewer
@@ -1704,6 +1768,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
 
   GemmParams prm{};
+  prm.lane_rows = 128;
   prm.a_s = a_s;
   prm.w_s = w_s;
   prm.c = static_cast<__nv_bfloat16*>(c);
@@ -1732,7 +1797,8 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   const uint64_t col_rows = static_cast<uint64_t>(pl.swap ? M : N);
   // Cluster pairs load the column tile in two 128-row halves.
   const uint32_t col_box = static_cast<uint32_t>(pl.cluster == 2 ? 128 : pl.bn);
-  if (!make_kmajor_map(&ml, lane_src, lane_rows, static_cast<uint64_t>(K), 128) ||
+  prm.lane_rows = pl.lane_rows;
+  if (!make_kmajor_map(&ml, lane_src, lane_rows, static_cast<uint64_t>(K), static_cast<uint32_t>(pl.lane_rows)) ||
       !make_kmajor_map(&mc, col_src, col_rows, static_cast<uint64_t>(K), col_box))
     return FP8BLK_ERR_CUDA;
 
@@ -1743,6 +1809,14 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     if (pl.bn == 256)
       return mx ? launch<CfgN256MX>(d, ml, mc, mc, prm, stream) : launch<CfgN256>(d, ml, mc, mc, prm, stream);
     return launch<CfgN128E8>(d, ml, mc, mc, prm, stream);
+  }
+  if (pl.lane_rows < 128) {
+    prm.l2_ahead = prm.Kb;  // every K block past the stage ring
+    switch (pl.bn) {
+      case 16: return launch<CfgSl16>(d, ml, mc, mc, prm, stream);
+      case 32: return launch<CfgSl32>(d, ml, mc, mc, prm, stream);
+      default: return launch<CfgSl64>(d, ml, mc, mc, prm, stream);
+    }
   }
   switch (pl.bn) {
     case 16: return launch<CfgS16>(d, ml, mc, mc, prm, stream, 0, pl.ksplit);
@@ -1774,11 +1848,17 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
   if (int st = current_device(&d)) return st;
   const int Kb = static_cast<int>(K / kBlock);
   const size_t extra = fused_extra_bytes(Kb, 16);
-  const int variant = CfgF16S8::kSmemBytes + extra <= kMaxDynSmem   ? 0   // 8 weight stages
+  // Weight slices (as make_plan picks them) when two such CTAs fit on an SM.
+  const int64_t slice = ((N + d->sm_count - 1) / d->sm_count + 7) / 8 * 8;
+  const bool slices = FP8BLK_SLICES && slice >= 48 && slice <= kSliceRows &&
+                      2 * (CfgF16Sl::kSmemBytes + extra + 1024) <= static_cast<size_t>(d->smem_per_sm);
+  const int variant = slices                                          ? 2   // slices, 6 weight stages
+                      : CfgF16S8::kSmemBytes + extra <= kMaxDynSmem   ? 0   // 8 weight stages
                       : CfgF16S4::kSmemBytes + extra <= kMaxDynSmem ? 1   // 4 weight stages
                                                                     : -1;
   if (variant < 0) return FP8BLK_OK;
   GemmParams prm{};
+  prm.lane_rows = 128;
   prm.w_s = w_s;
   prm.c = static_cast<__nv_bfloat16*>(y);
   prm.x = static_cast<const __nv_bfloat16*>(x);
@@ -1793,11 +1873,20 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
   prm.whole_tiles = prm.n_wblocks;
   prm.grid = prm.n_wblocks < d->sm_count ? prm.n_wblocks : d->sm_count;
   prm.ue8m0 = scale_fmt_ue8m0(scale_fmt);
+  if (variant == 2) {
+    prm.lane_rows = static_cast<int>(slice);
+    prm.tiles_lane = static_cast<int>((N + slice - 1) / slice);
+    prm.whole_tiles = prm.tiles_lane;
+    prm.grid = prm.tiles_lane;
+    prm.l2_ahead = Kb;
+  }
   CUtensorMap ml;
-  if (!make_kmajor_map(&ml, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128)) return FP8BLK_ERR_CUDA;
+  if (!make_kmajor_map(&ml, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint32_t>(prm.lane_rows)))
+    return FP8BLK_ERR_CUDA;
   *used = true;
-  return variant == 0 ? launch<CfgF16S8>(d, ml, ml, ml, prm, stream, extra)
-                      : launch<CfgF16S4>(d, ml, ml, ml, prm, stream, extra);
+  return variant == 2   ? launch<CfgF16Sl>(d, ml, ml, ml, prm, stream, extra)
+         : variant == 0 ? launch<CfgF16S8>(d, ml, ml, ml, prm, stream, extra)
+                        : launch<CfgF16S4>(d, ml, ml, ml, prm, stream, extra);
 }
 
 size_t swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t K) {
@@ -1826,6 +1915,7 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
   if (!workspace || workspace_bytes < plan_workspace(pl)) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   GemmParams prm{};
+  prm.lane_rows = 128;
   prm.a_s = xs;
   prm.w_s = w1s;
   prm.w3_s = w3s;
@@ -1868,6 +1958,7 @@ int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const f
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
   GemmParams prm{};
+  prm.lane_rows = 128;
   prm.a_s = xgs;
   prm.w_s = w1s;
   prm.w3_s = w3s;
@@ -1901,6 +1992,7 @@ int grouped_scatter_run(const void* uq, const float* us, const void* w2, const f
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
   GemmParams prm{};
+  prm.lane_rows = 128;
   prm.a_s = us;
   prm.w_s = w2s;
   prm.c = static_cast<__nv_bfloat16*>(out);

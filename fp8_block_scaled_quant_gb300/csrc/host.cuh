@@ -18,6 +18,7 @@ struct DevInfo {
   int cc_major;
   int cc_minor;
   int smem_optin;      // max dynamic shared memory per block (opt-in)
+  int smem_per_sm;     // shared memory per SM (all resident blocks together)
   unsigned* err_word;  // device address of this device's error word
 };
 

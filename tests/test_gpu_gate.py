@@ -6,7 +6,9 @@ computes the scores in fp64 and rounds them to fp32 once. The two therefore
 agree on every token except at near-ties, where two experts' keys differ by
 a few fp32 ulps. Such tokens are checked for validity instead: position by
 position, the keys of the kernel's experts must equal the oracle's within
-1e-5 (the fp32 rounding of the scores). They must also be rare. Weights are
+1e-5 (the fp32 rounding of the scores), and with group-limited routing every
+chosen expert must come from a kept group (the best topk_groups groups, up to
+a tie at the cut within fp32 noise). Such tokens must also be rare. Weights are
 compared wherever the ids agree: within 4e-6 relative for sigmoid scores (a
 few roundings of fp32 operations), and within 2e-5 for softmax scores, whose
 fp32 sum over the E experts carries up to E roundings."""
@@ -41,6 +43,13 @@ def keys(l, b, sigmoid):
     return s + b if b is not None else s
 
 
+def group_scores(z, G, bias):
+    """[T, G]: a group's largest key (no bias) or the sum of its two largest (bias)."""
+    T, E = z.shape
+    zg = np.sort(z.reshape(T, G, E // G).astype(np.float64), axis=2)
+    return zg[:, :, -2:].sum(axis=2) if bias else zg[:, :, -1]
+
+
 @pytest.mark.parametrize("T,E,G,TG,k,sigmoid,use_bias,scale,norm", CASES)
 def test_gate_matches_oracle(T, E, G, TG, k, sigmoid, use_bias, scale, norm):
     l = synthetic.gate_logits(T, E, synthetic.SEED_GATE + E)
@@ -53,11 +62,20 @@ def test_gate_matches_oracle(T, E, G, TG, k, sigmoid, use_bias, scale, norm):
     idx, w = idx.cpu().numpy(), w.cpu().numpy()
     same = np.all(idx == want_idx, axis=1)
     z = keys(l, b, sigmoid)
+    gs = group_scores(z, G, b is not None) if G > 1 else None
     for t in np.nonzero(~same)[0]:
         got_z = z[t, idx[t].astype(np.int64)]
         ref_z = z[t, want_idx[t].astype(np.int64)]
         assert len(set(idx[t].tolist())) == k
         assert np.allclose(got_z, ref_z, rtol=0, atol=1e-5), f"token {t}: {idx[t]} vs {want_idx[t]}"
+        if gs is not None:
+            # every chosen expert lies in a kept group: one of the TG best groups
+            # (the oracle's own, or one whose score ties the cut within fp32 noise)
+            kept = set(np.argsort(-gs[t], kind="stable")[:TG].tolist())
+            cut = np.sort(gs[t])[::-1][TG - 1]
+            for e in idx[t]:
+                g = int(e) // (E // G)
+                assert g in kept or gs[t, g] >= cut - 2e-5, f"token {t}: expert {e} from a dropped group"
     assert (~same).sum() <= max(1, T // 500)
     assert np.allclose(w[same], want_w[same], rtol=4e-6 if sigmoid else 2e-5, atol=0)
     assert fb.last_device_error() == 0

@@ -3,11 +3,12 @@ against the CPU oracle ("Administrator & Developer Guide", 6.4 and 8.4; 1.2
 MLP / Expert).
 
 - The routing permutation is integer work: bit-exact.
-- The fused w1/w3 GEMM's e4m3 output is checked structurally against the
-  oracle chain. Its codes and scales match in all but a few elements: one
-  bf16 step of silu or of the fp32 accumulation can flip a code.
-- The chains (dense FFN, MoE) are graded on their final output with the GEMM
-  tolerance |diff| <= 2^-7 |ref| + 1e-3 rms(ref)."""
+- The fused w1/w3 GEMM's e4m3 output: every scale and code lies in the
+  interval the oracle's fp64 h1, h3 admit (helpers: rules 1-4), and every
+  block's largest code matches its own scale.
+- The chains (dense FFN, MoE) are graded on every output element with the
+  GEMM tolerance |diff| <= 2^-7 |ref| + 1e-3 rms(ref) plus the exact change
+  the admissible intermediates permit."""
 import numpy as np
 import pytest
 import torch
@@ -15,8 +16,8 @@ import torch
 import fp8_block_scaled_quant_gb300 as fb
 import oracle
 import synthetic
-from helpers import (assert_chain_close, assert_gemm_close, bits_to_dev_bf16, dequant_weight, dev_to_bits,
-                     flip_allowance)
+from helpers import (admissible_quant, admissible_u, assert_chain_close, assert_gemm_close, assert_quant_admissible,
+                     bits_to_dev_bf16, dequant_weight, dev_to_bits, ffn_chain_allowance)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,10 +59,6 @@ def test_moe_permute_invalid_ids_reported_and_skipped():
 
 # ---- A4: fused w1/w3 GEMM with SwiGLU + act_quant --------------------------------
 
-def oracle_u(xq, xs, w1q, w1s, w3q, w3s, ue8m0=False):
-    h1 = oracle.bf16_round(oracle.gemm(xq, xs, w1q, w1s))
-    h3 = oracle.bf16_round(oracle.gemm(xq, xs, w3q, w3s))
-    return oracle.act_quant(oracle.swiglu(h1, h3), ue8m0)
 
 
 @pytest.mark.parametrize("M,dim,inter", [(5, 256, 384), (130, 512, 256), (300, 256, 1024)])
@@ -77,15 +74,10 @@ def test_swiglu_gemm_matches_oracle_chain(M, dim, inter, fmt):
     w1q, w1s = oracle.weight_quant(synthetic.weights(inter, dim, 601 + M), ue)
     w3q, w3s = oracle.weight_quant(synthetic.weights(inter, dim, 602 + M), ue)
     u, us = fb.swiglu_gemm(to_dev_q(xq), to_dev(xs), to_dev_q(w1q), to_dev(w1s), to_dev_q(w3q), to_dev(w3s), fmt)
-    uo, uso = oracle_u(xq, xs, w1q, w1s, w3q, w3s, ue)
-    got_q, got_s = dev_to_bits(u), us.cpu().numpy()
-    assert (got_s == uso).mean() > 0.98
-    assert (got_q == uo).mean() > 0.995
-    # dequantised u agrees with the oracle's to a few e4m3 steps everywhere
-    dq = oracle.e4m3_decode_array(got_q) * np.repeat(got_s.astype(np.float64), 128, axis=1)
-    dqo = oracle.e4m3_decode_array(uo) * np.repeat(uso.astype(np.float64), 128, axis=1)
-    scale = np.repeat(uso.astype(np.float64), 128, axis=1)
-    assert np.all(np.abs(dq - dqo) <= 2.0 ** -2 * np.abs(dqo) + 2 * scale * 2.0 ** -6)
+    H1 = oracle.gemm(xq, xs, w1q, w1s)
+    H3 = oracle.gemm(xq, xs, w3q, w3s)
+    adm = admissible_quant(*admissible_u(H1, H3), ue)
+    assert_quant_admissible(dev_to_bits(u), us.cpu().numpy(), adm, ue, what=f"swiglu {M}x{dim}x{inter}")
 
 
 # ---- A4 chain: dense FFN ---------------------------------------------------------
@@ -103,7 +95,7 @@ def test_ffn_full_compare(M, dim, inter):
     y = fb.ffn(bits_to_dev_bf16(x), to_dev_q(w1q), to_dev(w1s), to_dev_q(w3q), to_dev(w3s), to_dev_q(w2q),
                to_dev(w2s))
     ref, uq, us = oracle.ffn_rows(xq, xs, w1q, w1s, w3q, w3s, w2q, w2s, range(M), return_u=True)
-    allow = flip_allowance(uq, us, dequant_weight(w2q, w2s))
+    allow = ffn_chain_allowance(xq, xs, w1q, w1s, w3q, w3s, dequant_weight(w2q, w2s), uq, us)
     assert_chain_close(dev_to_bits(y), ref, allow, what=f"ffn {M}x{dim}x{inter}")
     # repeated call: workspaces were left clean
     y2 = fb.ffn(bits_to_dev_bf16(x), to_dev_q(w1q), to_dev(w1s), to_dev_q(w3q), to_dev(w3s), to_dev_q(w2q),
@@ -151,9 +143,10 @@ def test_ffn_full_size_sampled_rows():
     for (q, s), (qo, so) in zip(qs, host_q):
         assert np.array_equal(dev_to_bits(q), qo) and np.array_equal(s.cpu().numpy(), so)
     ref, uq, us = oracle.ffn_rows(xq, xs, *host_q[0], *host_q[1], *host_q[2], range(2), return_u=True)
-    allow = flip_allowance(uq, us, dequant_weight(*host_q[2]))
-    rms = float(y.float().pow(2).mean().sqrt())
-    assert_chain_close(dev_to_bits(y)[rows], ref, allow, rms=rms, what="ffn sampled rows")
+    allow = ffn_chain_allowance(xq, xs, *host_q[0], *host_q[1], dequant_weight(*host_q[2]), uq, us)
+    # the tolerance's rms term from the oracle's own rows (an estimate of the whole output's rms)
+    assert_chain_close(dev_to_bits(y)[rows], ref, allow, rms=float(np.sqrt(np.mean(ref ** 2))),
+                       what="ffn sampled rows")
 
 
 # ---- A6/A7: routed experts ----------------------------------------------------------
@@ -172,27 +165,30 @@ def moe_reference(p, tokens, E, ue8m0=False, wdeq_cache=None):
     """The oracle's MoE output rows (fp64 of its bf16 result) and the chain
     allowance: for each slot j, |w_j| times (one bf16 step of the expert output
     o_j, which a different fp32 summation may round the other way, plus the
-    expert's two-flip allowance)."""
+    expert's admissible-intermediate allowance)."""
     xq, xs, idx, wts, w1q, w1s, w3q, w3s, w2q, w2s = p
     dim = xq.shape[1]
     inter = w2q.shape[1]
     bi, bd = inter // 128, dim // 128
+    tokens = list(tokens)
     ref = synthetic.bf16_bits_to_f32(oracle.moe_tokens(*p, tokens, ue8m0=ue8m0)).astype(np.float64)
     allow = np.zeros((len(tokens), dim))
     cache = {} if wdeq_cache is None else wdeq_cache
-    for i, t in enumerate(tokens):
-        for j in range(idx.shape[1]):
-            e = int(idx[t, j])
-            if not 0 <= e < E:
-                continue
-            o, uq, us = oracle.ffn_rows(xq[t:t + 1], xs[t:t + 1],
-                                        w1q[e * inter:(e + 1) * inter], w1s[e * bi:(e + 1) * bi],
-                                        w3q[e * inter:(e + 1) * inter], w3s[e * bi:(e + 1) * bi],
-                                        w2q[e * dim:(e + 1) * dim], w2s[e * bd:(e + 1) * bd], [0],
-                                        ue8m0=ue8m0, return_u=True)
-            if e not in cache:
-                cache[e] = dequant_weight(w2q[e * dim:(e + 1) * dim], w2s[e * bd:(e + 1) * bd])
-            allow[i] += abs(float(wts[t, j])) * (2.0 ** -7 * np.abs(o[0]) + flip_allowance(uq, us, cache[e])[0])
+    pos = {t: i for i, t in enumerate(tokens)}
+    for e in range(E):
+        slots = [(t, j) for t in tokens for j in range(idx.shape[1]) if idx[t, j] == e]
+        if not slots:
+            continue
+        rows = np.array([t for t, _ in slots])
+        we = (w1q[e * inter:(e + 1) * inter], w1s[e * bi:(e + 1) * bi], w3q[e * inter:(e + 1) * inter],
+              w3s[e * bi:(e + 1) * bi])
+        w2e = (w2q[e * dim:(e + 1) * dim], w2s[e * bd:(e + 1) * bd])
+        o, uq, us = oracle.ffn_rows(xq[rows], xs[rows], *we, *w2e, range(len(rows)), ue8m0=ue8m0, return_u=True)
+        if e not in cache:
+            cache[e] = dequant_weight(*w2e)
+        al = ffn_chain_allowance(xq[rows], xs[rows], *we, cache[e], uq, us, ue8m0)
+        for r, (t, j) in enumerate(slots):
+            allow[pos[t]] += abs(float(wts[t, j])) * (2.0 ** -7 * np.abs(o[r]) + al[r])
     return ref, allow
 
 
@@ -265,12 +261,13 @@ def test_moe_full_size_sampled_tokens():
             wq = [oracle.weight_quant(expert_w(e, which).cpu().numpy()) for which in range(3)]
             o, uq, us = oracle.ffn_rows(xq[i:i + 1], xs[i:i + 1], *wq[0], *wq[1], *wq[2], [0], return_u=True)
             acc += np.float64(wts[t, j]) * synthetic.bf16_bits_to_f32(oracle.bf16_round(o[0]))
-            al += abs(float(wts[t, j])) * (2.0 ** -7 * np.abs(o[0]) +
-                                           flip_allowance(uq, us, dequant_weight(*wq[2]))[0])
+            al += abs(float(wts[t, j])) * (2.0 ** -7 * np.abs(o[0]) + ffn_chain_allowance(
+                xq[i:i + 1], xs[i:i + 1], *wq[0], *wq[1], dequant_weight(*wq[2]), uq, us)[0])
         ref.append(synthetic.bf16_bits_to_f32(oracle.bf16_round(acc)).astype(np.float64))
         allow.append(al)
-    rms = float(y.float().pow(2).mean().sqrt())
-    assert_chain_close(dev_to_bits(y)[tokens], np.array(ref), np.array(allow), rms=rms, frac=0.99,
+    ref = np.array(ref)
+    # the tolerance's rms term from the oracle's own rows (an estimate of the whole output's rms)
+    assert_chain_close(dev_to_bits(y)[tokens], ref, np.array(allow), rms=float(np.sqrt(np.mean(ref ** 2))),
                        what="moe sampled tokens")
     assert fb.last_device_error() == 0
 
@@ -292,9 +289,10 @@ def test_moe_shared_expert(T, E, dim, inter, k):
     routed = (xq, xs, idx, wts, w1q[:E * inter], w1s[:E * bi], w3q[:E * inter], w3s[:E * bi], w2q[:E * dim],
               w2s[:E * bd])
     ref_r, allow_r = moe_reference(routed, range(T), E)
-    z, uq, us = oracle.ffn_rows(xq, xs, w1q[E * inter:], w1s[E * bi:], w3q[E * inter:], w3s[E * bi:],
-                                w2q[E * dim:], w2s[E * bd:], range(T), return_u=True)
-    allow_z = 2.0 ** -7 * np.abs(z) + flip_allowance(uq, us, dequant_weight(w2q[E * dim:], w2s[E * bd:]))
+    sh = (w1q[E * inter:], w1s[E * bi:], w3q[E * inter:], w3s[E * bi:])
+    z, uq, us = oracle.ffn_rows(xq, xs, *sh, w2q[E * dim:], w2s[E * bd:], range(T), return_u=True)
+    allow_z = 2.0 ** -7 * np.abs(z) + ffn_chain_allowance(xq, xs, *sh, dequant_weight(w2q[E * dim:], w2s[E * bd:]),
+                                                          uq, us)
     allow = allow_r + allow_z + 2.0 ** -8 * (np.abs(ref_r) + np.abs(z))
     assert_chain_close(dev_to_bits(y), ref, allow, what=f"moe + shared expert T={T} E={E}")
     assert fb.last_device_error() == 0

@@ -1,10 +1,11 @@
 """Host-side check of the workspace sizes the library reports (no GPU).
 
 Without a device the library plans for 256 SMs, no cluster pairs and no
-split-K clusters. Every GEMM workspace is then the fixed 64 KB counter region
-followed by two stream-K partial slots (BN x 128 fp32) per CTA of the plan,
-the CTA count coming from the same schedule rule the kernels walk (mirrored in
-test_gemm_schedule). The composite layouts put that GEMM workspace first,
+split-K clusters. Every GEMM workspace is then the fixed 64 KB counter region,
+followed, for plans that cut tiles stream-K, by two partial slots (BN x 128
+fp32) per CTA of the plan, the CTA count coming from the same schedule rule
+the kernels walk (mirrored in test_gemm_schedule); plans of whole tiles or
+weight slices need the counter region only. The composite layouts put that GEMM workspace first,
 then their own parts, each 256-byte aligned: the sizes must be exactly those
 sums, so that the GEMM's counters sit at offset 0 whatever the shape."""
 import ctypes
@@ -30,16 +31,18 @@ def lib_size(name, *args):
 
 def gemm_ws(M, N, K):
     p = make_plan(M, N, K, 256, pairs=0, split_k=False)
-    return COUNTERS + 2 * p["grid"] * p["cluster"] * p["bn"] * 128 * 4
+    slots = 2 * p["grid"] * p["cluster"] * p["bn"] * 128 * 4 if p["sk_tiles"] > 0 else 0
+    return COUNTERS + slots
 
 
 def swiglu_ws(M, inter, dim):
     """The fused w1/w3 GEMM: 128 x 256 tiles (128 output columns), no pairs;
-    whole tiles or data-parallel waves use every SM, stream-K at most one CTA
-    per (tile, K block)."""
+    whole tiles (more tiles than counters: no slots) or data-parallel waves use
+    every SM, stream-K at most one CTA per (tile, K block)."""
     tiles = -(-M // 128) * (inter // 128)
-    many = tiles > COUNTERS // 4 or tiles >= 2 * 256
-    grid = 256 if many else min(256, tiles * (dim // 128))
+    if tiles > COUNTERS // 4:
+        return COUNTERS
+    grid = 256 if tiles >= 2 * 256 else min(256, tiles * (dim // 128))
     return COUNTERS + 2 * grid * 256 * 128 * 4
 
 
