@@ -738,48 +738,57 @@ def run_mla(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
 
 def run_gate(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     """The 671B gate (sigmoid scores, per-expert bias, 8 groups with 4 kept,
-    top-8, route_scale 2.5) on T tokens of fp32 logits, then the routing
-    permutation of its output: the step that turns gate logits into the
-    grouped GEMMs' row order."""
+    top-8, route_scale 2.5) on T tokens of fp32 logits together with the
+    routing permutation of its output (fp8blk_moe_route: the gate kernel also
+    ranks the pairs, one scatter pass): the step that turns gate logits into
+    the grouped GEMMs' row order. Also timed: the gate alone, and the gate
+    followed by the separate three-pass permutation."""
     T, E, G, TG, k, scale, seed = (shape[n] for n in ("T", "E", "groups", "kept", "k", "route_scale", "seed"))
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
     R = min(128, max(2, math.ceil(3 * l2 / (T * E * 4))))
     ls = [torch.from_numpy(synthetic.gate_logits(T, E, seed + i)).to(dev) for i in range(R)]
     b = torch.from_numpy(synthetic.gate_bias(E, seed)).to(dev)
-    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    out = (torch.empty((T, k), dtype=torch.int32, device=dev), torch.empty((T, k), dtype=torch.float32, device=dev),
+           torch.empty(E, dtype=torch.int32, device=dev), torch.empty(E + 1, dtype=torch.int32, device=dev),
+           torch.empty(T * k, dtype=torch.int32, device=dev))
 
     def gate(i):
-        fb.moe_gate(ls[i % R], b, G, TG, k, fb.SCORE_SIGMOID, scale, True, idx=idx, w=w)
+        fb.moe_gate(ls[i % R], b, G, TG, k, fb.SCORE_SIGMOID, scale, True, idx=out[0], w=out[1])
+
+    def unfused(i):
+        gate(i)
+        fb.moe_permute(out[0], E)
 
     def step(i):
-        gate(i)
-        fb.moe_permute(idx, E)
+        fb.moe_route(ls[i % R], b, G, TG, k, fb.SCORE_SIGMOID, scale, True, out=out)
 
     for i in range(3):
         step(i)
+        unfused(i)
     stream = torch.cuda.current_stream(dev)
     g_warm = make_runs(step, warmup, 50, torch, args.eager)
     g_main = make_runs(step, steps, 50, torch, args.eager)
     g_gate = make_runs(gate, steps, 50, torch, args.eager)
+    g_unf = make_runs(unfused, steps, 50, torch, args.eager)
     g_soak = make_runs(step, 50, 50, torch, args.eager)
     for g in g_warm:
         g.replay()
-    el, (el_gate,), clocks, _ = timed_runs(dev, stream, torch, g_main, (g_gate,), g_soak)
+    el, (el_gate, el_unf), clocks, _ = timed_runs(dev, stream, torch, g_main, (g_gate, g_unf), g_soak)
     assert fb.last_device_error(dev) == 0
     b_gate = T * E * 4 + E * 4 + T * k * 8            # logits, bias in; ids, weights out
-    b_step = b_gate + T * k * 4 + T * k * 4 + (2 * E + 1) * 4   # + ids read by the permutation, perm, counts
+    b_step = b_gate + T * k * 4 + (2 * E + 1) * 4      # + perm, counts, offsets out
     el_max, units = reduce_over_ranks(el, steps * b_step, dev)
-    achieved = b_gate / (el_gate / steps) / 1e9
+    achieved = b_step / (el / steps) / 1e9
     return {
         "value": units / el_max / 1e9, "unit": "GB/s", "ms_per_step": el_max / steps * 1e3,
-        "clocks": clocks, "gpu_launches": 4 * steps,
-        "kernels_us": {"gate_and_permute": el / steps * 1e6, "gate_alone": el_gate / steps * 1e6},
-        "roofline": {"bound": "hbm", "kernel": "moe_gate", "achieved": achieved, "peak": peaks["hbm"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None,
-                     "peak_source": f"hbm_gbs ({peaks['src']})", "algorithmic_bytes_per_launch": b_gate,
-                     "kernel_us": el_gate / steps * 1e6},
+        "clocks": clocks, "gpu_launches": 2 * steps,
+        "kernels_us": {"route (gate + permutation, 2 launches)": el / steps * 1e6, "gate_alone": el_gate / steps * 1e6,
+                       "gate then three-pass permutation (4 launches)": el_unf / steps * 1e6},
+        "roofline": {"bound": "hbm", "kernel": "moe_route (gate + rank kernel, scatter kernel)", "achieved": achieved,
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None,
+                     "peak_source": f"hbm_gbs ({peaks['src']})", "algorithmic_bytes_per_launch": b_step,
+                     "kernel_us": el / steps * 1e6},
         "e2e": None,
         "config": {"workload": args.workload, "T": T, "E": E, "groups": G, "kept_groups": TG, "topk": k,
                    "score": "sigmoid + per-expert bias", "route_scale": scale,

@@ -23,7 +23,7 @@ __all__ = [
     "SCALE_FP32", "SCALE_UE8M0", "SCALE_PROMOTE", "BLOCK", "lib", "lib_path", "header_functions", "Fp8BlkError",
     "act_quant", "weight_quant", "weight_dequant", "fp8_gemm", "linear", "linear_host",
     "gemm_workspace_bytes", "linear_workspace_bytes", "linear_host_workspace_bytes", "last_device_error",
-    "swiglu_gemm", "ffn", "moe_permute", "moe_workspace_bytes", "moe_grouped_gemm",
+    "swiglu_gemm", "ffn", "moe_permute", "moe_workspace_bytes", "moe_grouped_gemm", "moe_gate", "moe_route",
 ]
 
 SCALE_FP32 = 0
@@ -369,6 +369,35 @@ def moe_gate(logits: torch.Tensor, bias: torch.Tensor | None = None, n_groups: i
     _check(f(_ptr(logits), _ptr(bias), T, E, n_groups, topk_groups, topk, score_func, float(route_scale),
              int(bool(normalize)), _ptr(idx), _ptr(w), _stream(dev)), "moe_gate")
     return idx, w
+
+
+def moe_route(logits: torch.Tensor, bias: torch.Tensor | None = None, n_groups: int = 1, topk_groups: int = 1,
+              topk: int = 8, score_func: int = SCORE_SIGMOID, route_scale: float = 1.0, normalize: bool = True,
+              out=None):
+    """Gate and routing permutation in one call: logits fp32 [T, E] (+ bias)
+    -> (topk_idx int32 [T, topk], topk_w fp32 [T, topk], counts int32 [E],
+    offsets int32 [E+1], perm int32 [T*topk]). `out` may pass those five
+    tensors to be written in place."""
+    _need(logits, torch.float32, "logits")
+    if bias is not None:
+        _need(bias, torch.float32, "bias", ndim=1)
+    T, E = logits.shape
+    dev = logits.device
+    if out is None:
+        out = (torch.empty((T, topk), dtype=torch.int32, device=dev),
+               torch.empty((T, topk), dtype=torch.float32, device=dev),
+               torch.empty(E, dtype=torch.int32, device=dev), torch.empty(E + 1, dtype=torch.int32, device=dev),
+               torch.empty(max(T * topk, 1), dtype=torch.int32, device=dev))
+    idx, w, counts, offsets, perm = out
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    nbytes = int(_set_types("fp8blk_moe_route_workspace_bytes", [i64] * 3, sz)(T, topk, E))
+    ws = workspace(nbytes, dev, "moe_route")
+    f = _set_types("fp8blk_moe_route", [vp, vp, i64, i64, i64, i64, i64, i32, ctypes.c_float, i32] + [vp] * 6 +
+                   [sz, vp])
+    _check(f(_ptr(logits), _ptr(bias), T, E, n_groups, topk_groups, topk, score_func, float(route_scale),
+             int(bool(normalize)), _ptr(idx), _ptr(w), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(ws), ws.numel(),
+             _stream(dev)), "moe_route")
+    return idx, w, counts, offsets, perm[: T * topk]
 
 
 def moe_workspace_bytes(T: int, topk: int, E: int, dim: int, inter: int, n_shared: int = 0) -> int:

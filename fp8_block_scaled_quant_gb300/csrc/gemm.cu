@@ -183,6 +183,15 @@ constexpr int pow2_at_least(int v, int floor_) {
 }
 
 // TMEM columns per load (and per wait) in the register-split epilogue.
+// Swapped (decode) tiles: weight stages requested before the dependency wait.
+#ifndef FP8BLK_SWAP_PRE_STAGES
+#define FP8BLK_SWAP_PRE_STAGES 64
+#endif
+// Swapped (decode) tiles: K blocks whose scales are in flight ahead of the promotion.
+#ifndef FP8BLK_SWAP_SCALE_AHEAD
+#define FP8BLK_SWAP_SCALE_AHEAD 4
+#endif
+
 #ifndef FP8BLK_SPLIT_LD
 #define FP8BLK_SPLIT_LD 64
 #endif
@@ -619,10 +628,11 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
         Sched pre(prm, worker, -1, krank);
         Unit u;
         int nl2 = 0;
-        while ((npre < C::STAGES || nl2 < l2_ahead) && pre.next(u)) {
+        constexpr int kPre = C::SWAP && FP8BLK_SWAP_PRE_STAGES < C::STAGES ? FP8BLK_SWAP_PRE_STAGES : C::STAGES;
+        while ((npre < kPre || nl2 < l2_ahead) && pre.next(u)) {
           const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
           for (int kb = u.kb0; kb < u.kb1; ++kb) {
-            if (npre < C::STAGES) {
+            if (npre < kPre) {
               mbar_arrive_expect_tx(&full[npre], stage_tx);
               load_weights(npre, t, kb);
               ++npre;
@@ -1052,7 +1062,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
       float a, w, w3;
       float col[kColRegs];
     };
-    constexpr int kAhead = C::EPI_WARPS == 8 ? 3 : 4;
+    constexpr int kAhead = C::SWAP ? FP8BLK_SWAP_SCALE_AHEAD : C::EPI_WARPS == 8 ? 3 : 4;
     auto load_scales = [&](const TileInfo& t, int kb, int kb_end) -> ScaleRaw {
       ScaleRaw r;
       r.a = r.w = r.w3 = 0.0f;
@@ -1416,6 +1426,11 @@ using CfgS128 = Cfg<128, true, 6, 4, 4>;
 #define FP8BLK_SLICES 1
 #endif
 constexpr int kSliceRows = 80;
+// K blocks of a slice past its stage ring that are prefetched into L2 before
+// the dependency wait (-1: all of them).
+#ifndef FP8BLK_SLICE_L2_AHEAD
+#define FP8BLK_SLICE_L2_AHEAD -1
+#endif
 using CfgSl16 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
 using CfgSl32 = Cfg<32, true, 7, 8, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
 using CfgSl64 = Cfg<64, true, 6, 4, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
@@ -1811,7 +1826,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     return launch<CfgN128E8>(d, ml, mc, mc, prm, stream);
   }
   if (pl.lane_rows < 128) {
-    prm.l2_ahead = prm.Kb;  // every K block past the stage ring
+    prm.l2_ahead = FP8BLK_SLICE_L2_AHEAD < 0 ? prm.Kb : FP8BLK_SLICE_L2_AHEAD;  // K blocks past the stage ring
     switch (pl.bn) {
       case 16: return launch<CfgSl16>(d, ml, mc, mc, prm, stream);
       case 32: return launch<CfgSl32>(d, ml, mc, mc, prm, stream);
@@ -1878,7 +1893,7 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
     prm.tiles_lane = static_cast<int>((N + slice - 1) / slice);
     prm.whole_tiles = prm.tiles_lane;
     prm.grid = prm.tiles_lane;
-    prm.l2_ahead = Kb;
+    prm.l2_ahead = FP8BLK_SLICE_L2_AHEAD < 0 ? Kb : FP8BLK_SLICE_L2_AHEAD;
   }
   CUtensorMap ml;
   if (!make_kmajor_map(&ml, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint32_t>(prm.lane_rows)))

@@ -152,15 +152,16 @@ __global__ void __launch_bounds__(kPermThreads) moe_offsets_kernel(int* __restri
   }
 }
 
-// Scatter pass: perm[base[chunk][e] + rank] = pair, for every valid pair.
+// Scatter pass: perm[base[chunk][e] + rank] = pair, for every valid pair
+// (chunks of `chunk` consecutive pairs).
 __global__ void __launch_bounds__(256) moe_scatter_kernel(const int* __restrict__ idx, const int* __restrict__ rank,
-                                                          const int* __restrict__ base, int n, int E,
+                                                          const int* __restrict__ base, int n, int E, int chunk,
                                                           int* __restrict__ perm) {
   const int i = static_cast<int>(blockIdx.x) * 256 + static_cast<int>(threadIdx.x);
   if (i >= n) return;
   const int e = __ldg(idx + i);
   if (e < 0 || e >= E) return;
-  perm[__ldg(base + static_cast<size_t>(i / kPermChunk) * E + e) + __ldg(rank + i)] = i;
+  perm[__ldg(base + static_cast<size_t>(i / chunk) * E + e) + __ldg(rank + i)] = i;
 }
 
 // xg[r] = xq[perm[r] / topk] and its scales, for r < offsets[E] (one warp per row).
@@ -305,7 +306,8 @@ int launch_permute(const DevInfo* d, const int* idx, int64_t n, int64_t E, int* 
   if (int st = launch_status()) return st;
   if (n > 0) {
     moe_scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(idx, rank, base, static_cast<int>(n),
-                                                                                   static_cast<int>(E), perm);
+                                                                                   static_cast<int>(E), kPermChunk,
+                                                                                   perm);
   }
   return launch_status();
 }
@@ -341,16 +343,14 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
   return v;
 }
 
+// The gate of token t, computed by one warp: lane j < K ends with the expert
+// of slot j in *out_idx and its weight (normalised, times route_scale) in
+// *out_w.
 template <int V>
-__global__ void __launch_bounds__(kGateWarps * 32) moe_gate_kernel(const float* __restrict__ logits,
-                                                                   const float* __restrict__ bias, int T, int G,
-                                                                   int TG, int K, int sigmoid, float route_scale,
-                                                                   int normalize, int32_t* __restrict__ idx,
-                                                                   float* __restrict__ w) {
+__device__ __forceinline__ void gate_token(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                           int G, int TG, int K, int sigmoid, float route_scale, int normalize,
+                                           int lane, int* out_idx, float* out_w) {
   constexpr int E = 32 * V;
-  const int lane = threadIdx.x & 31;
-  const int t = static_cast<int>(blockIdx.x) * kGateWarps + static_cast<int>(threadIdx.x >> 5);
-  if (t >= T) return;  // whole warps leave together
   const float* l = logits + static_cast<size_t>(t) * E + lane * V;
   float s[V], z[V];
   if (sigmoid) {
@@ -440,10 +440,110 @@ __global__ void __launch_bounds__(kGateWarps * 32) moe_gate_kernel(const float* 
       my_s = se;
     }
   }
+  *out_idx = my_idx;
+  *out_w = __fmul_rn(normalize ? __fdiv_rn(my_s, sum) : my_s, route_scale);
+}
+
+template <int V>
+__global__ void __launch_bounds__(kGateWarps * 32) moe_gate_kernel(const float* __restrict__ logits,
+                                                                   const float* __restrict__ bias, int T, int G,
+                                                                   int TG, int K, int sigmoid, float route_scale,
+                                                                   int normalize, int32_t* __restrict__ idx,
+                                                                   float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = static_cast<int>(blockIdx.x) * kGateWarps + static_cast<int>(threadIdx.x >> 5);
+  if (t >= T) return;  // whole warps leave together
+  int e;
+  float v;
+  gate_token<V>(logits, bias, t, G, TG, K, sigmoid, route_scale, normalize, lane, &e, &v);
   if (lane < K) {
-    const float v = normalize ? __fdiv_rn(my_s, sum) : my_s;
-    idx[static_cast<size_t>(t) * K + lane] = my_idx;
-    w[static_cast<size_t>(t) * K + lane] = __fmul_rn(v, route_scale);
+    idx[static_cast<size_t>(t) * K + lane] = e;
+    w[static_cast<size_t>(t) * K + lane] = v;
+  }
+}
+
+// Gate and permutation in one launch. CTA c takes tokens [32 c, 32 c + 32)
+// (one warp each) and so the pairs [32 K c, 32 K (c + 1)) of the permutation:
+// after the gate it ranks each pair among the chunk's earlier pairs of its
+// expert and writes the chunk's per-expert histogram, as the rank pass does.
+// The last CTA to arrive on the workspace counter (no CTA waits for another)
+// turns the histograms into per-(chunk, expert) bases and writes counts and
+// offsets, then resets the counter; one scatter pass finishes the sort.
+constexpr int kRouteTokens = 32;
+
+template <int V>
+__global__ void __launch_bounds__(1024) moe_route_kernel(const float* __restrict__ logits,
+                                                         const float* __restrict__ bias, int T, int G, int TG, int K,
+                                                         int sigmoid, float route_scale, int normalize,
+                                                         int32_t* __restrict__ idx, float* __restrict__ w,
+                                                         int* __restrict__ rank, int* __restrict__ hist,
+                                                         int* __restrict__ arrivals, int nchunks,
+                                                         int* __restrict__ counts, int* __restrict__ offsets) {
+  constexpr int E = 32 * V;
+  __shared__ int ids[kRouteTokens * 32];
+  __shared__ int wtab[32 * E];  // per-warp counts of each expert, then their prefix over warps
+  __shared__ int wsum[40];
+  __shared__ int last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = static_cast<int>(blockIdx.x) * kRouteTokens + warp;
+  for (int k = tid; k < 32 * E; k += 1024) wtab[k] = 0;
+  if (t < T) {
+    int e;
+    float v;
+    gate_token<V>(logits, bias, t, G, TG, K, sigmoid, route_scale, normalize, lane, &e, &v);
+    if (lane < K) {
+      idx[static_cast<size_t>(t) * K + lane] = e;
+      w[static_cast<size_t>(t) * K + lane] = v;
+      ids[warp * K + lane] = e;
+    }
+  } else if (lane < K) {
+    ids[warp * K + lane] = -1;
+  }
+  __syncthreads();
+  // Ranks: thread p holds pair p of the chunk (global pair 32 K c + p).
+  const int npairs = kRouteTokens * K;
+  const int e = tid < npairs ? ids[tid] : -1;
+  const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+  const int wrank = __popc(m & ((1u << lane) - 1u));
+  if (e >= 0 && wrank == 0) wtab[warp * E + e] = __popc(m);
+  __syncthreads();
+  for (int x = tid; x < E; x += 1024) {
+    int run = 0;
+    for (int q = 0; q < 32; ++q) {
+      const int c = wtab[q * E + x];
+      wtab[q * E + x] = run;
+      run += c;
+    }
+    hist[static_cast<size_t>(blockIdx.x) * E + x] = run;
+  }
+  __syncthreads();
+  if (e >= 0) rank[static_cast<size_t>(blockIdx.x) * npairs + tid] = wtab[warp * E + e] + wrank;
+  // Arrive; the last CTA computes the bases.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(arrivals, 1) == nchunks - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  int total = 0;
+  if (tid < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      int* h = hist + static_cast<size_t>(c) * E + tid;
+      const int v = __ldcg(h);
+      *h = total;
+      total += v;
+    }
+  }
+  int rows;
+  const int off = block_exclusive_scan(total, wsum, &rows);
+  if (tid < E) {
+    counts[tid] = total;
+    offsets[tid] = off;
+    for (int c = 0; c < nchunks; ++c) hist[static_cast<size_t>(c) * E + tid] += off;
+  }
+  if (tid == 0) {
+    offsets[E] = rows;
+    *arrivals = 0;
   }
 }
 
@@ -468,6 +568,44 @@ int launch_gate(const float* logits, const float* bias, int64_t T, int64_t E, in
     default: return FP8BLK_ERR_SHAPE;
   }
 #undef FP8BLK_GATE_CASE
+  return launch_status();
+}
+
+// Workspace of the fused route: [arrival counter, 256 B][ranks: T*K ints][bases: chunks x E ints].
+size_t route_workspace_bytes(int64_t T, int64_t K, int64_t E) {
+  const int64_t nchunks = (T + kRouteTokens - 1) / kRouteTokens;
+  return 256 + align256(static_cast<size_t>(T) * K * 4) + align256(static_cast<size_t>(nchunks) * E * 4);
+}
+
+int launch_route(const float* logits, const float* bias, int64_t T, int64_t E, int64_t G, int64_t TG, int64_t K,
+                 int sigmoid, float route_scale, int normalize, int32_t* idx, float* w, int* counts, int* offsets,
+                 int* perm, void* workspace, cudaStream_t stream) {
+  const int nchunks = static_cast<int>((T + kRouteTokens - 1) / kRouteTokens);
+  int* arrivals = static_cast<int*>(workspace);
+  int* rank = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + 256);
+  int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + 256 + align256(static_cast<size_t>(T) * K * 4));
+  const int t = static_cast<int>(T), g = static_cast<int>(G), tg = static_cast<int>(TG), k = static_cast<int>(K);
+#define FP8BLK_ROUTE_CASE(v)                                                                                      \
+  case v:                                                                                                         \
+    moe_route_kernel<v><<<nchunks, 1024, 0, stream>>>(logits, bias, t, g, tg, k, sigmoid, route_scale, normalize, \
+                                                      idx, w, rank, base, arrivals, nchunks, counts, offsets);    \
+    break;
+  switch (E / 32) {
+    FP8BLK_ROUTE_CASE(1)
+    FP8BLK_ROUTE_CASE(2)
+    FP8BLK_ROUTE_CASE(3)
+    FP8BLK_ROUTE_CASE(4)
+    FP8BLK_ROUTE_CASE(5)
+    FP8BLK_ROUTE_CASE(6)
+    FP8BLK_ROUTE_CASE(7)
+    FP8BLK_ROUTE_CASE(8)
+    default: return FP8BLK_ERR_SHAPE;
+  }
+#undef FP8BLK_ROUTE_CASE
+  if (int st = launch_status()) return st;
+  const int64_t n = T * K;
+  moe_scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+      idx, rank, base, static_cast<int>(n), static_cast<int>(E), kRouteTokens * k, perm);
   return launch_status();
 }
 
@@ -496,15 +634,56 @@ extern "C" int fp8blk_moe_permute(const int32_t* topk_idx, int64_t T, int64_t to
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" int fp8blk_moe_gate(const float* logits, const float* bias, int64_t T, int64_t E, int64_t n_groups,
-                               int64_t topk_groups, int64_t topk, int score_func, float route_scale, int normalize,
-                               int32_t* topk_idx, float* topk_w, fp8blk_stream_t stream) {
+namespace {
+
+int gate_shape_status(const float* bias, int64_t T, int64_t E, int64_t n_groups, int64_t topk_groups, int64_t topk,
+                      int score_func, float route_scale) {
   if (score_func != FP8BLK_SCORE_SOFTMAX && score_func != FP8BLK_SCORE_SIGMOID) return FP8BLK_ERR_ARG;
   if (!(route_scale == route_scale) || route_scale == INFINITY || route_scale == -INFINITY) return FP8BLK_ERR_ARG;
   if (T < 0 || T > (int64_t{1} << 31) - 1 || E < 32 || E > 256 || E % 32 || n_groups < 1 || 32 % n_groups ||
       topk_groups < 1 || topk_groups > n_groups || topk < 1 || topk > 32 || topk > topk_groups * (E / n_groups) ||
       (bias && n_groups > 1 && E / n_groups < 2))
     return FP8BLK_ERR_SHAPE;
+  return FP8BLK_OK;
+}
+
+}  // namespace
+
+extern "C" size_t fp8blk_moe_route_workspace_bytes(int64_t T, int64_t topk, int64_t E) {
+  if (T < 0 || topk < 0 || E <= 0) return 0;
+  return route_workspace_bytes(T, topk, E);
+}
+
+extern "C" int fp8blk_moe_route(const float* logits, const float* bias, int64_t T, int64_t E, int64_t n_groups,
+                                int64_t topk_groups, int64_t topk, int score_func, float route_scale, int normalize,
+                                int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                void* workspace, size_t workspace_bytes, fp8blk_stream_t stream) {
+  if (int st = gate_shape_status(bias, T, E, n_groups, topk_groups, topk, score_func, route_scale)) return st;
+  if (T * topk > (int64_t{1} << 31) - 1) return FP8BLK_ERR_SHAPE;
+  if (!counts || !offsets) return FP8BLK_ERR_NULL;
+  if (T > 0 && (!logits || !topk_idx || !topk_w || !perm)) return FP8BLK_ERR_NULL;
+  if (!is_aligned(logits, 4) || !is_aligned(topk_idx, 4) || !is_aligned(topk_w, 4) || !is_aligned(counts, 4) ||
+      !is_aligned(offsets, 4) || !is_aligned(perm, 4) || (bias && !is_aligned(bias, 4)))
+    return FP8BLK_ERR_ALIGN;
+  if (!workspace || workspace_bytes < route_workspace_bytes(T, topk, E)) return FP8BLK_ERR_WORKSPACE;
+  if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {  // no pairs: every count and offset is zero
+    if (cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, cs) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, cs) != cudaSuccess)
+      return FP8BLK_ERR_CUDA;
+    return FP8BLK_OK;
+  }
+  return launch_route(logits, bias, T, E, n_groups, topk_groups, topk, score_func == FP8BLK_SCORE_SIGMOID,
+                      route_scale, normalize != 0, topk_idx, topk_w, counts, offsets, perm, workspace, cs);
+}
+
+extern "C" int fp8blk_moe_gate(const float* logits, const float* bias, int64_t T, int64_t E, int64_t n_groups,
+                               int64_t topk_groups, int64_t topk, int score_func, float route_scale, int normalize,
+                               int32_t* topk_idx, float* topk_w, fp8blk_stream_t stream) {
+  if (int st = gate_shape_status(bias, T, E, n_groups, topk_groups, topk, score_func, route_scale)) return st;
   if (T == 0) return FP8BLK_OK;
   if (!logits || !topk_idx || !topk_w) return FP8BLK_ERR_NULL;
   if (!is_aligned(logits, 4) || !is_aligned(topk_idx, 4) || !is_aligned(topk_w, 4) || (bias && !is_aligned(bias, 4)))

@@ -294,6 +294,30 @@ FP8BLK_API int fp8blk_moe_gate(const float *logits, const float *bias, int64_t T
                                int32_t *topk_idx, float *topk_w, fp8blk_stream_t stream);
 
 /*
+ * Gate and routing permutation together ("Administrator & Developer Guide",
+ * 8.4: the Gate, then steps 2-5 group the (token, slot) pairs by expert):
+ * topk_idx and topk_w exactly as fp8blk_moe_gate computes them, and counts,
+ * offsets and perm exactly as fp8blk_moe_permute would compute them from
+ * that topk_idx (counts[e] pairs per expert, offsets the exclusive prefix sum
+ * with offsets[E] = T * topk, perm the pairs t * topk + j in increasing order
+ * within each expert). Two launches: the gate kernel also ranks each pair
+ * among its chunk's pairs of the same expert and writes the chunk's
+ * histogram, its last CTA to finish turns the histograms into bases, counts
+ * and offsets; one scatter pass writes perm. Same shape rules and errors as
+ * fp8blk_moe_gate; counts int32 [E], offsets int32 [E + 1], perm int32
+ * [T * topk], 4-byte aligned. T == 0 zeroes counts and offsets.
+ * Workspace: fp8blk_moe_route_workspace_bytes(T, topk, E), 256-byte aligned;
+ * its first 256 bytes hold an arrival counter: ZERO-FILLED before the first
+ * use, and every call leaves it at zero. One workspace serves one stream at a
+ * time.
+ */
+FP8BLK_API size_t fp8blk_moe_route_workspace_bytes(int64_t T, int64_t topk, int64_t E);
+FP8BLK_API int fp8blk_moe_route(const float *logits, const float *bias, int64_t T, int64_t E, int64_t n_groups,
+                                int64_t topk_groups, int64_t topk, int score_func, float route_scale, int normalize,
+                                int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets, int32_t *perm,
+                                void *workspace, size_t workspace_bytes, fp8blk_stream_t stream);
+
+/*
  * Routed-expert FFN ("Administrator & Developer Guide", 6.4 and 8.4 steps
  * 2-5): y[t] = bf16( sum over slots j (in order) of
  *                    topk_w[t, j] * bf16(FFN_{topk_idx[t, j]}(x[t])) ),

@@ -81,6 +81,38 @@ def test_gate_matches_oracle(T, E, G, TG, k, sigmoid, use_bias, scale, norm):
     assert fb.last_device_error() == 0
 
 
+@pytest.mark.parametrize("T,E,G,TG,k,sigmoid,use_bias,scale,norm", CASES + [(4097, 256, 8, 4, 8, True, True, 2.5, True),
+                                                                      (1, 64, 1, 1, 6, False, False, 1.0, True)])
+def test_route_is_gate_then_permute(T, E, G, TG, k, sigmoid, use_bias, scale, norm):
+    """fp8blk_moe_route (the gate kernel also ranks the pairs and builds the
+    bases) gives exactly fp8blk_moe_gate's ids and weights, and exactly the
+    oracle's permutation of those ids (an integer stable sort: bit-exact)."""
+    l = synthetic.gate_logits(T, E, synthetic.SEED_GATE + E + 1)
+    b = synthetic.gate_bias(E, synthetic.SEED_GATE + 1) if use_bias else None
+    dev = torch.device("cuda")
+    ld = torch.from_numpy(l).to(dev)
+    bd = None if b is None else torch.from_numpy(b).to(dev)
+    sf = fb.SCORE_SIGMOID if sigmoid else fb.SCORE_SOFTMAX
+    gi, gw = fb.moe_gate(ld, bd, G, TG, k, sf, scale, norm)
+    for _ in range(2):   # twice: the workspace's arrival counter is left at zero
+        idx, w, counts, offsets, perm = fb.moe_route(ld, bd, G, TG, k, sf, scale, norm)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, gi) and torch.equal(w.view(torch.int32), gw.view(torch.int32))
+        co, oo, po = oracle.moe_permute(idx.cpu().numpy(), E)
+        assert np.array_equal(counts.cpu().numpy(), co)
+        assert np.array_equal(offsets.cpu().numpy(), oo)
+        assert np.array_equal(perm.cpu().numpy(), po)
+    assert fb.last_device_error() == 0
+
+
+def test_route_no_tokens():
+    dev = torch.device("cuda")
+    l = torch.zeros((0, 256), dtype=torch.float32, device=dev)
+    idx, w, counts, offsets, perm = fb.moe_route(l, None, 8, 4, 8)
+    torch.cuda.synchronize()
+    assert int(counts.abs().sum()) == 0 and int(offsets.abs().sum()) == 0
+
+
 def test_gate_feeds_the_permutation():
     """Gate output straight into the routing permutation: the per-expert
     counts are the bincount of the gate's ids."""
