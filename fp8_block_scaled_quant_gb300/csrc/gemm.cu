@@ -61,6 +61,11 @@
 
 namespace fp8blk {
 
+// The decode kernel (decode.cu).
+int decode_slice_rows(int64_t M, int64_t N, int64_t K, int sm_count, int smem_optin);
+int decode_gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
+                    int64_t K, int rows, cudaStream_t stream, bool* used);
+
 // Epilogue modes.
 enum : int {
   kEpiBf16 = 0,     // C[row, col] = bf16(acc)
@@ -99,8 +104,6 @@ struct GemmParams {
   int whole_tiles;     // > 0: that many whole tiles, round-robin over the CTAs (no stream-K)
   int ksplit;          // > 1: clusters of ksplit CTAs share one tile, each a K slice, reduced in DSMEM
   const __nv_bfloat16* x;  // fused decode linear: the bf16 activation [M, Kb * 128]
-  int lane_rows;       // swapped tiles: weight rows per tile (128, or fewer for weight slices)
-  int l2_ahead;        // swapped tiles: K blocks past the stage ring prefetched into L2 before the dependency wait
   int trace_id;        // phase-trace builds only: which of 8 trace slots this launch fills
 };
 
@@ -183,21 +186,13 @@ constexpr int pow2_at_least(int v, int floor_) {
 }
 
 // TMEM columns per load (and per wait) in the register-split epilogue.
-// Swapped (decode) tiles: weight stages requested before the dependency wait.
-#ifndef FP8BLK_SWAP_PRE_STAGES
-#define FP8BLK_SWAP_PRE_STAGES 64
-#endif
-// Swapped (decode) tiles: K blocks whose scales are in flight ahead of the promotion.
-#ifndef FP8BLK_SWAP_SCALE_AHEAD
-#define FP8BLK_SWAP_SCALE_AHEAD 4
-#endif
 
 #ifndef FP8BLK_SPLIT_LD
 #define FP8BLK_SPLIT_LD 64
 #endif
 
 template <int BN_, bool SWAP_, int STAGES_, int P_, int EPI_WARPS_, int MODE_ = kEpiBf16, bool GROUPED_ = false,
-          bool FUSED_ = false, int CLUSTER_ = 1, bool MX_ = false, int LROWS_ = 128>
+          bool FUSED_ = false, int CLUSTER_ = 1, bool MX_ = false>
 struct Cfg {
   // MX: power-of-two (UE8M0) scales applied by the tensor core itself
   // (tcgen05.mma kind::mxf8f6f4.block_scale). The scale of a K block is the
@@ -248,19 +243,10 @@ struct Cfg {
   // MX scale ring: slots of 16 TMEM columns after the accumulator, 4 K blocks each.
   static constexpr int kSfSlots = MX ? 8 : 0;
   static constexpr int kSfCol0 = P * BN;
-  // Weight slices (swapped tiles of fewer than 128 weight rows): a stage holds
-  // LROWS weight rows. The MMA still has M = 128 and reads 128 rows from the
-  // stage's start, past its weight rows; the lanes beyond the slice compute
-  // values nobody reads. Two such CTAs fit on one SM, so the next launch's
-  // CTAs start streaming their weights while this launch runs.
-  static constexpr int kLRows = SWAP ? LROWS_ : 128;
-  static constexpr int kABytes = kLRows * 128;
+  static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = FUSED ? kABytes : kABytes + kBBytes;
-  // Bytes after the ring that the last stage's 128-row MMA read may reach.
-  static constexpr int kRingPad = (kLRows < 128 && kStageBytes < 128 * 128) ? 128 * 128 - kStageBytes : 0;
-  static constexpr int kRingBytes = STAGES * kStageBytes + kRingPad;
-  static constexpr int kMinBlocks = kLRows < 128 ? 2 : 1;
+  static constexpr int kRingBytes = STAGES * kStageBytes;
   static constexpr int kTmemCols = pow2_at_least(P * BN + 16 * kSfSlots, 32);
   static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16 + (2 * kSfSlots + (MX ? 1 : 0)) * 8;
   // MX: the scale writers' exchange of activation-row scale words, double-buffered.
@@ -287,8 +273,6 @@ struct Cfg {
   static_assert(CLUSTER == 1 || (CLUSTER == 2 && !SWAP && !GROUPED && !FUSED && BN == 256),
                 "clusters pair the 128-row lane tiles of dense large-M GEMMs");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(kLRows % 8 == 0 && kLRows >= 8 && kLRows <= 128, "whole 8-row swizzle atoms per stage");
-  static_assert(kLRows == 128 || (SWAP && !GROUPED && CLUSTER == 1), "weight slices: swapped decode tiles");
 };
 
 // Where one output tile lives.
@@ -329,10 +313,9 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
     const int tl = (tile % p.tiles_lane) * C::CLUSTER + rank, tc = tile / p.tiles_lane;
     t.lane_y = tl * 128;
     if constexpr (C::SWAP) {
-      t.lane_y = tl * p.lane_rows;  // weight rows: 128-row tiles or slices of lane_rows
-      t.lane_valid = min(p.lane_rows, p.N - t.lane_y);
+      t.lane_valid = min(128, p.N - t.lane_y);
       t.col_y = tc * C::BN;
-      t.wblock = t.lane_y / 128;
+      t.wblock = tl;
       t.col0 = tc * C::BN;
     } else {
       t.lane_valid = min(128, p.M - t.lane_y);
@@ -371,7 +354,7 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
                                          int row, float* xchg, uint32_t unit_parity, Sync&& epi_sync) {
   if constexpr (C::SWAP) {
     const int n = t.lane_y + row;
-    if (row >= t.lane_valid) return true;  // a slice's lanes past its rows (or rows past N)
+    if (row >= t.lane_valid) return true;  // rows past N
 #pragma unroll
     for (int j = 0; j < C::kCpt; ++j) {
       const int m = t.col0 + j;
@@ -479,7 +462,7 @@ __host__ __device__ constexpr size_t fused_extra_bytes(int Kb, int BN) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
+__global__ void __launch_bounds__(C::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_lane, const __grid_constant__ CUtensorMap tmap_col,
                     const __grid_constant__ CUtensorMap tmap_col2, const GemmParams prm) {
   extern __shared__ uint8_t smem_raw[];
@@ -615,33 +598,20 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
         if constexpr (C::SWAP) tma_load_2d(sa + C::kABytes, &tmap_col, &full[st], kb * 128, t.col_y);
         else tma_load_2d(sa, &tmap_lane, &full[st], kb * 128, t.lane_y);
       };
-      // Bytes a stage receives: a weight slice has lane_rows rows (the TMA box).
-      const uint32_t stage_tx =
-          C::SWAP ? static_cast<uint32_t>(prm.lane_rows * 128 + (C::FUSED ? 0 : C::kBBytes)) : C::kStageBytes;
+      constexpr uint32_t stage_tx = C::kStageBytes;
       // Weights do not depend on the previous kernel on the stream: the first
-      // STAGES stages start loading them before the dependency wait, and the
-      // next l2_ahead K blocks are prefetched into L2; the activations follow
-      // once the previous kernel has completed.
-      const int l2_ahead = C::SWAP ? prm.l2_ahead : 0;
+      // STAGES stages start loading them before the dependency wait; the
+      // activations follow once the previous kernel has completed.
       int npre = 0;
       if constexpr (!C::GROUPED) {
         Sched pre(prm, worker, -1, krank);
         Unit u;
-        int nl2 = 0;
-        constexpr int kPre = C::SWAP && FP8BLK_SWAP_PRE_STAGES < C::STAGES ? FP8BLK_SWAP_PRE_STAGES : C::STAGES;
-        while ((npre < kPre || nl2 < l2_ahead) && pre.next(u)) {
+        while (npre < C::STAGES && pre.next(u)) {
           const TileInfo t = tile_info<C>(prm, u.tile, grp_rows, grp_mtiles, rank);
-          for (int kb = u.kb0; kb < u.kb1; ++kb) {
-            if (npre < kPre) {
-              mbar_arrive_expect_tx(&full[npre], stage_tx);
-              load_weights(npre, t, kb);
-              ++npre;
-            } else if (nl2 < l2_ahead) {
-              if constexpr (C::SWAP) tma_prefetch_l2_2d(&tmap_lane, kb * 128, t.lane_y);
-              ++nl2;
-            } else {
-              break;
-            }
+          for (int kb = u.kb0; kb < u.kb1 && npre < C::STAGES; ++kb) {
+            mbar_arrive_expect_tx(&full[npre], stage_tx);
+            load_weights(npre, t, kb);
+            ++npre;
           }
         }
       }
@@ -1062,7 +1032,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks)
       float a, w, w3;
       float col[kColRegs];
     };
-    constexpr int kAhead = C::SWAP ? FP8BLK_SWAP_SCALE_AHEAD : C::EPI_WARPS == 8 ? 3 : 4;
+    constexpr int kAhead = C::EPI_WARPS == 8 ? 3 : 4;
     auto load_scales = [&](const TileInfo& t, int kb, int kb_end) -> ScaleRaw {
       ScaleRaw r;
       r.a = r.w = r.w3 = 0.0f;
@@ -1420,20 +1390,7 @@ using CfgS32 = Cfg<32, true, (FP8BLK_DECODE_STAGES > 10 ? 10 : FP8BLK_DECODE_STA
 #endif
 using CfgS64 = Cfg<64, true, FP8BLK_S64_STAGES, 4, 4>;
 using CfgS128 = Cfg<128, true, 6, 4, 4>;
-// Weight slices for decode-sized M: up to kSliceRows weight rows per CTA and
-// all of K, one CTA per SM, stages small enough for two CTAs per SM.
-#ifndef FP8BLK_SLICES
-#define FP8BLK_SLICES 1
-#endif
-constexpr int kSliceRows = 80;
-// K blocks of a slice past its stage ring that are prefetched into L2 before
-// the dependency wait (-1: all of them).
-#ifndef FP8BLK_SLICE_L2_AHEAD
-#define FP8BLK_SLICE_L2_AHEAD -1
-#endif
-using CfgSl16 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
-using CfgSl32 = Cfg<32, true, 7, 8, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
-using CfgSl64 = Cfg<64, true, 6, 4, 4, kEpiBf16, false, false, 1, false, kSliceRows>;
+
 // Fused w1/w3 GEMM with the SwiGLU + act_quant epilogue (dense and grouped),
 // and the grouped GEMM whose rows are scattered back to token order.
 using CfgSwiGLU = Cfg<256, false, 4, 2, 8, kEpiSwiGLU, false>;
@@ -1456,7 +1413,7 @@ bool mx_for(int scale_fmt) { return scale_fmt_mx(scale_fmt); }
 // Decode linear with the act_quant fused in (M <= 16): weights-only stages.
 using CfgF16S8 = Cfg<16, true, 8, 8, 4, kEpiBf16, false, true>;
 using CfgF16S4 = Cfg<16, true, 4, 8, 4, kEpiBf16, false, true>;
-using CfgF16Sl = Cfg<16, true, 6, 8, 4, kEpiBf16, false, true, 1, false, kSliceRows>;
+
 constexpr int kMaxDynSmem = 232448;
 #ifndef FP8BLK_SMEM_CARVEOUT
 #define FP8BLK_SMEM_CARVEOUT 100  // percent of the unified L1 / shared memory (-1: the driver's choice)
@@ -1465,7 +1422,7 @@ constexpr int kMaxDynSmem = 232448;
 struct Plan {
   int bn;
   bool swap;
-  int lane_rows;  // swapped tiles: weight rows per tile (128, or a slice of 48..kSliceRows)
+  int slice_rows;  // > 0: decode weight slices of that many rows (the decode kernel), one CTA per slice
   int cluster;  // CTAs per schedule worker (2: lane-tile pairs); grid counts workers
   int ksplit;   // > 1: split-K clusters of that many CTAs per tile; grid counts CTAs
   int tiles_lane, tiles_col;
@@ -1516,27 +1473,23 @@ int swap_bn(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128
 
 // pair_workers: co-resident CTA pairs of the cluster kernel (0: no clusters).
 // caps: split-K cluster capacity of the swapped kernel (null: no split-K).
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, const SplitCaps* caps) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, const SplitCaps* caps,
+               int smem_optin) {
   Plan pl{};
   pl.cluster = 1;
   pl.ksplit = 1;
-  pl.lane_rows = 128;
   if (M <= 128) {
     pl.swap = true;
     pl.bn = swap_bn(M);
-    // Weight slices: one CTA per SM, each an equal slice of 48..kSliceRows
-    // weight rows over all of K (so no SM idles, as 128-row tiles would leave
-    // some when N / 128 is below the SM count, and no partial sums to fix up).
-    if (FP8BLK_SLICES && pl.bn <= 64) {
-      const int64_t rows = ((N + sm_count - 1) / sm_count + 7) / 8 * 8;
-      if (rows >= 48 && rows <= kSliceRows) {
-        pl.lane_rows = static_cast<int>(rows);
-        pl.tiles_lane = static_cast<int>((N + rows - 1) / rows);
-        pl.tiles_col = 1;
-        pl.grid = pl.tiles_lane;
-        pl.whole_tiles = pl.tiles_lane;
-        return pl;
-      }
+    // Weight slices: one CTA per SM, each an equal slice of 48..128 weight
+    // rows over all of K (no SM idles, no partial sums to fix up), run by the
+    // decode kernel.
+    if (const int rows = decode_slice_rows(M, N, K, sm_count, smem_optin)) {
+      pl.slice_rows = rows;
+      pl.tiles_lane = static_cast<int>((N + rows - 1) / rows);
+      pl.tiles_col = 1;
+      pl.grid = pl.tiles_lane;
+      return pl;
     }
     pl.tiles_lane = static_cast<int>((N + 127) / 128);
     pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
@@ -1747,8 +1700,8 @@ const SplitCaps* split_caps(const DevInfo* d, int64_t M) {
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 256;
   const DevInfo* d;
-  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_plan(M, N, K, 256, 0, nullptr));
-  return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M)));
+  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_plan(M, N, K, 256, 0, nullptr, kMaxDynSmem));
+  return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M), d->smem_optin));
 }
 
 // The argument checks of fp8_gemm, in order: FP8BLK_OK when they pass (an
@@ -1777,13 +1730,18 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   if (K == 0) return cuda_status(cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * 2, stream));
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
+  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M), d->smem_optin);
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
+  if (pl.slice_rows > 0) {
+    bool used = false;
+    const int st = decode_gemm_run(a, a_s, w, w_s, c, M, N, K, pl.slice_rows, stream, &used);
+    if (st || used) return st;
+    return FP8BLK_ERR_CUDA;  // the plan promised a slice kernel that fits
+  }
 
   GemmParams prm{};
-  prm.lane_rows = 128;
   prm.a_s = a_s;
   prm.w_s = w_s;
   prm.c = static_cast<__nv_bfloat16*>(c);
@@ -1812,8 +1770,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   const uint64_t col_rows = static_cast<uint64_t>(pl.swap ? M : N);
   // Cluster pairs load the column tile in two 128-row halves.
   const uint32_t col_box = static_cast<uint32_t>(pl.cluster == 2 ? 128 : pl.bn);
-  prm.lane_rows = pl.lane_rows;
-  if (!make_kmajor_map(&ml, lane_src, lane_rows, static_cast<uint64_t>(K), static_cast<uint32_t>(pl.lane_rows)) ||
+  if (!make_kmajor_map(&ml, lane_src, lane_rows, static_cast<uint64_t>(K), 128) ||
       !make_kmajor_map(&mc, col_src, col_rows, static_cast<uint64_t>(K), col_box))
     return FP8BLK_ERR_CUDA;
 
@@ -1824,14 +1781,6 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
     if (pl.bn == 256)
       return mx ? launch<CfgN256MX>(d, ml, mc, mc, prm, stream) : launch<CfgN256>(d, ml, mc, mc, prm, stream);
     return launch<CfgN128E8>(d, ml, mc, mc, prm, stream);
-  }
-  if (pl.lane_rows < 128) {
-    prm.l2_ahead = FP8BLK_SLICE_L2_AHEAD < 0 ? prm.Kb : FP8BLK_SLICE_L2_AHEAD;  // K blocks past the stage ring
-    switch (pl.bn) {
-      case 16: return launch<CfgSl16>(d, ml, mc, mc, prm, stream);
-      case 32: return launch<CfgSl32>(d, ml, mc, mc, prm, stream);
-      default: return launch<CfgSl64>(d, ml, mc, mc, prm, stream);
-    }
   }
   switch (pl.bn) {
     case 16: return launch<CfgS16>(d, ml, mc, mc, prm, stream, 0, pl.ksplit);
@@ -1863,17 +1812,11 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
   if (int st = current_device(&d)) return st;
   const int Kb = static_cast<int>(K / kBlock);
   const size_t extra = fused_extra_bytes(Kb, 16);
-  // Weight slices (as make_plan picks them) when two such CTAs fit on an SM.
-  const int64_t slice = ((N + d->sm_count - 1) / d->sm_count + 7) / 8 * 8;
-  const bool slices = FP8BLK_SLICES && slice >= 48 && slice <= kSliceRows &&
-                      2 * (CfgF16Sl::kSmemBytes + extra + 1024) <= static_cast<size_t>(d->smem_per_sm);
-  const int variant = slices                                          ? 2   // slices, 6 weight stages
-                      : CfgF16S8::kSmemBytes + extra <= kMaxDynSmem   ? 0   // 8 weight stages
+  const int variant = CfgF16S8::kSmemBytes + extra <= kMaxDynSmem   ? 0   // 8 weight stages
                       : CfgF16S4::kSmemBytes + extra <= kMaxDynSmem ? 1   // 4 weight stages
                                                                     : -1;
   if (variant < 0) return FP8BLK_OK;
   GemmParams prm{};
-  prm.lane_rows = 128;
   prm.w_s = w_s;
   prm.c = static_cast<__nv_bfloat16*>(y);
   prm.x = static_cast<const __nv_bfloat16*>(x);
@@ -1888,20 +1831,11 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
   prm.whole_tiles = prm.n_wblocks;
   prm.grid = prm.n_wblocks < d->sm_count ? prm.n_wblocks : d->sm_count;
   prm.ue8m0 = scale_fmt_ue8m0(scale_fmt);
-  if (variant == 2) {
-    prm.lane_rows = static_cast<int>(slice);
-    prm.tiles_lane = static_cast<int>((N + slice - 1) / slice);
-    prm.whole_tiles = prm.tiles_lane;
-    prm.grid = prm.tiles_lane;
-    prm.l2_ahead = FP8BLK_SLICE_L2_AHEAD < 0 ? Kb : FP8BLK_SLICE_L2_AHEAD;
-  }
   CUtensorMap ml;
-  if (!make_kmajor_map(&ml, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint32_t>(prm.lane_rows)))
-    return FP8BLK_ERR_CUDA;
+  if (!make_kmajor_map(&ml, w, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 128)) return FP8BLK_ERR_CUDA;
   *used = true;
-  return variant == 2   ? launch<CfgF16Sl>(d, ml, ml, ml, prm, stream, extra)
-         : variant == 0 ? launch<CfgF16S8>(d, ml, ml, ml, prm, stream, extra)
-                        : launch<CfgF16S4>(d, ml, ml, ml, prm, stream, extra);
+  return variant == 0 ? launch<CfgF16S8>(d, ml, ml, ml, prm, stream, extra)
+                      : launch<CfgF16S4>(d, ml, ml, ml, prm, stream, extra);
 }
 
 size_t swiglu_workspace_bytes(int64_t M, int64_t inter, int64_t K) {
@@ -1930,7 +1864,6 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
   if (!workspace || workspace_bytes < plan_workspace(pl)) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
   GemmParams prm{};
-  prm.lane_rows = 128;
   prm.a_s = xs;
   prm.w_s = w1s;
   prm.w3_s = w3s;
@@ -1973,7 +1906,6 @@ int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const f
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
   GemmParams prm{};
-  prm.lane_rows = 128;
   prm.a_s = xgs;
   prm.w_s = w1s;
   prm.w3_s = w3s;
@@ -2007,7 +1939,6 @@ int grouped_scatter_run(const void* uq, const float* us, const void* w2, const f
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
   GemmParams prm{};
-  prm.lane_rows = 128;
   prm.a_s = us;
   prm.w_s = w2s;
   prm.c = static_cast<__nv_bfloat16*>(out);
@@ -2083,7 +2014,7 @@ extern "C" int fp8blk_gemm_noalloc(const void* a_e4m3, const float* a_s, const v
     return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, nullptr, 0, cs);
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
+  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M), d->smem_optin);
   if (plan_workspace(pl) > FP8BLK_NOALLOC_SCRATCH_BYTES) return FP8BLK_ERR_TOO_LARGE;
   void* scratch = nullptr;
   if (int st = noalloc_scratch(d->device, &scratch)) return st;

@@ -12,7 +12,7 @@ import pytest
 
 
 MAX_COUNTERS = 64 * 1024 // 4   # the workspace's fixed counter region, one int32 per tile
-SLICE_ROWS = 80                 # most weight rows of a decode slice (the slice kernels' stage size)
+SLICE_ROWS = 128                # most weight rows of a decode slice (one MMA's 128 lanes)
 
 
 def make_plan(M, N, K, sms, pairs=None, split_k=True):
@@ -27,7 +27,7 @@ def make_plan(M, N, K, sms, pairs=None, split_k=True):
     if M <= 128:
         swap = True
         bn = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
-        if bn <= 64:   # weight slices: one CTA per SM, rows..rows of the weight over all of K
+        if bn <= 64:   # weight slices (the decode kernel): one CTA per SM, a slice of rows over all of K
             rows = (-(-N // sms) + 7) // 8 * 8
             if 48 <= rows <= SLICE_ROWS:
                 tl = -(-N // rows)
@@ -173,6 +173,8 @@ def test_decode_plan_uses_weight_slices():
         assert p["swap"] and p["bn"] == bn and p["grid"] == 152 and p["lane_rows"] == 72 and p["whole"] == 152
     p = make_plan(8, 10944, 2048, 148)       # 148 SMs: 74-row slices rounded to 80
     assert p["lane_rows"] == 80 and p["grid"] == 137
+    p = make_plan(8, 19000, 1024, 152)       # 125 rows per SM: slices of 128
+    assert p["lane_rows"] == 128 and p["grid"] == 149
     p = make_plan(8, 24576, 1536, 152)       # slices would exceed SLICE_ROWS: 128-row tiles, stream-K
     assert "lane_rows" not in p and p["sk_tiles"] > 0
     p = make_plan(8, 4000, 2048, 152)        # slices below 48 rows: 128-row tiles split K in clusters
@@ -181,7 +183,7 @@ def test_decode_plan_uses_weight_slices():
     assert p["grid"] == 152 and p["dp"] == 0
 
 
-@pytest.mark.parametrize("N", [10944, 7300, 12160, 9999])
+@pytest.mark.parametrize("N", [10944, 7300, 12160, 9999, 19000])
 @pytest.mark.parametrize("sms", [152, 148, 132])
 def test_weight_slices_cover_every_row_once(N, sms):
     """Slices are whole 8-row swizzle atoms, cover rows [0, N) exactly once with
