@@ -61,11 +61,6 @@
 
 namespace fp8blk {
 
-// The decode kernel (decode.cu).
-int decode_slice_rows(int64_t M, int64_t N, int64_t K, int sm_count, int smem_optin);
-int decode_gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
-                    int64_t K, int rows, cudaStream_t stream, bool* used);
-
 // Epilogue modes.
 enum : int {
   kEpiBf16 = 0,     // C[row, col] = bf16(acc)
@@ -1422,7 +1417,6 @@ constexpr int kMaxDynSmem = 232448;
 struct Plan {
   int bn;
   bool swap;
-  int slice_rows;  // > 0: decode weight slices of that many rows (the decode kernel), one CTA per slice
   int cluster;  // CTAs per schedule worker (2: lane-tile pairs); grid counts workers
   int ksplit;   // > 1: split-K clusters of that many CTAs per tile; grid counts CTAs
   int tiles_lane, tiles_col;
@@ -1473,24 +1467,13 @@ int swap_bn(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128
 
 // pair_workers: co-resident CTA pairs of the cluster kernel (0: no clusters).
 // caps: split-K cluster capacity of the swapped kernel (null: no split-K).
-Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, const SplitCaps* caps,
-               int smem_optin) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, const SplitCaps* caps) {
   Plan pl{};
   pl.cluster = 1;
   pl.ksplit = 1;
   if (M <= 128) {
     pl.swap = true;
     pl.bn = swap_bn(M);
-    // Weight slices: one CTA per SM, each an equal slice of 48..128 weight
-    // rows over all of K (no SM idles, no partial sums to fix up), run by the
-    // decode kernel.
-    if (const int rows = decode_slice_rows(M, N, K, sm_count, smem_optin)) {
-      pl.slice_rows = rows;
-      pl.tiles_lane = static_cast<int>((N + rows - 1) / rows);
-      pl.tiles_col = 1;
-      pl.grid = pl.tiles_lane;
-      return pl;
-    }
     pl.tiles_lane = static_cast<int>((N + 127) / 128);
     pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
     const long long tiles = static_cast<long long>(pl.tiles_lane) * pl.tiles_col;
@@ -1700,8 +1683,8 @@ const SplitCaps* split_caps(const DevInfo* d, int64_t M) {
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 256;
   const DevInfo* d;
-  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_plan(M, N, K, 256, 0, nullptr, kMaxDynSmem));
-  return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M), d->smem_optin));
+  if (current_device(&d) != FP8BLK_OK) return plan_workspace(make_plan(M, N, K, 256, 0, nullptr));
+  return plan_workspace(make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M)));
 }
 
 // The argument checks of fp8_gemm, in order: FP8BLK_OK when they pass (an
@@ -1730,16 +1713,10 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   if (K == 0) return cuda_status(cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * 2, stream));
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M), d->smem_optin);
+  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
-  if (pl.slice_rows > 0) {
-    bool used = false;
-    const int st = decode_gemm_run(a, a_s, w, w_s, c, M, N, K, pl.slice_rows, stream, &used);
-    if (st || used) return st;
-    return FP8BLK_ERR_CUDA;  // the plan promised a slice kernel that fits
-  }
 
   GemmParams prm{};
   prm.a_s = a_s;
@@ -2014,7 +1991,7 @@ extern "C" int fp8blk_gemm_noalloc(const void* a_e4m3, const float* a_s, const v
     return gemm_run(a_e4m3, a_s, w_e4m3, w_s, c_bf16, M, N, K, scale_fmt, nullptr, 0, cs);
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
-  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M), d->smem_optin);
+  const Plan pl = make_plan(M, N, K, d->sm_count, cluster_workers<CfgN256C2>(d), split_caps(d, M));
   if (plan_workspace(pl) > FP8BLK_NOALLOC_SCRATCH_BYTES) return FP8BLK_ERR_TOO_LARGE;
   void* scratch = nullptr;
   if (int st = noalloc_scratch(d->device, &scratch)) return st;

@@ -134,18 +134,6 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorM
 }
 
 // Prefetch of the same box into L2 only (no shared memory, no completion).
-// 3-D tile load: box at (x, y, z) of `map` into shared memory, completing
-// `bar`'s transaction count. With the K blocks of a K-major matrix as the
-// third dimension, one box carries several 128-byte-wide K blocks, each
-// landing as its own swizzled tile.
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),

@@ -12,7 +12,6 @@ import pytest
 
 
 MAX_COUNTERS = 64 * 1024 // 4   # the workspace's fixed counter region, one int32 per tile
-SLICE_ROWS = 128                # most weight rows of a decode slice (one MMA's 128 lanes)
 
 
 def make_plan(M, N, K, sms, pairs=None, split_k=True):
@@ -27,12 +26,6 @@ def make_plan(M, N, K, sms, pairs=None, split_k=True):
     if M <= 128:
         swap = True
         bn = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
-        if bn <= 64:   # weight slices (the decode kernel): one CTA per SM, a slice of rows over all of K
-            rows = (-(-N // sms) + 7) // 8 * 8
-            if 48 <= rows <= SLICE_ROWS:
-                tl = -(-N // rows)
-                return dict(swap=swap, bn=bn, tl=tl, tc=1, grid=tl, dp=0, sk_tiles=0, sk_iters=0, Kb=Kb,
-                            tiles=tl, cluster=1, ksplit=1, whole=tl, lane_rows=rows)
         tl, tc = -(-N // 128), -(-M // bn)
         tiles = tl * tc
         if bn <= 64 and tiles <= sms and 2 * tiles >= sms:   # decode: one CTA per whole weight tile
@@ -166,43 +159,13 @@ def test_split_k_clusters(M, N, K):
         assert sorted((u[1], u[2]) for u in slices)[0][0] == 0 and max(u[2] for u in slices) == p["Kb"]
 
 
-def test_decode_plan_uses_weight_slices():
-    """N = 10944 on 152 SMs: 152 slices of 72 weight rows, one per SM, all of K each."""
-    for M, bn in ((1, 16), (8, 16), (32, 32), (64, 64)):
-        p = make_plan(M, 10944, 2048, 152)
-        assert p["swap"] and p["bn"] == bn and p["grid"] == 152 and p["lane_rows"] == 72 and p["whole"] == 152
-    p = make_plan(8, 10944, 2048, 148)       # 148 SMs: 74-row slices rounded to 80
-    assert p["lane_rows"] == 80 and p["grid"] == 137
-    p = make_plan(8, 19000, 1024, 152)       # 125 rows per SM: slices of 128
-    assert p["lane_rows"] == 128 and p["grid"] == 149
-    p = make_plan(8, 24576, 1536, 152)       # slices would exceed SLICE_ROWS: 128-row tiles, stream-K
-    assert "lane_rows" not in p and p["sk_tiles"] > 0
-    p = make_plan(8, 4000, 2048, 152)        # slices below 48 rows: 128-row tiles split K in clusters
-    assert "lane_rows" not in p
+def test_decode_plan_uses_whole_tiles():
+    p = make_plan(8, 10944, 2048, 152)
+    assert p["swap"] and p["bn"] == 16 and p["grid"] == 86 and p["dp"] == 1 and p["sk_iters"] == 0
+    p = make_plan(64, 10944, 2048, 152)      # BN 64: whole tiles as well
+    assert p["bn"] == 64 and p["grid"] == 86 and p["dp"] == 1
     p = make_plan(128, 10944, 2048, 152)     # BN 128: stream-K over the whole machine
     assert p["grid"] == 152 and p["dp"] == 0
-
-
-@pytest.mark.parametrize("N", [10944, 7300, 12160, 9999, 19000])
-@pytest.mark.parametrize("sms", [152, 148, 132])
-def test_weight_slices_cover_every_row_once(N, sms):
-    """Slices are whole 8-row swizzle atoms, cover rows [0, N) exactly once with
-    every CTA holding at least one row, and a slice spans at most two 128-row
-    weight-scale blocks (the epilogue takes each row's block scale)."""
-    p = make_plan(8, N, 2048, sms)
-    if "lane_rows" not in p:
-        pytest.skip("no slice plan for this N")
-    R = p["lane_rows"]
-    assert R % 8 == 0 and 48 <= R <= SLICE_ROWS and p["grid"] <= sms
-    seen = []
-    for c in range(p["grid"]):
-        (tile, kb0, kb1, part, nparts), = list(units(p, c))
-        assert tile == c and (kb0, kb1) == (0, p["Kb"])
-        rows = range(tile * R, min(tile * R + R, N))
-        assert len(rows) >= 1
-        assert rows[-1] // 128 - rows[0] // 128 <= 1
-        seen.extend(rows)
-    assert seen == list(range(N))
 
 
 def test_tile_width_rule():
