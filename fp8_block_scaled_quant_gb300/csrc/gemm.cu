@@ -53,6 +53,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "fp8blk.h"
 #include "host.cuh"
@@ -95,6 +96,7 @@ struct GemmParams {
   int sk_tiles;        // the remaining tiles run stream-K
   long long sk_iters;  // sk_tiles * Kb
   int vec_store;       // C rows 16-byte aligned and N % 8 == 0
+  int vec_scales;      // Kb % 4 == 0 and the scale arrays 16-byte aligned: scales load four K blocks at a time
   int ue8m0;           // power-of-two scales for a fused act_quant (SwiGLU output, decode input)
   int whole_tiles;     // > 0: that many whole tiles, round-robin over the CTAs (no stream-K)
   int ksplit;          // > 1: clusters of ksplit CTAs share one tile, each a K slice, reduced in DSMEM
@@ -179,6 +181,15 @@ constexpr int pow2_at_least(int v, int floor_) {
   while (p < v) p <<= 1;
   return p;
 }
+
+// Plain (bf16-output, dense) non-swapped tiles: K blocks of scales per vector
+// load in the promotion (1: one K block at a time, kAhead blocks ahead). The
+// SwiGLU, scatter and grouped epilogues keep one K block at a time: their
+// extra registers spill. Measured on the prefill GEMMs (4096 x 18432 x 7168,
+// 4096 x 7168 x 18432): 519 / 508 us with 1, 506 / 496 us with 4.
+#ifndef FP8BLK_SCALE_VEC
+#define FP8BLK_SCALE_VEC 4
+#endif
 
 // TMEM columns per load (and per wait) in the register-split epilogue.
 
@@ -1059,6 +1070,45 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       return r;
     };
 
+    // Non-swapped tiles: this thread's activation-row scales and the tile's
+    // weight-block scales of kQ consecutive K blocks (a group), one vector
+    // load each when the arrays allow it, the next group in flight while the
+    // current one is used (the same a_s * w_s products as one K block at a time).
+    constexpr int kQ = (C::MODE == kEpiBf16 && !C::GROUPED) ? FP8BLK_SCALE_VEC : 1;
+    using QV = typename std::conditional<kQ == 4, float4, typename std::conditional<kQ == 2, float2, float>::type>::type;
+    struct Quad {
+      QV a, w, w3;
+    };
+    auto load_quad = [&](const TileInfo& t, int q) -> Quad {
+      Quad r{};
+      const int k0 = q * kQ;
+      if (k0 >= prm.Kb) return r;
+      auto ld4 = [&](const float* p) -> QV {
+        if (prm.vec_scales) return __ldg(reinterpret_cast<const QV*>(p));
+        QV v{};
+        float* f = reinterpret_cast<float*>(&v);
+#pragma unroll
+        for (int i = 0; i < kQ; ++i) f[i] = k0 + i < prm.Kb ? __ldg(p + i) : 0.0f;
+        return v;
+      };
+      if (row < t.lane_valid) r.a = ld4(prm.a_s + static_cast<size_t>(t.lane_y + row) * prm.Kb + k0);
+      if constexpr (C::MODE == kEpiSwiGLU) {
+        r.w = ld4(prm.w_s + static_cast<size_t>(t.wblock) * prm.Kb + k0);
+        r.w3 = ld4(prm.w3_s + static_cast<size_t>(t.wblock) * prm.Kb + k0);
+      } else {
+        const int nb = t.wblock + (group * C::kCpt) / 128;
+        if (C::GROUPED || nb < prm.n_wblocks) r.w = ld4(prm.w_s + static_cast<size_t>(nb) * prm.Kb + k0);
+      }
+      return r;
+    };
+    auto pick4 = [](const QV& v, int i) -> float {
+      const float* f = reinterpret_cast<const float*>(&v);
+      float r = f[0];
+#pragma unroll
+      for (int j = 1; j < kQ; ++j) r = i == j ? f[j] : r;
+      return r;
+    };
+
     Sched sch(prm, worker, grouped_tiles, krank);
     Unit u;
     int pb = 0;
@@ -1094,19 +1144,40 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       } else {
 #pragma unroll
       for (int i = 0; i < C::kCpt; ++i) acc[i] = 0.0f;
-      ScaleRaw pipe[kAhead];
+      constexpr bool kPipe = C::SWAP || kQ == 1;
+      ScaleRaw pipe[kPipe ? kAhead : 1];
+      Quad qc{}, qn{};
+      int qcur = u.kb0 / kQ;
+      if constexpr (kPipe) {
 #pragma unroll
-      for (int d = 0; d < kAhead; ++d) pipe[d] = load_scales(t, u.kb0 + d, u.kb1);
+        for (int d = 0; d < kAhead; ++d) pipe[d] = load_scales(t, u.kb0 + d, u.kb1);
+      } else {
+        qc = load_quad(t, qcur);
+        qn = (qcur + 1) * kQ < u.kb1 ? load_quad(t, qcur + 1) : Quad{};
+      }
 
       for (int kb = u.kb0; kb < u.kb1; ++kb) {
-        // Scales of this K block: loaded kAhead blocks earlier (the shifting
-        // window `pipe`), multiplied here. sc_lo applies to the first half of
-        // the thread's columns, sc_hi to the second (they differ only in
-        // SwiGLU mode: w1 vs w3 scales).
-        const ScaleRaw cur = pipe[0];
+        // Scales of this K block: loaded kAhead blocks earlier (swapped tiles:
+        // the shifting window `pipe`) or with its quad of four K blocks, the
+        // next quad in flight; multiplied here. sc_lo applies to the first
+        // half of the thread's columns, sc_hi to the second (they differ only
+        // in SwiGLU mode: w1 vs w3 scales).
+        ScaleRaw cur{};
+        if constexpr (kPipe) {
+          cur = pipe[0];
 #pragma unroll
-        for (int d = 0; d + 1 < kAhead; ++d) pipe[d] = pipe[d + 1];
-        pipe[kAhead - 1] = load_scales(t, kb + kAhead, u.kb1);
+          for (int d = 0; d + 1 < kAhead; ++d) pipe[d] = pipe[d + 1];
+          pipe[kAhead - 1] = load_scales(t, kb + kAhead, u.kb1);
+        } else {
+          if (kb / kQ != qcur) {
+            qc = qn;
+            ++qcur;
+            qn = (qcur + 1) * kQ < u.kb1 ? load_quad(t, qcur + 1) : Quad{};
+          }
+          cur.a = pick4(qc.a, kb % kQ);
+          cur.w = pick4(qc.w, kb % kQ);
+          cur.w3 = pick4(qc.w3, kb % kQ);
+        }
         float sc_lo = 0.0f, sc_hi = 0.0f;
         // Swapped tiles: sc_col[i] is the activation scale of token lane + 32 i
         // (shuffled to the thread that owns each column), w_row this thread's
@@ -1540,6 +1611,13 @@ Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count, int pai
 
 size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
+// Scale rows of Kb floats load FP8BLK_SCALE_VEC at a time when every row of
+// each array starts on that many floats' boundary.
+int vec_scales_ok(int Kb, const float* a, const float* b, const float* c) {
+  const int q = FP8BLK_SCALE_VEC;
+  return q > 1 && Kb % q == 0 && is_aligned(a, 4u * q) && is_aligned(b, 4u * q) && is_aligned(c, 4u * q) ? 1 : 0;
+}
+
 // Workspace: the counter region (one arrival counter per output tile), then,
 // for plans that cut tiles stream-K, two partial slots per CTA. Plans of whole
 // tiles, weight slices or split-K clusters write no partial sums to memory.
@@ -1738,6 +1816,7 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   prm.whole_tiles = pl.whole_tiles;
   prm.ksplit = pl.ksplit;
   prm.vec_store = (N % 8 == 0 && is_aligned(c, 16)) ? 1 : 0;
+  prm.vec_scales = vec_scales_ok(prm.Kb, a_s, w_s, w_s);
   prm.ldc = static_cast<int>(N);
 
   CUtensorMap ml, mc;
@@ -1862,6 +1941,7 @@ int swiglu_run(const void* xq, const float* xs, const void* w1, const float* w1s
   prm.sk_iters = pl.sk_iters;
   prm.whole_tiles = pl.whole_tiles;
   prm.ue8m0 = scale_fmt_ue8m0(scale_fmt);
+  prm.vec_scales = 0;  // one K block at a time in the SwiGLU epilogue
   CUtensorMap ml, m1, m3;
   if (!make_kmajor_map(&ml, xq, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128) ||
       !make_kmajor_map(&m1, w1, static_cast<uint64_t>(inter), static_cast<uint64_t>(K), 64) ||
@@ -1899,6 +1979,7 @@ int grouped_swiglu_run(const void* xg, const float* xgs, const void* w1, const f
   prm.tiles_col = static_cast<int>(inter / 128);
   prm.grid = d->sm_count;
   prm.ue8m0 = scale_fmt_ue8m0(scale_fmt);
+  prm.vec_scales = 0;
   CUtensorMap ml, m1, m3;
   if (!make_kmajor_map(&ml, xg, static_cast<uint64_t>(rows), static_cast<uint64_t>(K), 128) ||
       !make_kmajor_map(&m1, w1, static_cast<uint64_t>(E * inter), static_cast<uint64_t>(K), 64) ||
@@ -1931,6 +2012,7 @@ int grouped_scatter_run(const void* uq, const float* us, const void* w2, const f
   prm.tiles_col = static_cast<int>(dim / 256);
   prm.grid = d->sm_count;
   prm.vec_store = (dim % 8 == 0 && is_aligned(out, 16)) ? 1 : 0;
+  prm.vec_scales = 0;
   CUtensorMap ml, mc;
   if (!make_kmajor_map(&ml, uq, static_cast<uint64_t>(rows), static_cast<uint64_t>(inter), 128) ||
       !make_kmajor_map(&mc, w2, static_cast<uint64_t>(E * dim), static_cast<uint64_t>(inter), 256))

@@ -525,21 +525,39 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const float* __restrict
   __syncthreads();
   if (!last) return;
   __threadfence();
-  int total = 0;
-  if (tid < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      int* h = hist + static_cast<size_t>(c) * E + tid;
-      const int v = __ldcg(h);
-      *h = total;
-      total += v;
-    }
+  // Bases of every (chunk, expert): thread (s, e) takes expert e and the s-th
+  // of kSlices ranges of chunks; the ranges' sums are scanned per expert (in
+  // shared memory, reusing wtab), the totals over experts.
+  constexpr int kSlices = 1024 / E;
+  const int e_t = tid % E, s_t = tid / E;  // threads past kSlices * E take no chunks
+  const int c0 = s_t < kSlices ? static_cast<int>(static_cast<long long>(s_t) * nchunks / kSlices) : 0;
+  const int c1 = s_t < kSlices ? static_cast<int>(static_cast<long long>(s_t + 1) * nchunks / kSlices) : 0;
+  int part = 0;
+  for (int c = c0; c < c1; ++c) part += __ldcg(hist + static_cast<size_t>(c) * E + e_t);
+  __syncthreads();
+  if (s_t < kSlices) wtab[s_t * E + e_t] = part;
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int q = 0; q < kSlices; ++q) {
+    const int v = wtab[q * E + e_t];
+    before += q < s_t ? v : 0;
+    total += v;
   }
   int rows;
-  const int off = block_exclusive_scan(total, wsum, &rows);
+  const int off = block_exclusive_scan(tid < E ? total : 0, wsum, &rows);
   if (tid < E) {
     counts[tid] = total;
     offsets[tid] = off;
-    for (int c = 0; c < nchunks; ++c) hist[static_cast<size_t>(c) * E + tid] += off;
+  }
+  __syncthreads();
+  if (tid < E) wtab[tid] = off;  // expert offsets, for every slice's threads
+  __syncthreads();
+  int run = wtab[e_t] + before;
+  for (int c = c0; c < c1; ++c) {
+    int* h = hist + static_cast<size_t>(c) * E + e_t;
+    const int v = __ldcg(h);
+    *h = run;
+    run += v;
   }
   if (tid == 0) {
     offsets[E] = rows;
