@@ -7,12 +7,16 @@
 // sum is fp32 (a bf16 product accumulated in fp32).
 //
 // The tensor cores take bf16 x bf16 (tcgen05.mma kind::f16, both operands
-// bf16): the FP8 weight tile is TMA-loaded as bytes, dequantised by four warps
-// into a bf16 K-major 128-byte-swizzled tile in shared memory (transposed in
-// the qk case, where W's rows are the K dimension), and fed to the MMA next to
-// the TMA-loaded bf16 activation tile. One CTA per (head, 128-token tile,
-// 128-column tile); the fp32 accumulator stays in TMEM over the whole K
-// (no per-block promotion: the block scale is inside the dequantised weight).
+// bf16): the FP8 weight tile is TMA-loaded as bytes, dequantised row by row by
+// four warps into a bf16 128-byte-swizzled tile in shared memory, and fed to
+// the MMA next to the TMA-loaded bf16 activation tile. W's rows are the N
+// dimension for v (a K-major operand) and the K dimension for qk (W keeps its
+// layout and is read as an MN-major operand, so no transpose). Persistent
+// CTAs, one per SM, walk the tiles of (head, 128-token tile, 128-column
+// tile); a tile's fp32 accumulator stays in TMEM over its whole K (no
+// per-block promotion: the block scale is inside the dequantised weight), in
+// one of two buffers, so a tile's stores overlap the next tile's loads,
+// dequantisation and MMAs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -29,21 +33,37 @@
 namespace fp8blk {
 namespace {
 
-constexpr int kMlaThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2-5 dequant + epilogue
+constexpr int kMlaThreads = 352;  // warp 0 activation TMA, 1 MMA, 2-5 dequant, 6-9 epilogue, 10 weight TMA
 constexpr int kAHalf = 128 * 128;                // 128 rows x 64 bf16 (one 128-byte swizzled half)
 constexpr int kATile = 2 * kAHalf;               // 128 token rows x 128 bf16
-constexpr int kB8Tile = 128 * 128;               // 128 x 128 e4m3, unswizzled rows of 128 bytes
+constexpr int kB8Tile = 128 * 128;               // 128 x 128 e4m3
 constexpr int kB16Tile = 2 * kAHalf;             // the dequantised weight tile, K-major, two halves
-constexpr int kMlaStageBytes = kATile + kB8Tile + kB16Tile;
-// Stages: one for qk (a single K block, so two CTAs fit on an SM), two for v.
-__host__ __device__ constexpr int mla_smem(int stages) { return 1024 + stages * kMlaStageBytes + (3 * stages + 2) * 8 + 16; }
+// The epilogue's staging tile: per epilogue warp, its 32 output rows x 128
+// bf16 as two 64-column halves of 32 rows x 128 bytes, 128-byte swizzled (the
+// TMA store's box).
+constexpr int kOutHalf = 32 * 128;
+constexpr int kOutWarp = 2 * kOutHalf;
+constexpr int kOutBytes = 4 * kOutWarp;
+// Three rings, one entry per (tile, K block) step: activation tiles (freed by
+// the MMAs), e4m3 weight tiles (freed once dequantised) and bf16 weight tiles
+// (freed by the MMAs). The weight stream runs ahead of the MMAs by up to
+// kWRing + kBRing steps, the activation stream by kARing.
+constexpr int kARing = 3, kWRing = 2, kBRing = 2;
+constexpr int kOffW = kARing * kATile;
+constexpr int kOffB = kOffW + kWRing * kB8Tile;
+constexpr int kOffO = kOffB + kBRing * kB16Tile;
+constexpr int kOffBar = kOffO + kOutBytes;
+constexpr int kNumBars = 2 * (kARing + kWRing + kBRing) + 4 + 1;
+constexpr int kMlaSmem = 1024 + kOffBar + kNumBars * 8 + 16;
+static_assert(kMlaSmem <= 232448, "shared memory per CTA");
 constexpr unsigned kDevErrTimeoutMla = 1u << 6;
 
 // kind::f16 instruction descriptor: f32 accumulator, A and B both bf16 (one
-// value sets both format fields), both K-major, an M x N tile.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// value sets both format fields), A K-major, B K-major or (b_mn) MN-major
+// (bit 16), an M x N tile.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn) {
   constexpr uint32_t kBf16 = 1;
-  return (1u << 4) | (kBf16 << 7) | (kBf16 << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+  return (1u << 4) | (kBf16 << 7) | (kBf16 << 10) | (b_mn ? 1u << 16 : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -68,57 +88,95 @@ struct MlaParams {
   int n_tiles, m_tiles;   // column tiles (qk C / 128, v 1), 128-token tiles
 };
 
-// Byte offset of element (row r, k) of a K-major bf16 tile of 128 rows x 128
-// k: two halves of 64 k (128-byte rows), 8-row atoms of 1024 bytes, 16-byte
-// chunk c of row r stored at chunk c ^ (r % 8).
-__device__ __forceinline__ uint32_t b16_chunk_offset(int r, int q) {  // q: 16-byte chunk 0..15 (8 k each)
+// Byte offset of 16-byte chunk q (elements 8q .. 8q + 7) of row r of a bf16
+// tile of 128 rows x 128 elements, 128-byte swizzled: two halves of 64
+// elements (128-byte rows), 8-row atoms of 1024 bytes, chunk c of row r stored
+// at chunk c ^ (r % 8). For the v projection the rows are N and the elements
+// K (a K-major operand); for qk the rows are K and the elements N (an
+// MN-major operand with 16 KB between the halves and 1 KB between 8-row
+// groups).
+__device__ __forceinline__ uint32_t b16_chunk_offset(int r, int q) {
   return static_cast<uint32_t>((q >> 3) * kAHalf + (r >> 3) * 1024 + (r & 7) * 128 + (((q & 7) ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t dequant_pack2(uint8_t a, uint8_t b, float s) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(static_cast<uint16_t>(a) | (static_cast<uint16_t>(b) << 8)), __NV_E4M3);
+// Two e4m3 codes (the first in the low byte) times the block scale, as bf16x2.
+__device__ __forceinline__ uint32_t dequant_pack2(uint32_t pair, float s) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair & 0xFFFFu), __NV_E4M3);
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
   const __nv_bfloat162 r = __floats2bfloat162_rn(__fmul_rn(f.x, s), __fmul_rn(f.y, s));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int kMlaStages>
+// Persistent CTAs: CTA c takes tiles c, c + grid, ... of (head, 128-token
+// tile, 128-column tile), head-major, each KB K blocks long, as steps j =
+// (its i-th tile) * KB + kb. The MMA accumulates a tile in one of two TMEM
+// buffers, so the epilogue drains tile i while the loads, dequantisation and
+// MMAs of tile i + 1 go on.
+//
+// Launched with programmatic stream serialization: the weight tiles and
+// scales may be read while the previous kernel on the stream still runs; the
+// activations are loaded, and the output written, after it has completed.
 __global__ void __launch_bounds__(kMlaThreads, 1)
     mla_absorb_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_w,
-                      const MlaParams prm) {
+                      const __grid_constant__ CUtensorMap tmap_o, const MlaParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMlaStages * kMlaStageBytes);
-  uint64_t* bready = full + kMlaStages;
-  uint64_t* empty = bready + kMlaStages;
-  uint64_t* tfull = empty + kMlaStages;
-  uint64_t* drain = tfull + 1;
+  uint8_t* out_stage = smem + kOffO;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* a_empty = a_full + kARing;
+  uint64_t* w_full = a_empty + kARing;
+  uint64_t* w_empty = w_full + kWRing;
+  uint64_t* b_full = w_empty + kWRing;
+  uint64_t* b_empty = b_full + kBRing;
+  uint64_t* tfull = b_empty + kBRing;  // [2]: accumulator buffer complete
+  uint64_t* tempty = tfull + 2;        // [2]: accumulator buffer drained
+  uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bid = static_cast<int>(blockIdx.x);
-  const int nt = bid % prm.n_tiles;
-  const int mt = (bid / prm.n_tiles) % prm.m_tiles;
-  const int h = bid / (prm.n_tiles * prm.m_tiles);
   const int KB = prm.kb_count;
   const int kdim = prm.v_mode ? prm.C : 128;  // the activation's per-head width
+  const int per_head = prm.n_tiles * prm.m_tiles;
+  const int ntiles = prm.H * per_head;
+  const int grid = static_cast<int>(gridDim.x);
+  const int my_tiles = static_cast<int>(blockIdx.x) < ntiles ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / grid + 1 : 0;
+  const long long nsteps = static_cast<long long>(my_tiles) * KB;
+  auto tile_of = [&](int i, int& h, int& mt, int& nt) {
+    const int tt = static_cast<int>(blockIdx.x) + i * grid;
+    h = tt / per_head;
+    const int r = tt - h * per_head;
+    mt = r / prm.n_tiles;
+    nt = r - mt * prm.n_tiles;
+  };
+  // Parity of the n-th completion (n >= 0) of a ring entry used every `depth` steps.
+  auto use_parity = [](long long j, int depth) { return static_cast<uint32_t>((j / depth) & 1); };
 
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kMlaStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&bready[s], 4);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kARing; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1);
     }
-    mbar_init(tfull, 1);
+    for (int s = 0; s < kWRing; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 4);
+    }
+    for (int s = 0; s < kBRing; ++s) {
+      mbar_init(&b_full[s], 4);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -126,135 +184,204 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == 10) {
+    // ---------------- TMA producers: activations (warp 0), weights (warp 10) ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_a);
-      tma_prefetch_desc(&tmap_w);
-      int issued = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int st = kb % kMlaStages;
-        if (kb >= kMlaStages &&
-            !mbar_wait(&empty[st], ((kb / kMlaStages) & 1) ^ 1u, abort_flag, prm.err, kDevErrTimeoutMla))
+      const bool act = warp == 0;
+      const int depth = act ? kARing : kWRing;
+      uint64_t* full = act ? a_full : w_full;
+      uint64_t* empty = act ? a_empty : w_empty;
+      if (act) {
+        tma_prefetch_desc(&tmap_a);
+        griddep_wait();  // the activations come from the previous kernel
+      } else {
+        tma_prefetch_desc(&tmap_w);
+      }
+      long long j = 0;
+      for (; j < nsteps; ++j) {
+        const int i = static_cast<int>(j / KB), kb = static_cast<int>(j - static_cast<long long>(i) * KB);
+        int h, mt, nt;
+        tile_of(i, h, mt, nt);
+        const int st = static_cast<int>(j % depth);
+        if (j >= depth &&
+            !mbar_wait(&empty[st], use_parity(j, depth) ^ 1u, abort_flag, prm.err, kDevErrTimeoutMla))
           break;
-        uint8_t* sa = smem + st * kMlaStageBytes;
-        mbar_arrive_expect_tx(&full[st], kATile + kB8Tile);
-        const int ax = h * kdim + kb * 128;
-        tma_load_2d(sa, &tmap_a, &full[st], ax, mt * 128);
-        tma_load_2d(sa + kAHalf, &tmap_a, &full[st], ax + 64, mt * 128);
-        if (prm.v_mode) tma_load_2d(sa + kATile, &tmap_w, &full[st], kb * 128, h * 256 + 128);
-        else tma_load_2d(sa + kATile, &tmap_w, &full[st], nt * 128, h * 256);
-        ++issued;
+        if (act) {
+          uint8_t* sa = smem + st * kATile;
+          mbar_arrive_expect_tx(&full[st], kATile);
+          const int ax = h * kdim + kb * 128;
+          tma_load_2d(sa, &tmap_a, &full[st], ax, mt * 128);
+          tma_load_2d(sa + kAHalf, &tmap_a, &full[st], ax + 64, mt * 128);
+        } else {
+          uint8_t* sw = smem + kOffW + st * kB8Tile;
+          mbar_arrive_expect_tx(&full[st], kB8Tile);
+          if (prm.v_mode) tma_load_2d(sw, &tmap_w, &full[st], kb * 128, h * 256 + 128);
+          else tma_load_2d(sw, &tmap_w, &full[st], nt * 128, h * 256);
+        }
       }
       // No copy may still be landing when the CTA exits.
-      for (int i = issued - 1; i >= 0 && i >= issued - kMlaStages; --i)
-        mbar_wait(&full[i % kMlaStages], static_cast<uint32_t>((i / kMlaStages) & 1), nullptr, prm.err,
-                  kDevErrTimeoutMla);
+      for (long long q = j - 1; q >= 0 && q >= j - depth; --q)
+        mbar_wait(&full[q % depth], use_parity(q, depth), nullptr, prm.err, kDevErrTimeoutMla);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     const bool leader = elect_one_sync();
-    constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128);
-    for (int kb = 0; kb < KB; ++kb) {
-      const int st = kb % kMlaStages;
-      const bool w =
-          mbar_wait(&bready[st], static_cast<uint32_t>((kb / kMlaStages) & 1), abort_flag, prm.err, kDevErrTimeoutMla);
-      if (!__all_sync(0xFFFFFFFFu, w)) break;
-      tc_fence_after_sync();
-      const uint32_t a_addr = smem_u32(smem + st * kMlaStageBytes);
-      const uint32_t b_addr = a_addr + kATile + kB8Tile;
-      if (leader) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint64_t ad = sdesc_kmajor_sw128(a_addr + half * kAHalf);
-          const uint64_t bd = sdesc_kmajor_sw128(b_addr + half * kAHalf);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)  // 16 bf16 = 32 bytes per MMA: the start address advances by 2 x 16 B
-            mma_bf16(tmem_base, ad + 2 * k, bd + 2 * k, kIdesc, (kb | half | k) != 0 ? 1u : 0u);
-        }
-        mma_commit(&empty[st]);
-        if (kb == KB - 1) mma_commit(tfull);
+    constexpr uint32_t kIdescK = idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t kIdescMN = idesc_bf16_f32(128, 128, true);
+    long long j = 0;
+    bool ok = true;
+    for (int i = 0; ok && i < my_tiles; ++i) {
+      const int b = i & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tempty[b], static_cast<uint32_t>(((i >> 1) & 1) ^ 1), abort_flag,
+                                             prm.err, kDevErrTimeoutMla))) {
+        ok = false;
+        break;
       }
-      __syncwarp();
+      tc_fence_after_sync();
+      const uint32_t d = tmem_base + static_cast<uint32_t>(b * 128);
+      for (int kb = 0; kb < KB; ++kb, ++j) {
+        const int sa = static_cast<int>(j % kARing), sb = static_cast<int>(j % kBRing);
+        if (!__all_sync(0xFFFFFFFFu,
+                        mbar_wait(&a_full[sa], use_parity(j, kARing), abort_flag, prm.err, kDevErrTimeoutMla) &&
+                            mbar_wait(&b_full[sb], use_parity(j, kBRing), abort_flag, prm.err, kDevErrTimeoutMla))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_addr = smem_u32(smem + sa * kATile);
+        const uint32_t b_addr = smem_u32(smem + kOffB + sb * kB16Tile);
+        if (leader) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint64_t ad = sdesc_kmajor_sw128(a_addr + half * kAHalf);
+            const uint64_t bd = sdesc_kmajor_sw128(b_addr + half * kAHalf);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              // 16 K per MMA. A (and B for v): 32 bytes along the K-major row,
+              // the descriptor's start address advances by 2 x 16 B. B for qk:
+              // 16 K rows, two 1 KB groups of the MN-major tile.
+              const uint32_t acc = (kb | half | k) != 0 ? 1u : 0u;
+              if (prm.v_mode)
+                mma_bf16(d, ad + 2 * k, bd + 2 * k, kIdescK, acc);
+              else
+                mma_bf16(d, ad + 2 * k, sdesc_mnmajor_sw128(b_addr + (half * 4 + k) * 2048, kAHalf, 1024), kIdescMN,
+                         acc);
+            }
+          }
+          mma_commit(&a_empty[sa]);
+          mma_commit(&b_empty[sb]);
+          if (kb == KB - 1) mma_commit(&tfull[b]);
+        }
+        __syncwarp();
+      }
     }
     if (leader) {  // every MMA done before TMEM is released
       mma_commit(drain);
       mbar_wait(drain, 0, nullptr, prm.err, kDevErrTimeoutMla);
     }
     __syncwarp();
-  } else {
-    // ---------------- weight dequant, then the epilogue ----------------
-    const int n = (warp - 2) * 32 + lane;  // the dequantised tile's row (MMA N index)
+  } else if (warp < 6) {
+    // ---------------- weight dequantisation ----------------
+    // Thread r converts row r of the e4m3 tile into row r of the bf16 tile:
+    // for v, row r is output column d = r (N) over 128 c (K); for qk, row r
+    // is d = r (K) over 128 output columns c (N).
+    const int r = (warp - 2) * 32 + lane;
     const int cblocks = prm.C / 128;
-    bool ok = true;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int st = kb % kMlaStages;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], static_cast<uint32_t>((kb / kMlaStages) & 1), abort_flag,
-                                             prm.err, kDevErrTimeoutMla))) {
-        ok = false;
-        break;
-      }
-      const uint8_t* b8 = smem + st * kMlaStageBytes + kATile;
-      uint8_t* b16 = smem + st * kMlaStageBytes + kATile + kB8Tile;
-      // qk: W rows h*256 + d (d = K), columns nt*128 + n; v: rows h*256 + 128 + n, columns kb*128 + k.
+    for (long long j = 0; j < nsteps; ++j) {
+      const int i = static_cast<int>(j / KB), kb = static_cast<int>(j - static_cast<long long>(i) * KB);
+      int h, mt, nt;
+      tile_of(i, h, mt, nt);
+      const int sw = static_cast<int>(j % kWRing), sb = static_cast<int>(j % kBRing);
+      // qk: W rows h*256 + d, columns nt*128 + c; v: rows h*256 + 128 + d, columns kb*128 + c.
       const float s = prm.v_mode ? __ldg(prm.ws + static_cast<size_t>(2 * h + 1) * cblocks + kb)
                                  : __ldg(prm.ws + static_cast<size_t>(2 * h) * cblocks + nt);
+      if (!__all_sync(0xFFFFFFFFu,
+                      mbar_wait(&w_full[sw], use_parity(j, kWRing), abort_flag, prm.err, kDevErrTimeoutMla) &&
+                          (j < kBRing || mbar_wait(&b_empty[sb], use_parity(j, kBRing) ^ 1u, abort_flag, prm.err,
+                                                   kDevErrTimeoutMla))))
+        break;
+      const uint8_t* b8 = smem + kOffW + sw * kB8Tile;
+      uint8_t* b16 = smem + kOffB + sb * kB16Tile;
+      // The e4m3 tile is 128-byte swizzled by the TMA: 16-byte chunk c of row
+      // r (16 elements) sits at chunk c ^ (r % 8).
 #pragma unroll 4
-      for (int q = 0; q < 16; ++q) {  // 8 k per 16-byte chunk
-        uint8_t v8[8];
-        if (prm.v_mode) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(b8 + n * 128 + q * 8);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            v8[i] = static_cast<uint8_t>(raw.x >> (8 * i));
-            v8[4 + i] = static_cast<uint8_t>(raw.y >> (8 * i));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v8[i] = b8[(q * 8 + i) * 128 + n];  // column n of rows k: the transpose
-        }
-        const uint4 packed = make_uint4(dequant_pack2(v8[0], v8[1], s), dequant_pack2(v8[2], v8[3], s),
-                                        dequant_pack2(v8[4], v8[5], s), dequant_pack2(v8[6], v8[7], s));
-        *reinterpret_cast<uint4*>(b16 + b16_chunk_offset(n, q)) = packed;
+      for (int c = 0; c < 8; ++c) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(b8 + r * 128 + ((c ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(b16 + b16_chunk_offset(r, 2 * c)) =
+            make_uint4(dequant_pack2(raw.x, s), dequant_pack2(raw.x >> 16, s), dequant_pack2(raw.y, s),
+                       dequant_pack2(raw.y >> 16, s));
+        *reinterpret_cast<uint4*>(b16 + b16_chunk_offset(r, 2 * c + 1)) =
+            make_uint4(dequant_pack2(raw.z, s), dequant_pack2(raw.z >> 16, s), dequant_pack2(raw.w, s),
+                       dequant_pack2(raw.w >> 16, s));
       }
-      fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bready[st]);
+      if (lane == 0) mbar_arrive(&w_empty[sw]);  // the e4m3 tile is read
+      fence_proxy_async_smem();                   // generic-proxy writes, read next by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b_full[sb]);
     }
-    if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(tfull, 0, abort_flag, prm.err, kDevErrTimeoutMla))) {
+  } else {
+    // ---------------- epilogue ----------------
+    // Each warp drains its 32 TMEM lanes (tokens) into its own staging slab,
+    // then one lane stores the slab with two TMA boxes of 32 rows x 64 columns.
+    griddep_wait();  // no output is written before the previous kernel has completed
+    const int quarter = warp & 3;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int nout = prm.v_mode ? 128 : prm.C;
+    uint8_t* slab = out_stage + quarter * kOutWarp;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int b = i & 1;
+      int h, mt, nt;
+      tile_of(i, h, mt, nt);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[b], static_cast<uint32_t>((i >> 1) & 1), abort_flag, prm.err,
+                                             kDevErrTimeoutMla)))
+        break;
       tc_fence_after_sync();
-      const int quarter = warp & 3;
-      const int r = mt * 128 + quarter * 32 + lane;  // token
-      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-      const int nout = prm.v_mode ? 128 : prm.C;
-      __nv_bfloat16* dst = prm.out + (static_cast<size_t>(r) * prm.H + h) * nout + nt * 128;
+      if (lane == 0) bulk_wait_group_read0();  // the previous tile's stores have read the slab
+      __syncwarp();
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0), v);
-        if (r < prm.T) {
+        tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(b * 128 + c0), v);
+        if (c0 == 96) {  // the buffer's last columns are in registers: free it for tile i + 2
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[b]);
+        }
+        uint8_t* row = slab + (c0 >> 6) * kOutHalf + lane * 128;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t w4[4];
+        for (int g = 0; g < 4; ++g) {  // 16-byte chunk ((c0 % 64) / 8 + g) of the row, at chunk ^ (lane % 8)
+          uint32_t w4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 b =
-                  __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * e]), __uint_as_float(v[g * 8 + 2 * e + 1]));
-              w4[e] = *reinterpret_cast<const uint32_t*>(&b);
-            }
-            *reinterpret_cast<uint4*>(dst + c0 + g * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 bb =
+                __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * e]), __uint_as_float(v[g * 8 + 2 * e + 1]));
+            w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
           }
+          const int chunk = ((c0 & 63) >> 3) + g;
+          *reinterpret_cast<uint4*>(row + ((chunk ^ (lane & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
+      fence_proxy_async_smem();  // the slab's generic-proxy writes, read next by the TMA
+      __syncwarp();
+      const int y = mt * 128 + quarter * 32;
+      if (lane == 0 && y < prm.T) {  // rows past T inside the box are clipped by the TMA
+        const int x = h * nout + nt * 128;
+        tma_store_2d(&tmap_o, slab, x, y);
+        tma_store_2d(&tmap_o, slab + kOutHalf, x + 64, y);
+        bulk_commit_group();
+      }
     }
+    if (lane == 0) bulk_wait_group0();  // every store written before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 128);
+    tmem_dealloc(tmem_base, 256);
   }
 }
 
@@ -301,19 +428,22 @@ int mla_run(const void* in, const void* w, const float* ws, void* out, int64_t T
   if (int st = current_device(&d)) return st;
   static bool attr_done[64] = {};
   if (d->device >= 64 || !attr_done[d->device]) {
-    if (cudaFuncSetAttribute(mla_absorb_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla_smem(1)) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(mla_absorb_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mla_smem(2)) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(mla_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem) !=
+        cudaSuccess)
       return FP8BLK_ERR_CUDA;
     if (d->device < 64) attr_done[d->device] = true;
   }
   const int64_t kdim = v_mode ? C : dn;
-  CUtensorMap ma, mw;
+  const int64_t nout = v_mode ? dv : C;
+  // The e4m3 tile is read a row per thread: 128-byte swizzled so a warp's
+  // 16-byte reads spread over the banks.
+  CUtensorMap ma, mw, mo;
   if (!make_map_2d(&ma, in, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(T),
                    static_cast<uint64_t>(H * kdim), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&mw, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(H * (dn + dv)),
-                   static_cast<uint64_t>(C), 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   static_cast<uint64_t>(C), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(T),
+                   static_cast<uint64_t>(H * nout), 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return FP8BLK_ERR_CUDA;
   MlaParams prm{};
   prm.ws = ws;
@@ -326,11 +456,21 @@ int mla_run(const void* in, const void* w, const float* ws, void* out, int64_t T
   prm.kb_count = static_cast<int>(kdim / 128);
   prm.n_tiles = v_mode ? 1 : static_cast<int>(C / 128);
   prm.m_tiles = static_cast<int>((T + 127) / 128);
-  const int64_t grid = H * prm.m_tiles * prm.n_tiles;
-  if (grid > (int64_t{1} << 31) - 1) return FP8BLK_ERR_SHAPE;
-  if (v_mode) mla_absorb_kernel<2><<<static_cast<unsigned>(grid), kMlaThreads, mla_smem(2), stream>>>(ma, mw, prm);
-  else mla_absorb_kernel<1><<<static_cast<unsigned>(grid), kMlaThreads, mla_smem(1), stream>>>(ma, mw, prm);
-  return launch_status();
+  const int64_t tiles = H * prm.m_tiles * prm.n_tiles;
+  if (tiles > (int64_t{1} << 31) - 1) return FP8BLK_ERR_SHAPE;
+  // Persistent: one CTA per SM (the rings' shared memory), at most one per tile.
+  const int grid = static_cast<int>(tiles < d->sm_count ? tiles : d->sm_count);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kMlaThreads);
+  cfg.dynamicSmemBytes = kMlaSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, mla_absorb_kernel, ma, mw, mo, prm));
 }
 
 }  // namespace

@@ -29,11 +29,12 @@
  *   - Sizes of 0 are valid and launch nothing (except where noted).
  *   - Not thread-safe per workspace: calls that share a workspace must be
  *     ordered on one stream.
- *   - Overlap on a stream: the GEMM kernels (and act_quant inside
- *     fp8blk_linear / fp8blk_ffn) let the next kernel of this library on the
- *     same stream start early (programmatic dependent launch). That kernel
- *     may begin loading its WEIGHT operands (w, w1, w3, w2) before the
- *     previous one has finished; it reads activations and scales, and writes
+ *   - Overlap on a stream: the GEMM kernels, the MLA absorb kernels (and
+ *     act_quant inside fp8blk_linear / fp8blk_ffn) let the next kernel of
+ *     this library on the same stream start early (programmatic dependent
+ *     launch). That kernel may begin loading its WEIGHT operands (w, w1, w3,
+ *     w2; wkv_b and its scales for the MLA absorb) before the previous one
+ *     has finished; it reads activations and activation scales, and writes
  *     anything, only after. Inside fp8blk_linear / fp8blk_ffn the GEMM's
  *     weight loads may even start while the library call before is still
  *     running. So a weight operand must not be the output of either of the

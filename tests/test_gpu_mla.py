@@ -1,9 +1,11 @@
 """GPU parity of the MLA absorb projections against the CPU oracle.
 
 Both sides use the dequantised weight bf16(fp32(code) * scale) and bf16
-activations. The oracle sums the exact products in fp64; the tensor cores sum
-them in fp32. Tolerance per element: one bf16 step of the result (2^-8 |ref|)
-plus 1e-3 of the output's rms for sums that cancel."""
+activations. The oracle rounds the exact (fp64) sum to bf16; the kernel rounds
+its fp32 sum to bf16. Where the two sums straddle a rounding boundary the
+results differ by one bf16 step, which is at most 2^-7 |ref| (the step of a
+value in [2^e, 2^(e+1)) is 2^(e-7)). Tolerance per element: 2^-7 |ref| plus
+1e-3 of the output's rms for sums that cancel."""
 import numpy as np
 import pytest
 import torch
@@ -22,7 +24,7 @@ def close(got_bits, ref_bits, rms=None, what=""):
     ref = synthetic.bf16_bits_to_f32(ref_bits).astype(np.float64)
     if rms is None:
         rms = float(np.sqrt(np.mean(ref ** 2)))
-    bad = np.abs(got - ref) > 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    bad = np.abs(got - ref) > 2.0 ** -7 * np.abs(ref) + 1e-3 * rms
     assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside, e.g. {got[bad][:4]} vs {ref[bad][:4]}"
 
 
@@ -34,7 +36,10 @@ def dev_w(wq, ws):
     return torch.from_numpy(wq).cuda().view(torch.float8_e4m3fn), torch.from_numpy(ws).cuda()
 
 
-@pytest.mark.parametrize("T,H,C", [(5, 3, 256), (130, 2, 512), (1, 4, 512), (257, 1, 128)])
+# (20, 320, 128) and (33, 160, 256): 320 tiles, more than one per SM, so
+# persistent CTAs cycle both accumulator buffers and the operand ring.
+@pytest.mark.parametrize("T,H,C", [(5, 3, 256), (130, 2, 512), (1, 4, 512), (257, 1, 128), (20, 320, 128),
+                                   (33, 160, 256)])
 @pytest.mark.parametrize("mode", ["qk", "v"])
 def test_mla_full_compare(T, H, C, mode):
     wq, ws = weights(H, C, 300 + T + H)
@@ -66,6 +71,32 @@ def test_mla_full_size_sampled(T, mode):
     # rms of the whole output, estimated from the oracle's sampled rows
     rms = float(np.sqrt(np.mean(synthetic.bf16_bits_to_f32(ref).astype(np.float64) ** 2)))
     close(got, ref, rms=rms, what=f"mla {mode} sampled T={T}")
+    assert fb.last_device_error() == 0
+
+
+def test_mla_chain_reads_the_previous_kernels_output():
+    """qk then v on its output, back to back on one stream: the v kernel may
+    start while qk still runs (it loads wkv_b early) but must read qk's
+    output only once qk has completed, and qk may overwrite its output only
+    after the v launch before it has read it. Checked against the same calls
+    with a synchronisation between them, over several rounds that reuse the
+    buffers."""
+    T, H, C = 300, 128, 512
+    wq, ws = weights(H, C, 500)
+    w, s = dev_w(wq, ws)
+    qs = [bits_to_dev_bf16(synthetic.activations(T, H * DN, 501 + r)).view(T, H, DN) for r in range(3)]
+    mid = torch.empty((T, H, C), dtype=torch.bfloat16, device="cuda")
+    outs = [torch.empty((T, H, DV), dtype=torch.bfloat16, device="cuda") for _ in qs]
+    for q, o in zip(qs, outs):
+        fb.mla_absorb(q, w, s, "qk", out=mid)
+        fb.mla_absorb(mid, w, s, "v", out=o)
+    torch.cuda.synchronize()
+    for q, o in zip(qs, outs):
+        m = fb.mla_absorb(q, w, s, "qk")
+        torch.cuda.synchronize()
+        ref = fb.mla_absorb(m, w, s, "v")
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
     assert fb.last_device_error() == 0
 
 
