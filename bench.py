@@ -255,6 +255,7 @@ KERNEL_SOURCES = {
     "swiglu_gemm": ("gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
     "linear_fused": ("api.cu", "gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
     "weight_dequant": ("quant.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
+    "mla": ("mla.cu", "ptx.cuh", "host.cuh"),
     "moe_step": None,
 }
 
@@ -744,7 +745,8 @@ def run_mla(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
         roof = {"bound": "tensor", "achieved": flops / per / 1e12, "peak": peaks["bf16"], "unit": "TFLOP/s",
                 "frac": flops / per / 1e12 / peaks["bf16"],
                 "peak_source": f"bf16_tflops ({peaks['src']}): the products are bf16"}
-    roof.update({"kernel": "mla_absorb_kernel (qk + v)", "traffic": None, "algorithmic_bytes_per_launch": b // 2,
+    roof.update({"kernel": "mla_absorb_kernel (qk + v)", "traffic": recorded_traffic(args.workload, "mla"),
+                 "algorithmic_bytes_per_launch": b // 2,
                  "kernel_us": per / 2 * 1e6})
     return {
         "value": value, "unit": unit, "ms_per_step": el_max / steps * 1e3, "clocks": clocks,

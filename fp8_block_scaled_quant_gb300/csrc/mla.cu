@@ -33,7 +33,9 @@
 namespace fp8blk {
 namespace {
 
-constexpr int kMlaThreads = 352;  // warp 0 activation TMA, 1 MMA, 2-5 dequant, 6-9 epilogue, 10 weight TMA
+// Warps: 0 activation TMA, 1 MMA, 2-5 and 11-14 dequant, 6-9 epilogue, 10 weight TMA.
+constexpr int kMlaThreads = 480;
+constexpr int kDequantWarps = 8;
 constexpr int kAHalf = 128 * 128;                // 128 rows x 64 bf16 (one 128-byte swizzled half)
 constexpr int kATile = 2 * kAHalf;               // 128 token rows x 128 bf16
 constexpr int kB8Tile = 128 * 128;               // 128 x 128 e4m3
@@ -57,6 +59,38 @@ constexpr int kNumBars = 2 * (kARing + kWRing + kBRing) + 4 + 1;
 constexpr int kMlaSmem = 1024 + kOffBar + kNumBars * 8 + 16;
 static_assert(kMlaSmem <= 232448, "shared memory per CTA");
 constexpr unsigned kDevErrTimeoutMla = 1u << 6;
+
+// 2-D tiled store of the box at (x, y) from shared memory, tracked in the
+// issuing thread's bulk async-group; rows and columns past the tensor's extent
+// are not written. x and y must not be negative.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// The issuing thread's bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for an MN-major operand tile with 128-byte
+// swizzling: each 128-byte row holds 64 consecutive M/N elements (16-bit) of
+// one K index, 8 K rows form a 1024-byte swizzle atom; `lbo` is the byte
+// stride between 64-element blocks along M/N, `sbo` the byte stride between
+// 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
 
 // kind::f16 instruction descriptor: f32 accumulator, A and B both bf16 (one
 // value sets both format fields), A K-major, B K-major or (b_mn) MN-major
@@ -160,10 +194,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
     for (int s = 0; s < kWRing; ++s) {
       mbar_init(&w_full[s], 1);
-      mbar_init(&w_empty[s], 4);
+      mbar_init(&w_empty[s], kDequantWarps);
     }
     for (int s = 0; s < kBRing; ++s) {
-      mbar_init(&b_full[s], 4);
+      mbar_init(&b_full[s], kDequantWarps);
       mbar_init(&b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -281,12 +315,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mbar_wait(drain, 0, nullptr, prm.err, kDevErrTimeoutMla);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp > 10) {
     // ---------------- weight dequantisation ----------------
-    // Thread r converts row r of the e4m3 tile into row r of the bf16 tile:
-    // for v, row r is output column d = r (N) over 128 c (K); for qk, row r
-    // is d = r (K) over 128 output columns c (N).
-    const int r = (warp - 2) * 32 + lane;
+    // Row r of the e4m3 tile becomes row r of the bf16 tile: for v, row r is
+    // output column d = r (N) over 128 c (K); for qk, row r is d = r (K) over
+    // 128 output columns c (N). Two warps share each row range (one on each
+    // half of the row), one pair per SM sub-partition.
+    const int dw = warp < 6 ? warp - 2 : warp - 7;  // 0..7
+    const int r = (dw & 3) * 32 + lane;
+    const int c_lo = (dw >> 2) * 4;
     const int cblocks = prm.C / 128;
     for (long long j = 0; j < nsteps; ++j) {
       const int i = static_cast<int>(j / KB), kb = static_cast<int>(j - static_cast<long long>(i) * KB);
@@ -305,8 +342,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       uint8_t* b16 = smem + kOffB + sb * kB16Tile;
       // The e4m3 tile is 128-byte swizzled by the TMA: 16-byte chunk c of row
       // r (16 elements) sits at chunk c ^ (r % 8).
-#pragma unroll 4
-      for (int c = 0; c < 8; ++c) {
+#pragma unroll
+      for (int c = c_lo; c < c_lo + 4; ++c) {
         const uint4 raw = *reinterpret_cast<const uint4*>(b8 + r * 128 + ((c ^ (r & 7)) << 4));
         *reinterpret_cast<uint4*>(b16 + b16_chunk_offset(r, 2 * c)) =
             make_uint4(dequant_pack2(raw.x, s), dequant_pack2(raw.x >> 16, s), dequant_pack2(raw.y, s),
@@ -373,7 +410,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         bulk_commit_group();
       }
     }
-    if (lane == 0) bulk_wait_group0();  // every store written before the CTA exits
+    if (lane == 0) bulk_wait_group_read0();  // the slab is read before the CTA's shared memory goes
     __syncwarp();
   }
 

@@ -121,26 +121,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// 2-D tiled store of the box at (x, y) from shared memory, tracked in the
-// issuing thread's bulk async-group; rows and columns past the tensor's extent
-// are not written. x and y must not be negative.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(x), "r"(y)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// The issuing thread's bulk stores have read their shared-memory sources.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// The issuing thread's bulk stores are complete (written to global memory).
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // The same box, written at the same shared-memory offset of every CTA of the
 // cluster in `cta_mask`; each destination's mbarrier at `bar`'s offset receives
 // the bytes that land in that CTA.
@@ -221,21 +201,6 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(1) << 16;
   d |= static_cast<uint64_t>(1024 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
-// Shared-memory matrix descriptor for an MN-major operand tile with 128-byte
-// swizzling: each 128-byte row holds 64 consecutive M/N elements (16-bit) of
-// one K index, 8 K rows form a 1024-byte swizzle atom; `lbo` is the byte
-// stride between 64-element blocks along M/N, `sbo` the byte stride between
-// 8-row groups along K.
-__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
