@@ -96,6 +96,7 @@ struct GemmParams {
   int sk_tiles;        // the remaining tiles run stream-K
   long long sk_iters;  // sk_tiles * Kb
   int vec_store;       // C rows 16-byte aligned and N % 8 == 0
+  int tma_store;       // kTmaStore tiles: C written by TMA through tmap_col2
   int vec_scales;      // Kb % 4 == 0 and the scale arrays 16-byte aligned: scales load four K blocks at a time
   int ue8m0;           // power-of-two scales for a fused act_quant (SwiGLU output, decode input)
   int whole_tiles;     // > 0: that many whole tiles, round-robin over the CTAs (no stream-K)
@@ -257,7 +258,14 @@ struct Cfg {
   static constexpr int kBarBytes = (2 * STAGES + 2 * P + 3) * 8 + 16 + (2 * kSfSlots + (MX ? 1 : 0)) * 8;
   // MX: the scale writers' exchange of activation-row scale words, double-buffered.
   static constexpr int kSfxBytes = MX ? 2 * 128 * 4 : 0;
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kGroupBytes + kXchgBytes + kSfxBytes;
+  // Dense bf16 tiles with activation rows as lanes store C through TMA: each
+  // epilogue warp stages 32 rows x 64 columns (a 4 KB, 128-byte-swizzled box)
+  // at a time after the stage ring.
+  static constexpr bool kTmaStore = !SWAP && !FUSED && !GROUPED && MODE == kEpiBf16;
+  static constexpr int kOutSlab = 32 * 128;
+  static constexpr int kOutStageBytes = kTmaStore ? EPI_WARPS * kOutSlab : 0;
+  static constexpr int kSmemBytes =
+      1024 + kRingBytes + kOutStageBytes + kBarBytes + kGroupBytes + kXchgBytes + kSfxBytes;
 
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(MODE == kEpiBf16 || !SWAP, "SwiGLU and scatter epilogues use activation rows as lanes");
@@ -355,9 +363,14 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 // Writes one thread's finished accumulators: row `row` of the tile, the
 // column group `group`. Returns false if an epilogue-wide wait gave up.
+// kTmaStore tiles with p.tma_store: the whole warp (all 32 rows, valid or
+// not) converts its rows 64 columns at a time into `slab` (row r's 16-byte
+// chunk c at chunk c ^ (r % 8), the 128-byte swizzle) and one lane stores the
+// box through `tmap_out`; rows past M and columns past N are clipped by the TMA.
 template <class C, class Sync>
 __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kCpt], const TileInfo& t, int group,
-                                         int row, float* xchg, uint32_t unit_parity, Sync&& epi_sync) {
+                                         int row, float* xchg, uint32_t unit_parity, Sync&& epi_sync, uint8_t* slab,
+                                         const CUtensorMap* tmap_out) {
   if constexpr (C::SWAP) {
     const int n = t.lane_y + row;
     if (row >= t.lane_valid) return true;  // rows past N
@@ -405,6 +418,37 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
     }
     return true;
   } else {
+    if constexpr (C::kTmaStore) {
+      if (p.tma_store) {
+        const int lane = row & 31;
+        const int y = t.lane_y + (row & ~31);             // the warp's first row
+        const bool any_row = (row & ~31) < t.lane_valid;  // warp-uniform
+#pragma unroll
+        for (int h = 0; h < C::kCpt / 64; ++h) {
+          const int x = t.col0 + group * C::kCpt + h * 64;
+          if (lane == 0) bulk_wait_group_read0();  // the slab's previous box has been read
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b =
+                  __floats2bfloat162_rn(acc[h * 64 + c * 8 + 2 * e], acc[h * 64 + c * 8 + 2 * e + 1]);
+              w[e] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            *reinterpret_cast<uint4*>(slab + lane * 128 + ((c ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes, read next by the TMA
+          __syncwarp();
+          if (lane == 0 && any_row && x < p.N) {
+            tma_store_2d(tmap_out, slab, x, y);
+            bulk_commit_group();
+          }
+        }
+        return true;
+      }
+    }
     if (row >= t.lane_valid) return true;
     const int r = t.lane_y + row;
     const size_t out_row = C::MODE == kEpiScatter ? static_cast<size_t>(__ldg(p.perm + r)) : static_cast<size_t>(r);
@@ -471,11 +515,14 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_lane, const __grid_constant__ CUtensorMap tmap_col,
                     const __grid_constant__ CUtensorMap tmap_col2, const GemmParams prm) {
+  // tmap_col2: the w3 operand (SwiGLU), or C as TMA stores see it (kTmaStore
+  // tiles with prm.tma_store), else unused.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
   // Fused decode: the quantised activation (all K blocks, BN token rows each,
   // 128-byte swizzled like a TMA tile) and its scales follow the stage ring.
-  uint8_t* act_smem = smem + C::kRingBytes;
+  uint8_t* out_stage = smem + C::kRingBytes;  // kTmaStore: one slab per epilogue warp
+  uint8_t* act_smem = out_stage + C::kOutStageBytes;
   float* act_scale = reinterpret_cast<float*>(act_smem + static_cast<size_t>(prm.Kb) * C::BN * 128);
   uint8_t* tail = act_smem + (C::FUSED ? fused_extra_bytes(prm.Kb, C::BN) : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(tail);
@@ -946,6 +993,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     constexpr int kAsRegs = (C::kCpt + 31) / 32;
+    uint8_t* out_slab = out_stage + ew * C::kOutSlab;  // kTmaStore: this warp's staging box
+    if constexpr (C::kTmaStore) {
+      if (prm.tma_store && lane == 0) tma_prefetch_desc(&tmap_col2);
+    }
 
     // Epilogue-wide barrier on an mbarrier (bounded wait, unlike bar.sync, so a
     // warp that gave up cannot strand the others).
@@ -1301,7 +1352,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < C::kCpt; ++i) part[(group * C::kCpt + i) * 128 + row] = acc[i];
       } else if (u.nparts == 1) {
-        ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync);
+        ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync, out_slab, &tmap_col2);
       } else {
         // Stream-K fixup: publish this part, count arrivals, the last part sums.
         float* mine = prm.slots + static_cast<size_t>(2 * blockIdx.x + (u.part == 0 ? 1 : 0)) * (C::BN * 128);
@@ -1326,12 +1377,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < C::kCpt; ++i) acc[i] += __ldcg(src + (group * C::kCpt + i) * 128 + row);
           }
-          ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync);
+          ok = finalize<C>(prm, acc, t, group, row, xchg, unit_parity, epi_sync, out_slab, &tmap_col2);
           if (ew == 0 && lane == 0) prm.counters[u.tile * C::CLUSTER + rank] = 0;
         }
       }
       FP8BLK_TOC(t_fin, t2);
       unit_parity ^= 1u;
+    }
+    if constexpr (C::kTmaStore) {
+      if (lane == 0) bulk_wait_group_read0();  // the slab is read before the CTA's shared memory goes
+      __syncwarp();
     }
 #ifdef FP8BLK_TRACE
     if (threadIdx.x == C::kEpiWarp0 * 32) {
@@ -1414,6 +1469,20 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
   const cuuint32_t box[2] = {128, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 output map for TMA stores: rows x cols (row stride cols * 2 bytes,
+// a multiple of 16), boxes of 32 rows x 64 columns, 128-byte swizzled.
+bool make_out_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1832,11 +1901,14 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
 
   if (!pl.swap) {
     const bool mx = mx_for(scale_fmt);
+    // C through TMA stores: boxes of 32 rows x 64 columns, rows of N bf16.
+    CUtensorMap mo = mc;
+    if (prm.vec_store && make_out_map(&mo, c, static_cast<uint64_t>(M), static_cast<uint64_t>(N))) prm.tma_store = 1;
     if (pl.cluster == 2)
-      return mx ? launch<CfgN256C2MX>(d, ml, mc, mc, prm, stream) : launch<CfgN256C2>(d, ml, mc, mc, prm, stream);
+      return mx ? launch<CfgN256C2MX>(d, ml, mc, mo, prm, stream) : launch<CfgN256C2>(d, ml, mc, mo, prm, stream);
     if (pl.bn == 256)
-      return mx ? launch<CfgN256MX>(d, ml, mc, mc, prm, stream) : launch<CfgN256>(d, ml, mc, mc, prm, stream);
-    return launch<CfgN128E8>(d, ml, mc, mc, prm, stream);
+      return mx ? launch<CfgN256MX>(d, ml, mc, mo, prm, stream) : launch<CfgN256>(d, ml, mc, mo, prm, stream);
+    return launch<CfgN128E8>(d, ml, mc, mo, prm, stream);
   }
   switch (pl.bn) {
     case 16: return launch<CfgS16>(d, ml, mc, mc, prm, stream, 0, pl.ksplit);

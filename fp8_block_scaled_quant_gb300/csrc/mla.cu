@@ -60,23 +60,6 @@ constexpr int kMlaSmem = 1024 + kOffBar + kNumBars * 8 + 16;
 static_assert(kMlaSmem <= 232448, "shared memory per CTA");
 constexpr unsigned kDevErrTimeoutMla = 1u << 6;
 
-// 2-D tiled store of the box at (x, y) from shared memory, tracked in the
-// issuing thread's bulk async-group; rows and columns past the tensor's extent
-// are not written. x and y must not be negative.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(x), "r"(y)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// The issuing thread's bulk stores have read their shared-memory sources.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // Shared-memory matrix descriptor for an MN-major operand tile with 128-byte
 // swizzling: each 128-byte row holds 64 consecutive M/N elements (16-bit) of
 // one K index, 8 K rows form a 1024-byte swizzle atom; `lbo` is the byte

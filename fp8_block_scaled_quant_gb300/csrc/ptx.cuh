@@ -121,6 +121,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 2-D tiled store of the box at (x, y) from shared memory, tracked in the
+// issuing thread's bulk async-group; rows and columns past the tensor's extent
+// are not written. x and y must not be negative.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// The issuing thread's bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // The same box, written at the same shared-memory offset of every CTA of the
 // cluster in `cta_mask`; each destination's mbarrier at `bar`'s offset receives
 // the bytes that land in that CTA.
