@@ -262,8 +262,14 @@ struct Cfg {
   // epilogue warp stages 32 rows x 64 columns (a 4 KB, 128-byte-swizzled box)
   // at a time after the stage ring.
   static constexpr bool kTmaStore = !SWAP && !FUSED && !GROUPED && MODE == kEpiBf16;
-  static constexpr int kOutSlab = 32 * 128;
-  static constexpr int kOutStageBytes = kTmaStore ? EPI_WARPS * kOutSlab : 0;
+  // The SwiGLU (u codes) and scatter (rows in slot order) epilogues write
+  // their rows through a 2 KB slab per warp instead (32 rows x 64 bytes),
+  // four lanes per row, eight rows per store instruction. (Not the MX scatter
+  // epilogue: its 200-register share cannot hold the staging next to the 128
+  // accumulators.)
+  static constexpr bool kSlabStore = !SWAP && (MODE == kEpiSwiGLU || (MODE == kEpiScatter && !MX));
+  static constexpr int kOutSlab = kTmaStore ? 32 * 128 : kSlabStore ? 32 * 64 : 0;
+  static constexpr int kOutStageBytes = EPI_WARPS * kOutSlab;
   static constexpr int kSmemBytes =
       1024 + kRingBytes + kOutStageBytes + kBarBytes + kGroupBytes + kXchgBytes + kSfxBytes;
 
@@ -361,6 +367,27 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return (lo & 0xFFFFu) | (hi << 16);
 }
 
+// Coalesced row stores of one warp: lane i holds four 16-byte chunks of row i
+// of the warp's 32. They go through `slab` (32 rows x 64 bytes; chunk c of row
+// r at position (c + r / 2) % 4, so eight consecutive lanes cover all banks in
+// both phases) and out eight rows per instruction, four lanes per row, to
+// dst (this lane's row; null for a row that is not written). Every lane of
+// the warp must call it.
+__device__ __forceinline__ void warp_store_rows(uint8_t* slab, int lane, const uint4 (&v)[4], uint8_t* dst) {
+  __syncwarp();  // the slab's previous contents have been read
+#pragma unroll
+  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(slab + lane * 64 + (((c + (lane >> 1)) & 3) << 4)) = v[c];
+  __syncwarp();
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), c = lane & 3;
+    const unsigned long long d = __shfl_sync(0xFFFFFFFFu, mine, r);
+    const uint4 val = *reinterpret_cast<const uint4*>(slab + r * 64 + (((c + (r >> 1)) & 3) << 4));
+    if (d) *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(d) + c * 16) = val;
+  }
+}
+
 // Writes one thread's finished accumulators: row `row` of the tile, the
 // column group `group`. Returns false if an epilogue-wide wait gave up.
 // kTmaStore tiles with p.tma_store: the whole warp (all 32 rows, valid or
@@ -400,22 +427,24 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
     amax = fmaxf(x[row], x[128 + row]);
     const float sc = quant_block_scale(amax, p.ue8m0 != 0);
     const float rc = __frcp_rn(sc);  // the block's quotients: see quotient.cuh
-    if (row < t.lane_valid) {
-      const size_t r = static_cast<size_t>(t.lane_y + row);
-      uint4* dst = reinterpret_cast<uint4*>(p.uq + r * p.ldc + t.col0 + group * 64);
+    // This row's 64 codes of the block (rows past the tile's valid rows are
+    // computed and not written).
+    uint4 q[4];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint32_t w[4];
+    for (int v = 0; v < 4; ++v) {
+      uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = v * 16 + e * 4;
-          w[e] = pack_e4m3x4(div_by_scale(acc[i], sc, rc), div_by_scale(acc[i + 1], sc, rc),
-                             div_by_scale(acc[i + 2], sc, rc), div_by_scale(acc[i + 3], sc, rc));
-        }
-        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int e = 0; e < 4; ++e) {
+        const int i = v * 16 + e * 4;
+        w[e] = pack_e4m3x4(div_by_scale(acc[i], sc, rc), div_by_scale(acc[i + 1], sc, rc),
+                           div_by_scale(acc[i + 2], sc, rc), div_by_scale(acc[i + 3], sc, rc));
       }
-      if (group == 0) p.us[r * (p.ldc / 128) + t.col0 / 128] = sc;
+      q[v] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    const bool valid = row < t.lane_valid;
+    const size_t r = static_cast<size_t>(t.lane_y + row);
+    warp_store_rows(slab, row & 31, q, valid ? p.uq + r * p.ldc + t.col0 + group * 64 : nullptr);
+    if (valid && group == 0) p.us[r * (p.ldc / 128) + t.col0 / 128] = sc;
     return true;
   } else {
     if constexpr (C::kTmaStore) {
@@ -445,6 +474,34 @@ __device__ __forceinline__ bool finalize(const GemmParams& p, float (&acc)[C::kC
             tma_store_2d(tmap_out, slab, x, y);
             bulk_commit_group();
           }
+        }
+        return true;
+      }
+    }
+    if constexpr (C::kSlabStore) {
+      if (p.vec_store && t.col0 + C::BN <= p.N) {  // warp-uniform: whole 16-byte chunks, all columns inside N
+        const bool valid = row < t.lane_valid;
+        uint8_t* base = nullptr;
+        if (valid) {
+          const int r = t.lane_y + row;
+          const size_t out_row = C::MODE == kEpiScatter ? static_cast<size_t>(__ldg(p.perm + r)) : static_cast<size_t>(r);
+          base = reinterpret_cast<uint8_t*>(p.c + out_row * p.ldc + t.col0 + group * C::kCpt);
+        }
+#pragma unroll
+        for (int q = 0; q < C::kCpt / 32; ++q) {  // 32 columns (64 bytes) per round
+          uint4 v[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b =
+                  __floats2bfloat162_rn(acc[q * 32 + c * 8 + 2 * e], acc[q * 32 + c * 8 + 2 * e + 1]);
+              w[e] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            v[c] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          warp_store_rows(slab, row & 31, v, base ? base + q * 64 : nullptr);
         }
         return true;
       }
