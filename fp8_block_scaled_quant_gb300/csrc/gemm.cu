@@ -367,6 +367,36 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return (lo & 0xFFFFu) | (hi << 16);
 }
 
+// A shared-memory counter written by one thread with release semantics and
+// read with acquire semantics by others.
+__device__ __forceinline__ void st_release_shared(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// Waits until *p > k, bounded like mbar_wait: gives up after kWaitLimitNs (or
+// once another role has given up), setting *abort and the error bit `code`.
+__device__ __forceinline__ bool wait_count_above(const int* p, int k, volatile int* abort, unsigned* err,
+                                                 unsigned code) {
+  if (ld_acquire_shared(p) > k) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire_shared(p) > k) return true;
+    if ((i & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (abort) *abort = 1;
+        atomicOr(err, code);
+        return false;
+      }
+    }
+  }
+}
+
 // Coalesced row stores of one warp: lane i holds four 16-byte chunks of row i
 // of the warp's 32. They go through `slab` (32 rows x 64 bytes; chunk c of row
 // r at position (c + r / 2) % 4, so eight consecutive lanes cover all banks in
@@ -588,8 +618,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint64_t* tempty = tfull + C::P;
   uint64_t* drain = tempty + C::P;
   uint64_t* epi_bar = drain + 1;    // epilogue-only barrier (stream-K fixup, SwiGLU amax exchange)
-  uint64_t* act_ready = epi_bar + 1;  // fused decode: activation operand written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(act_ready + 1);
+  // Fused decode: the number of K blocks of the activation operand already
+  // quantised (written with release semantics after each pass, read with
+  // acquire semantics by the MMA warp); an 8-byte slot of the barrier area.
+  int* act_kb = reinterpret_cast<int*>(epi_bar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
   int* grp_rows = reinterpret_cast<int*>(tail + C::kBarBytes);
@@ -632,7 +665,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(epi_bar, C::EPI_WARPS);
-    mbar_init(act_ready, C::EPI_WARPS);
+    *act_kb = 0;
     for (int q = 0; q < C::kSfSlots; ++q) {
       mbar_init(&sf_full[q], 4);
       mbar_init(&sf_empty[q], 1);
@@ -863,13 +896,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     uint32_t ph = 0, pph = 0;
     bool ok = true;
     // Every lane waits; a wait that gave up in any lane stops the whole warp.
-    if constexpr (C::FUSED) ok = __all_sync(0xFFFFFFFFu, mbar_wait(act_ready, 0, abort_flag, prm.err, kDevErrTimeoutMma));
+
 #ifdef FP8BLK_TRACE
     long long tw_full = 0, tw_tmem = 0, n_kb = 0;
     FP8BLK_TIC(t_loop);
 #endif
     while (ok && sch.next(u)) {
       for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        if constexpr (C::FUSED) {
+          // K block kb of the activation operand has been quantised.
+          if (!__all_sync(0xFFFFFFFFu, wait_count_above(act_kb, kb, abort_flag, prm.err, kDevErrTimeoutMma))) {
+            ok = false;
+            break;
+          }
+        }
         FP8BLK_TIC(t0);
         bool w = mbar_wait(&full[st], ph, abort_flag, prm.err, kDevErrTimeoutMma);
         FP8BLK_TOC(tw_full, t0);
@@ -1066,21 +1106,38 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       return r;
     };
 
+    if constexpr (C::FUSED) {
+      // Rows M..BN-1 of the resident operand and their scales are zero; they
+      // do not depend on x, so they are written before the dependency wait.
+      const int et = threadIdx.x - C::kEpiWarp0 * 32;  // 0 .. 127
+      const int pad_rows = C::BN - prm.M;
+      for (int i = et; i < pad_rows * prm.Kb * 8; i += C::EPI_WARPS * 32) {
+        const int r = prm.M + i / (prm.Kb * 8), rem = i % (prm.Kb * 8);
+        const int kb = rem >> 3, chunk = rem & 7;
+        *reinterpret_cast<uint4*>(act_smem + kb * (C::BN * 128) + (r >> 3) * 1024 + (r & 7) * 128 + chunk * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int i = et; i < pad_rows * prm.Kb; i += C::EPI_WARPS * 32)
+        act_scale[(i % prm.Kb) * C::BN + prm.M + i / prm.Kb] = 0.0f;
+    }
     griddep_wait();  // activation scales and every output are the previous kernel's business
     if (threadIdx.x == C::kEpiWarp0 * 32) FP8BLK_STAMP(5);
     if constexpr (C::FUSED) {
       // act_quant of x [M, K] into the resident MMA operand: the act_quant rule
       // per (row, 128 columns) -- amax, max(amax, 1e-4) / 448 (ue8m0: rounded
       // up to 2^k), codes e4m3(x / s) -- one 128-element block per 16 lanes.
-      // Rows M..BN-1 of the operand are zero. Layout: block kb at kb*BN*128,
-      // row m at (m / 8) * 1024 + (m % 8) * 128, its 16-byte chunk c stored at
-      // chunk c ^ (m % 8) (the 128-byte swizzle the descriptors name).
+      // Layout: block kb at kb*BN*128, row m at (m / 8) * 1024 + (m % 8) * 128,
+      // its 16-byte chunk c stored at chunk c ^ (m % 8) (the 128-byte swizzle
+      // the descriptors name). Blocks go K block by K block (b = kb * M + m),
+      // eight per pass (one per half-warp); after each pass the K blocks it
+      // completed are published to the MMA warp, which starts on K block 0
+      // while later ones are still being quantised.
       const int et = threadIdx.x - C::kEpiWarp0 * 32;  // 0 .. 127
       const int sub = et & 15, hw = et >> 4;
       const int total = prm.M * prm.Kb;
       const int K = prm.Kb * 128;
-      // Up to kQb blocks per half-warp are loaded before any is used, so their
-      // L2/DRAM round trips overlap.
+      // Up to kQb passes are loaded before any is used, so their L2/DRAM round
+      // trips overlap.
       constexpr int kQb = 16;
       constexpr int kPass = C::EPI_WARPS * 2;  // half-warps
       for (int base = 0; base < total; base += kPass * kQb) {
@@ -1088,7 +1145,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int q = 0; q < kQb; ++q) {
           const int b = base + q * kPass + hw;
-          const int m = b / prm.Kb, kb = b - m * prm.Kb;
+          const int kb = b / prm.M, m = b - kb * prm.M;
           v[q] = b < total ? __ldg(reinterpret_cast<const uint4*>(prm.x + static_cast<size_t>(m) * K + kb * 128) +
                                    sub)
                            : make_uint4(0u, 0u, 0u, 0u);
@@ -1096,9 +1153,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int q = 0; q < kQb; ++q) {
           const int b = base + q * kPass + hw;
-          if (base + q * kPass >= total) break;  // uniform over the warp: no block of this pass exists
+          if (base + q * kPass >= total) break;  // uniform over the epilogue: no block of this pass exists
           const bool valid = b < total;
-          const int m = valid ? b / prm.Kb : 0, kb = valid ? b - m * prm.Kb : 0;
+          const int kb = valid ? b / prm.M : 0, m = valid ? b - kb * prm.M : 0;
           const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
           float f[8];
 #pragma unroll
@@ -1122,21 +1179,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             *reinterpret_cast<uint2*>(rowp + (((sub >> 1) ^ (m & 7)) << 4) + (sub & 1) * 8) = make_uint2(lo, hi);
             if (sub == 0) act_scale[kb * C::BN + m] = sc;
           }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+          named_barrier_sync(1, C::EPI_WARPS * 32);
+          if (et == 0) {
+            const int done = (base + (q + 1) * kPass) / prm.M;  // K blocks all of whose rows are written
+            st_release_shared(act_kb, done < prm.Kb ? done : prm.Kb);
+          }
         }
       }
-      // zero rows M..BN-1 (16 bytes per thread per step) and their scales
-      const int pad_rows = C::BN - prm.M;
-      for (int i = et; i < pad_rows * prm.Kb * 8; i += C::EPI_WARPS * 32) {
-        const int r = prm.M + i / (prm.Kb * 8), rem = i % (prm.Kb * 8);
-        const int kb = rem >> 3, chunk = rem & 7;
-        *reinterpret_cast<uint4*>(act_smem + kb * (C::BN * 128) + (r >> 3) * 1024 + (r & 7) * 128 + chunk * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
-      for (int i = et; i < pad_rows * prm.Kb; i += C::EPI_WARPS * 32)
-        act_scale[(i % prm.Kb) * C::BN + prm.M + i / prm.Kb] = 0.0f;
-      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-      named_barrier_sync(1, C::EPI_WARPS * 32);
-      if (lane == 0) mbar_arrive(act_ready);
       if (threadIdx.x == C::kEpiWarp0 * 32) FP8BLK_STAMP(6);
     }
     // Raw scale loads of one K block, issued kAhead blocks before their use so
