@@ -31,7 +31,8 @@
 //   - Large M, BN = 256: CTA pairs in clusters of 2 over adjacent 128-row lane
 //     tiles; each CTA loads its own lane tile and one half of the weight tile,
 //     multicast into both CTAs.
-//   - Decode with SMs/2..SMs weight tiles: one CTA per whole tile.
+//   - Decode with at least SMs/2 weight tiles: whole tiles, one CTA per tile
+//     up to one per SM, round-robin beyond.
 //   - Decode with fewer tiles: split-K clusters of 2, 4 or 8 CTAs per tile,
 //     partials reduced in rank order through distributed shared memory.
 //   - Otherwise (and for the pairs): tiles numbered lane-tile fastest; the first
@@ -1724,10 +1725,18 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count, int pair_workers, 
     pl.tiles_lane = static_cast<int>((N + 127) / 128);
     pl.tiles_col = static_cast<int>((M + pl.bn - 1) / pl.bn);
     const long long tiles = static_cast<long long>(pl.tiles_lane) * pl.tiles_col;
-    if (FP8BLK_SWAP_WHOLE_TILES && pl.bn <= FP8BLK_WHOLE_TILE_MAX_BN && tiles <= sm_count && 2 * tiles >= sm_count) {
-      // One CTA streams each whole weight tile: no stream-K fixup.
-      pl.grid = static_cast<int>(tiles);
-      pl.dp_waves = 1;
+    if (FP8BLK_SWAP_WHOLE_TILES && pl.bn <= FP8BLK_WHOLE_TILE_MAX_BN && 2 * tiles >= sm_count) {
+      // CTAs stream whole weight tiles, one per CTA up to one per SM and then
+      // round-robin: no stream-K fixup, which costs a decode launch more than
+      // an uneven last round of tiles (measured from 160 to 768 tiles).
+      if (tiles <= sm_count) {
+        pl.grid = static_cast<int>(tiles);
+        pl.dp_waves = 1;
+      } else {
+        pl.grid = sm_count;
+        pl.dp_waves = 0;
+        pl.whole_tiles = static_cast<int>(tiles);
+      }
       pl.sk_tiles = 0;
       pl.sk_iters = 0;
       return pl;

@@ -28,9 +28,12 @@ def make_plan(M, N, K, sms, pairs=None, split_k=True):
         bn = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
         tl, tc = -(-N // 128), -(-M // bn)
         tiles = tl * tc
-        if bn <= 64 and tiles <= sms and 2 * tiles >= sms:   # decode: one CTA per whole weight tile
-            return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tiles, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
-                        tiles=tiles, cluster=1, ksplit=1)
+        if bn <= 64 and 2 * tiles >= sms:   # decode: whole weight tiles
+            if tiles <= sms:                 # one CTA per tile
+                return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tiles, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
+                            tiles=tiles, cluster=1, ksplit=1)
+            return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=sms, dp=0, sk_tiles=0, sk_iters=0, Kb=Kb,
+                        tiles=tiles, cluster=1, ksplit=1, whole=tiles)   # round-robin beyond one per SM
         if split_k and 2 * tiles < sms:   # few tiles: split-K clusters of ks CTAs per tile
             for ks in (8, 4, 2):      # (co-resident clusters assumed: sms // ks)
                 if Kb >= 2 * ks and tiles * ks <= sms:
@@ -92,7 +95,7 @@ def units(p, c):
 SHAPES = [
     (16, 320, 256), (1, 10944, 2048), (8, 10944, 2048), (64, 10944, 2048),
     (4096, 18432, 7168), (4096, 7168, 18432),
-    (64, 1536, 7168), (64, 576, 7168), (64, 24576, 1536), (64, 32768, 512),
+    (64, 1536, 7168), (64, 576, 7168), (64, 24576, 1536), (64, 32768, 512), (8, 65536, 1024), (32, 40960, 1536),
     (2048, 1536, 7168), (2048, 576, 7168), (2048, 24576, 1536), (2048, 32768, 512),
     (129, 130, 128), (300, 700, 384), (1, 1, 128), (128, 129, 2048), (33, 4000, 128),
     (5000, 100, 256),
@@ -166,6 +169,9 @@ def test_decode_plan_uses_whole_tiles():
     assert p["bn"] == 64 and p["grid"] == 86 and p["dp"] == 1
     p = make_plan(128, 10944, 2048, 152)     # BN 128: stream-K over the whole machine
     assert p["grid"] == 152 and p["dp"] == 0
+    p = make_plan(8, 24576, 1536, 152)       # 192 tiles: whole tiles, round-robin over every SM
+    assert p["grid"] == 152 and p["whole"] == 192 and p["sk_iters"] == 0
+    assert [u[0] for u in units(p, 3)] == [3, 155] and [u[0] for u in units(p, 40)] == [40]
 
 
 def test_tile_width_rule():

@@ -46,7 +46,8 @@ def swiglu_ws(M, inter, dim):
     return COUNTERS + 2 * grid * 256 * 128 * 4
 
 
-SHAPES = [(16, 320, 256), (8, 10944, 2048), (64, 10944, 2048), (300, 576, 1024), (1300, 7000, 640),
+SHAPES = [(16, 320, 256), (8, 10944, 2048), (64, 10944, 2048), (8, 65536, 1024), (32, 40960, 1536),
+          (100, 24576, 1536), (300, 576, 1024), (1300, 7000, 640),
           (4096, 18432, 7168), (4096, 7168, 18432), (2048, 32768, 512), (129, 130, 128), (40000, 60000, 256)]
 
 
