@@ -28,7 +28,7 @@ def make_plan(M, N, K, sms, pairs=None, split_k=True):
         bn = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
         tl, tc = -(-N // 128), -(-M // bn)
         tiles = tl * tc
-        if bn <= 64 and 2 * tiles >= sms:   # decode: whole weight tiles
+        if 2 * tiles >= sms:   # decode (any token-tile width): whole weight tiles
             if tiles <= sms:                 # one CTA per tile
                 return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=tiles, dp=1, sk_tiles=0, sk_iters=0, Kb=Kb,
                             tiles=tiles, cluster=1, ksplit=1)
@@ -167,8 +167,12 @@ def test_decode_plan_uses_whole_tiles():
     assert p["swap"] and p["bn"] == 16 and p["grid"] == 86 and p["dp"] == 1 and p["sk_iters"] == 0
     p = make_plan(64, 10944, 2048, 152)      # BN 64: whole tiles as well
     assert p["bn"] == 64 and p["grid"] == 86 and p["dp"] == 1
-    p = make_plan(128, 10944, 2048, 152)     # BN 128: stream-K over the whole machine
-    assert p["grid"] == 152 and p["dp"] == 0
+    p = make_plan(128, 10944, 2048, 152)     # BN 128: whole tiles as well
+    assert p["bn"] == 128 and p["grid"] == 86 and p["dp"] == 1
+    p = make_plan(128, 3000, 2048, 152)      # few tiles: split-K clusters
+    assert p["ksplit"] == 4 and p["grid"] == 96
+    p = make_plan(128, 3000, 2048, 152, split_k=False)   # ... or, without them, stream-K
+    assert p["grid"] == 152 and p["dp"] == 0 and p["sk_tiles"] == 24
     p = make_plan(8, 24576, 1536, 152)       # 192 tiles: whole tiles, round-robin over every SM
     assert p["grid"] == 152 and p["whole"] == 192 and p["sk_iters"] == 0
     assert [u[0] for u in units(p, 3)] == [3, 155] and [u[0] for u in units(p, 40)] == [40]
