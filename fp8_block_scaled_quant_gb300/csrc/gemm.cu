@@ -230,7 +230,7 @@ struct Cfg {
   static constexpr int MODE = MODE_;
   static constexpr bool GROUPED = GROUPED_;
   // Weight rows one tile covers (SwiGLU: 128 rows of w1 and the same 128 of w3).
-  static constexpr int kWRows = MODE == kEpiSwiGLU ? BN / 2 : BN;
+  static constexpr int w_rows() { return MODE == kEpiSwiGLU ? BN / 2 : BN; }
   // Extra shared memory: grouped tables (row offsets, cumulative tiles) and
   // the SwiGLU amax exchange between the two column groups (double-buffered).
   static constexpr int kGroupBytes = GROUPED ? 2 * (kMaxGroups + 4) * 4 : 0;
@@ -326,9 +326,9 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
     const int nt = local / mt_e, mt = local - nt * mt_e;
     t.lane_y = rows[e] + mt * 128;
     t.lane_valid = min(128, rows[e + 1] - t.lane_y);
-    t.col_y = e * p.N + nt * C::kWRows;
+    t.col_y = e * p.N + nt * C::w_rows();
     t.wblock = t.col_y / 128;
-    t.col0 = nt * C::kWRows;
+    t.col0 = nt * C::w_rows();
   } else {
     // Clusters: the schedule's lane index counts CTA pairs; `rank` picks the half.
     const int tl = (tile % p.tiles_lane) * C::CLUSTER + rank, tc = tile / p.tiles_lane;
@@ -340,9 +340,9 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int tile, con
       t.col0 = tc * C::BN;
     } else {
       t.lane_valid = min(128, p.M - t.lane_y);
-      t.col_y = tc * C::kWRows;
+      t.col_y = tc * C::w_rows();
       t.wblock = t.col_y / 128;
-      t.col0 = tc * C::kWRows;
+      t.col0 = tc * C::w_rows();
     }
   }
   return t;
@@ -1795,7 +1795,6 @@ Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count, int pai
   return pl;
 }
 
-size_t align256(size_t v) { return (v + 255) & ~size_t{255}; }
 
 // Scale rows of Kb floats load FP8BLK_SCALE_VEC at a time when every row of
 // each array starts on that many floats' boundary.
