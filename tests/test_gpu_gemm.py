@@ -48,6 +48,7 @@ SHAPES = [
     (1300, 7000, 640, 0.0),   # 128 x 256 cluster pairs: odd row-tile count, ragged N
     (257, 128, 2048, 0.0),    # BN 128 path
     (1000, 1000, 128, 0.0),   # single K block, N % 8 == 0
+    (80, 20000, 128, 0.0),    # swapped BN 128, 157 whole weight tiles round-robin (more than SMs), ragged N
     (512, 2304, 1536, 0.0),   # several data-parallel waves
     (64, 1536, 7168, 0.0),    # few weight tiles: split-K clusters (8 CTAs per tile)
     (8, 1536, 7168, 0.01),
@@ -246,7 +247,7 @@ def sampled_check(M, N, K, seed, frac=0.0, n_random=48, fmt=fb.SCALE_FP32):
 
 @pytest.mark.parametrize("M,N,K", [(4096, 18432, 7168), (4096, 7168, 18432), (2048, 1536, 7168),
                                    (2048, 576, 7168), (2048, 24576, 1536), (2048, 32768, 512),
-                                   (64, 24576, 1536), (64, 32768, 512), (64, 576, 7168)])
+                                   (64, 24576, 1536), (64, 32768, 512), (64, 576, 7168), (100, 10944, 2048)])
 def test_gemm_full_size_sampled(M, N, K):
     sampled_check(M, N, K, 4000 + M % 97 + N % 89, frac=0.01)
 
