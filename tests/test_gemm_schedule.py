@@ -50,6 +50,11 @@ def make_plan(M, N, K, sms, pairs=None, split_k=True):
         cluster, workers = 2, pairs
         tl = (tl + 1) // 2
     tiles = tl * tc
+    rounds = -(-tiles // workers)
+    if not swap and tiles * cluster <= MAX_COUNTERS and rounds * Kb * workers - tiles * Kb <= 32 * workers:
+        # dense large-M tiles: whole tiles unless stream-K saves the busiest worker more than 32 K blocks
+        return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=min(tiles, workers), dp=0, sk_tiles=0, sk_iters=0, Kb=Kb,
+                    tiles=tiles, cluster=cluster, ksplit=1, whole=tiles)
     if tiles * cluster > MAX_COUNTERS:   # more tiles than the counter region holds: whole tiles only
         return dict(swap=swap, bn=bn, tl=tl, tc=tc, grid=workers, dp=0, sk_tiles=0, sk_iters=0, Kb=Kb,
                     tiles=tiles, cluster=cluster, ksplit=1, whole=tiles)
@@ -329,3 +334,16 @@ def test_permute_mirror_is_the_stable_sort():
     c, o, p = permute_mirror(bad, 16, chunk=256)
     keep = np.flatnonzero((bad.ravel() >= 0) & (bad.ravel() < 16))
     assert np.array_equal(p, keep[np.argsort(bad.ravel()[keep], kind="stable")])
+
+
+def test_dense_plans_prefer_whole_tiles():
+    """Large-M tiles run whole (round-robin over SMs or CTA pairs) unless
+    stream-K shortens the busiest worker by more than 32 K blocks."""
+    whole = [(2048, 576, 7168), (512, 7168, 2048), (256, 18432, 7168), (4096, 7168, 18432), (1300, 7000, 640)]
+    streamk = [(2048, 1536, 7168), (4096, 18432, 7168)]
+    for M, N, K in whole:
+        p = make_plan(M, N, K, 152)
+        assert p.get("whole") == p["tiles"] and p["sk_iters"] == 0, (M, N, K)
+    for M, N, K in streamk:
+        p = make_plan(M, N, K, 152)
+        assert not p.get("whole") and p["sk_tiles"] > 0, (M, N, K)
