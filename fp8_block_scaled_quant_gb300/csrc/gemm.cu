@@ -1818,7 +1818,7 @@ Plan make_swiglu_plan(int64_t M, int64_t inter, int64_t K, int sm_count, int pai
   pl.tiles_lane = static_cast<int>((M + 127) / 128);
   pl.tiles_lane = (pl.tiles_lane + pl.cluster - 1) / pl.cluster;
   pl.tiles_col = static_cast<int>(inter / 128);
-  plan_schedule(pl, K / kBlock, pair_workers > 0 ? pair_workers : sm_count);
+  plan_dense_schedule(pl, K / kBlock, pair_workers > 0 ? pair_workers : sm_count);
   return pl;
 }
 

@@ -37,10 +37,14 @@ def gemm_ws(M, N, K):
 
 def swiglu_ws(M, inter, dim):
     """The fused w1/w3 GEMM: 128 x 256 tiles (128 output columns), no pairs;
-    whole tiles (more tiles than counters: no slots) or data-parallel waves use
-    every SM, stream-K at most one CTA per (tile, K block)."""
+    whole tiles (more tiles than counters, or stream-K saving the busiest CTA
+    at most 32 K blocks: no slots) or data-parallel waves use every SM,
+    stream-K at most one CTA per (tile, K block)."""
     tiles = -(-M // 128) * (inter // 128)
     if tiles > COUNTERS // 4:
+        return COUNTERS
+    Kb = dim // 128
+    if -(-tiles // 256) * Kb * 256 - tiles * Kb <= 32 * 256:
         return COUNTERS
     grid = 256 if tiles >= 2 * 256 else min(256, tiles * (dim // 128))
     return COUNTERS + 2 * grid * 256 * 128 * 4
