@@ -35,12 +35,15 @@
 //     up to one per SM, round-robin beyond.
 //   - Decode with fewer tiles: split-K clusters of 2, 4 or 8 CTAs per tile,
 //     partials reduced in rank order through distributed shared memory.
-//   - Otherwise (and for the pairs): tiles numbered lane-tile fastest; the first
-//     dp_waves * workers tiles go round-robin to whole workers (data-parallel
-//     waves: concurrent tiles share column-operand tiles in L2); the rest are
-//     split stream-K, and a tile cut between workers is finished by whichever
-//     of them arrives last on its counter, summing the fp32 partials in part
-//     order and storing bf16.
+//   - Large M (and the pairs): tiles numbered lane-tile fastest (concurrent
+//     tiles share column-operand tiles in L2), whole tiles round-robin over the
+//     workers unless splitting K would shorten the busiest worker by more than
+//     kStreamKSlackKb K blocks. Then the first dp_waves * workers tiles go
+//     round-robin to whole workers and the rest are split stream-K: a tile cut
+//     between workers is finished by whichever of them arrives last on its
+//     counter, summing the fp32 partials in part order and storing bf16.
+//     Small decode problems without split-K clusters take the same waves +
+//     stream-K.
 //   - Grouped (MoE) tiles: (group, column tile, 128-row tile), whole tiles
 //     round-robin.
 //
