@@ -71,6 +71,9 @@ WORKLOADS = {
     "moe_t4096_zipf": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=1.2, seed=synthetic.SEED_MOE)),
     "moe_t4096_uniform_shared": ("moe", dict(T=4096, E=256, dim=7168, inter=2048, k=8, zipf=0.0, shared=1,
                                              seed=synthetic.SEED_MOE)),
+    # The same expert shapes and rows per expert (128) with 32 experts: a
+    # 1.4 GB step small enough for a full ncu capture of the grouped GEMMs.
+    "moe_t512_e32_uniform": ("moe", dict(T=512, E=32, dim=7168, inter=2048, k=8, zipf=0.0, seed=synthetic.SEED_MOE)),
     "mla_absorb_m64": ("mla", dict(T=64, H=128, C=512, seed=synthetic.SEED_ATTN)),
     "mla_absorb_m2048": ("mla", dict(T=2048, H=128, C=512, seed=synthetic.SEED_ATTN)),
     "moe_gate_t4096_e256": ("gate", dict(T=4096, E=256, groups=8, kept=4, k=8, route_scale=2.5,
