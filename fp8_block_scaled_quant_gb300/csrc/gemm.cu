@@ -17,7 +17,10 @@
 //   epilogue    promotion: tcgen05.ld each partial, multiply by the block's
 //   warps       a_s * w_s and add into fp32 registers (the pages'
 //               acc += dot(a, b) * a_s * b_s); at the end of a tile bf16
-//               stores, or the SwiGLU + act_quant epilogue, or scattered rows.
+//               stores (dense large-M tiles: through a swizzled shared-memory
+//               slab per warp and TMA boxes), or the SwiGLU + act_quant
+//               epilogue, or rows scattered to slots (both through per-warp
+//               slabs, eight rows per store instruction).
 //   Large-M tiles (BN = 256, two column groups) run 12 warps: warps 0-3 give
 //   registers to the two epilogue warpgroups (setmaxnreg 56 / 224).
 //
