@@ -1499,7 +1499,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       unit_parity ^= 1u;
     }
     if constexpr (C::kTmaStore) {
-      if (lane == 0) bulk_wait_group_read0();  // the slab is read before the CTA's shared memory goes
+      if (lane == 0) bulk_wait_group0();  // every store written before the CTA exits
       __syncwarp();
     }
 #ifdef FP8BLK_TRACE

@@ -75,6 +75,12 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
   return d;
 }
 
+// The issuing thread's bulk stores, all but the most recent group, have read
+// their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_group_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // kind::f16 instruction descriptor: f32 accumulator, A and B both bf16 (one
 // value sets both format fields), A K-major, B K-major or (b_mn) MN-major
 // (bit 16), an M x N tile.
@@ -358,42 +364,51 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                                              kDevErrTimeoutMla)))
         break;
       tc_fence_after_sync();
-      if (lane == 0) bulk_wait_group_read0();  // the previous tile's stores have read the slab
-      __syncwarp();
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(b * 128 + c0), v);
-        if (c0 == 96) {  // the buffer's last columns are in registers: free it for tile i + 2
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[b]);
-        }
-        uint8_t* row = slab + (c0 >> 6) * kOutHalf + lane * 128;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {  // 16-byte chunk ((c0 % 64) / 8 + g) of the row, at chunk ^ (lane % 8)
-          uint32_t w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 bb =
-                __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * e]), __uint_as_float(v[g * 8 + 2 * e + 1]));
-            w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
-          }
-          const int chunk = ((c0 & 63) >> 3) + g;
-          *reinterpret_cast<uint4*>(row + ((chunk ^ (lane & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-      }
-      fence_proxy_async_smem();  // the slab's generic-proxy writes, read next by the TMA
-      __syncwarp();
       const int y = mt * 128 + quarter * 32;
-      if (lane == 0 && y < prm.T) {  // rows past T inside the box are clipped by the TMA
-        const int x = h * nout + nt * 128;
-        tma_store_2d(&tmap_o, slab, x, y);
-        tma_store_2d(&tmap_o, slab + kOutHalf, x + 64, y);
-        bulk_commit_group();
+      const int x = h * nout + nt * 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        // Each half of the slab is committed as its own bulk group (one per
+        // half and tile, empty where nothing is stored); groups complete in
+        // order, so with at most one pending, the store that last used this
+        // half has read it.
+        if (lane == 0) bulk_wait_group_read_le1();
+        __syncwarp();
+#pragma unroll
+        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(b * 128 + c0), v);
+          if (c0 == 96) {  // the buffer's last columns are in registers: free it for tile i + 2
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+          }
+          uint8_t* row = slab + half * kOutHalf + lane * 128;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {  // 16-byte chunk ((c0 % 64) / 8 + g) of the row, at chunk ^ (lane % 8)
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 bb =
+                  __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * e]), __uint_as_float(v[g * 8 + 2 * e + 1]));
+              w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            const int chunk = ((c0 & 63) >> 3) + g;
+            *reinterpret_cast<uint4*>(row + ((chunk ^ (lane & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        fence_proxy_async_smem();  // the slab's generic-proxy writes, read next by the TMA
+        __syncwarp();
+        if (lane == 0) {
+          // Rows past T inside the box are clipped by the TMA; a quarter wholly
+          // past T stores nothing but still commits its (empty) group, so that
+          // every half of every tile owns exactly one group.
+          if (y < prm.T) tma_store_2d(&tmap_o, slab + half * kOutHalf, x + half * 64, y);
+          bulk_commit_group();
+        }
       }
     }
-    if (lane == 0) bulk_wait_group_read0();  // the slab is read before the CTA's shared memory goes
+    if (lane == 0) bulk_wait_group0();  // every store written before the CTA exits
     __syncwarp();
   }
 

@@ -138,6 +138,11 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// The issuing thread's bulk stores are complete: written to global memory.
+// A kernel waits for this before it exits, so that the next kernel, released
+// by griddepcontrol.wait when this one completes, reads the stored data.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // The same box, written at the same shared-memory offset of every CTA of the
 // cluster in `cta_mask`; each destination's mbarrier at `bar`'s offset receives
 // the bytes that land in that CTA.

@@ -279,6 +279,34 @@ def test_gemm_ue8m0_flags_scales_that_are_not_powers_of_two():
     assert fb.last_device_error() == 0
 
 
+def test_linear_chain_reads_the_previous_output():
+    """Two dense linears back to back on one stream, the second reading the
+    first's output (M > 128: the first stores through TMA boxes; the second's
+    act_quant may launch early and reads x after its dependency wait), over
+    reused buffers, against the same calls with a synchronisation between
+    them: the first kernel's stores are in memory when it completes."""
+    dev = torch.device("cuda")
+    M, D, H = 300, 512, 1024
+    q1, s1 = fb.weight_quant(synthetic.device_normal((H, D), 71, 0.02, dev))
+    q2, s2 = fb.weight_quant(synthetic.device_normal((D, H), 72, 0.02, dev))
+    xs = [synthetic.device_activations(M, D, 73 + r, dev) for r in range(3)]
+    mid = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    outs = [torch.empty((M, D), dtype=torch.bfloat16, device=dev) for _ in xs]
+    ws1 = fb.workspace(fb.linear_workspace_bytes(M, H, D), dev, "chain1")
+    ws2 = fb.workspace(fb.linear_workspace_bytes(M, D, H), dev, "chain2")
+    for x, o in zip(xs, outs):
+        fb.linear(x, q1, s1, out=mid, ws=ws1)
+        fb.linear(mid, q2, s2, out=o, ws=ws2)
+    torch.cuda.synchronize()
+    for x, o in zip(xs, outs):
+        m = fb.linear(x, q1, s1)
+        torch.cuda.synchronize()
+        ref = fb.linear(m, q2, s2)
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+    assert fb.last_device_error() == 0
+
+
 def test_linear_matches_quant_then_gemm():
     x, w, xq, xs, wq, ws = host_problem(8, 10944, 2048, 21, 0.01)
     xd = bits_to_dev_bf16(x)
