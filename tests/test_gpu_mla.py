@@ -100,6 +100,26 @@ def test_mla_chain_reads_the_previous_kernels_output():
     assert fb.last_device_error() == 0
 
 
+@pytest.mark.parametrize("mode", ["qk", "v"])
+def test_mla_many_tiles_per_cta_match_one_tile_per_cta(mode):
+    """The 128-head layer at 300 tokens gives each persistent CTA about ten
+    tiles, some of whose 32-row quarters lie wholly past T (the last token
+    tile holds 44 rows), so each epilogue warp alternates tiles it stores
+    and tiles it skips while reusing its staging slab. The same heads run 8
+    at a time (one tile per CTA) must give the same bits."""
+    T, H, C = 300, 128, 512
+    wq, ws = weights(H, C, 600)
+    w, s = dev_w(wq, ws)
+    width = DN if mode == "qk" else C
+    x = bits_to_dev_bf16(synthetic.activations(T, H * width, 601)).view(T, H, width)
+    full = fb.mla_absorb(x, w, s, mode)
+    for h0 in range(0, H, 8):
+        part = fb.mla_absorb(x[:, h0:h0 + 8].contiguous(), w[h0 * (DN + DV):(h0 + 8) * (DN + DV)],
+                             s[2 * h0:2 * (h0 + 8)], mode)
+        assert torch.equal(part.view(torch.int16), full[:, h0:h0 + 8].view(torch.int16)), f"heads {h0}..{h0 + 7}"
+    assert fb.last_device_error() == 0
+
+
 def test_mla_argument_errors():
     L = fb.lib()
     x = torch.zeros((4, 2, 128), dtype=torch.bfloat16, device="cuda")
