@@ -254,9 +254,9 @@ _COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
 # the device helpers it includes and the host code that plans its launch.
 # None: every source (a workload of several kernels).
 KERNEL_SOURCES = {
-    "fp8_gemm": ("gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
+    "fp8_gemm": ("gemm.cu", "gemm_decode.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
     "swiglu_gemm": ("gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
-    "linear_fused": ("api.cu", "gemm.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
+    "linear_fused": ("api.cu", "gemm.cu", "gemm_decode.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
     "weight_dequant": ("quant.cu", "ptx.cuh", "quotient.cuh", "host.cuh"),
     "mla": ("mla.cu", "ptx.cuh", "host.cuh"),
     "moe_step": None,
@@ -454,9 +454,9 @@ def run_linear(args, shape, dev, torch, fb, peaks, steps, warmup, rank, world):
     el, (el_gemm, el_aq), clocks, uploaded = timed_runs(dev, stream, torch, g_main, (g_gemm, g_aq), g_soak)
     assert fb.last_device_error(dev) == 0, "a kernel reported a wait timeout"
 
-    # M <= 2: fp8blk_linear is one kernel (act_quant fused into the GEMM);
-    # otherwise act_quant then fp8_gemm.
-    fused = M <= 2
+    # One kernel where the library fuses act_quant into the GEMM (M <= 2 on
+    # shapes the decode GEMM does not take); otherwise act_quant then fp8_gemm.
+    fused = fb.linear_kernels(M, N, K) == 1
     step_bytes = linear_bytes(M, N, K)
     gemm_b = gemm_kernel_bytes(M, N, K)
     flops = linear_flops(M, N, K)

@@ -22,7 +22,8 @@ import torch
 __all__ = [
     "SCALE_FP32", "SCALE_UE8M0", "SCALE_PROMOTE", "BLOCK", "lib", "lib_path", "header_functions", "Fp8BlkError",
     "act_quant", "weight_quant", "weight_dequant", "fp8_gemm", "linear", "linear_host",
-    "gemm_workspace_bytes", "linear_workspace_bytes", "linear_host_workspace_bytes", "last_device_error",
+    "gemm_workspace_bytes", "linear_workspace_bytes", "linear_host_workspace_bytes", "linear_kernels",
+    "last_device_error",
     "swiglu_gemm", "ffn", "moe_permute", "moe_workspace_bytes", "moe_grouped_gemm", "moe_gate", "moe_route",
 ]
 
@@ -80,6 +81,7 @@ def lib():
             L.fp8blk_linear_host_workspace_bytes.argtypes = [i64, i64, i64]
             L.fp8blk_linear_host_workspace_bytes.restype = sz
             L.fp8blk_linear_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
+            L.fp8blk_linear_kernels.argtypes = [i64, i64, i64, ctypes.POINTER(i32)]
             L.fp8blk_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
             for name in header_functions():
                 if getattr(L, name).restype is ctypes.c_int:
@@ -183,6 +185,15 @@ def linear_workspace_bytes(M: int, N: int, K: int) -> int:
 
 def linear_host_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(lib().fp8blk_linear_host_workspace_bytes(M, N, K))
+
+
+def linear_kernels(M: int, N: int, K: int) -> int:
+    """Kernels one linear() call of this shape launches on the current device:
+    1 when act_quant runs inside the GEMM kernel, 2 when it is a kernel of its
+    own, 0 for an empty problem."""
+    n = ctypes.c_int(0)
+    _check(lib().fp8blk_linear_kernels(M, N, K, ctypes.byref(n)), "linear_kernels")
+    return n.value
 
 
 def fp8_gemm(a: torch.Tensor, a_s: torch.Tensor, w: torch.Tensor, w_s: torch.Tensor,

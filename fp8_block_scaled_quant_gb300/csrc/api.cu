@@ -22,6 +22,8 @@ int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, in
                      int scale_fmt, cudaStream_t stream, bool* used);
 int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
              int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+bool decode_gemm_fits(int64_t M, int64_t N, int64_t K, int sm_count);
+bool linear_fused_fits(int64_t M, int64_t N, int64_t K);
 
 namespace {
 
@@ -128,10 +130,14 @@ extern "C" int fp8blk_linear(const void* x_bf16, const void* w_e4m3, const float
                              fp8blk_stream_t stream) {
   if (M < 0 || N < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
   if (M == 0 || N == 0) return FP8BLK_OK;
-  // M <= 2: act_quant runs inside the GEMM kernel (one launch). For larger M
-  // its in-kernel cost (every CTA quantises all of x) exceeds the launch it
-  // saves, so act_quant is a kernel of its own.
-  if (M <= kFusedLinearMaxM) {
+  // M <= 2: act_quant runs inside the GEMM kernel (one launch), unless the
+  // slice-per-SM decode GEMM takes the shape (act_quant + that kernel is the
+  // faster pair). For larger M the in-kernel act_quant (every CTA quantises
+  // all of x) costs more than the launch it saves, so act_quant is a kernel
+  // of its own.
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  if (M <= kFusedLinearMaxM && !decode_gemm_fits(M, N, K, d->sm_count)) {
     bool used = false;
     const int st = linear_fused_run(x_bf16, w_e4m3, w_s, y_bf16, M, N, K, scale_fmt,
                                     reinterpret_cast<cudaStream_t>(stream), &used);
@@ -149,6 +155,19 @@ extern "C" int fp8blk_linear(const void* x_bf16, const void* w_e4m3, const float
     return st;
   return gemm_run(xq, xs, w_e4m3, w_s, y_bf16, M, N, K, scale_fmt, gws, gbytes,
                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8blk_linear_kernels(int64_t M, int64_t N, int64_t K, int* kernels) {
+  if (!kernels) return FP8BLK_ERR_NULL;
+  if (M < 0 || N < 0 || K < 0 || K % kBlock != 0) return FP8BLK_ERR_SHAPE;
+  if (M == 0 || N == 0 || K == 0) {
+    *kernels = 0;
+    return FP8BLK_OK;
+  }
+  const DevInfo* d;
+  if (int st = current_device(&d)) return st;
+  *kernels = (M <= kFusedLinearMaxM && !decode_gemm_fits(M, N, K, d->sm_count) && linear_fused_fits(M, N, K)) ? 1 : 2;
+  return FP8BLK_OK;
 }
 
 // Host variant: [linear workspace][x bf16 M*K][y bf16 M*N] (the linear

@@ -2002,6 +2002,9 @@ int gemm_check_args(const void* a, const float* a_s, const void* w, const float*
   return FP8BLK_OK;
 }
 
+int decode_gemm_run(const DevInfo* dev, const void* a, const float* a_s, const void* w, const float* w_s, void* c,
+                    int64_t M, int64_t N, int64_t K, cudaStream_t stream, bool* used);
+
 int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, void* c, int64_t M, int64_t N,
              int64_t K, int scale_fmt, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (int st = gemm_check_args(a, a_s, w, w_s, c, M, N, K, scale_fmt)) return st;
@@ -2013,6 +2016,13 @@ int gemm_run(const void* a, const float* a_s, const void* w, const float* w_s, v
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need) return FP8BLK_ERR_WORKSPACE;
   if (!is_aligned(workspace, 256)) return FP8BLK_ERR_ALIGN;
+  // Up to 16 tokens, when a CTA's weight slice fits in shared memory: the
+  // slice-per-SM decode kernel (no workspace used).
+  {
+    bool used = false;
+    const int st = decode_gemm_run(d, a, a_s, w, w_s, c, M, N, K, stream, &used);
+    if (st || used) return st;
+  }
 
   GemmParams prm{};
   prm.a_s = a_s;
@@ -2077,22 +2087,33 @@ bool scale_fmt_ok(int f) { return scale_fmt_valid(f); }
 // CTAs, whole 128-row weight tiles per CTA. Sets *used = false (and launches
 // nothing) when the shape does not fit the fused kernel's shared memory; the
 // caller then runs act_quant + fp8_gemm.
+namespace {
+
+// Which fused kernel takes the shape: 0 (8 weight stages), 1 (4 stages), or
+// -1 (none: the resident activation operand does not fit).
+int linear_fused_variant(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || M > 16 || N < 1 || K < kBlock || K % kBlock || N > (int64_t{1} << 31) - 1 || K > (int64_t{1} << 24))
+    return -1;
+  const size_t extra = fused_extra_bytes(static_cast<int>(K / kBlock), 16);
+  return CfgF16S8::kSmemBytes + extra <= kMaxDynSmem ? 0 : CfgF16S4::kSmemBytes + extra <= kMaxDynSmem ? 1 : -1;
+}
+
+}  // namespace
+
+bool linear_fused_fits(int64_t M, int64_t N, int64_t K) { return linear_fused_variant(M, N, K) >= 0; }
+
 int linear_fused_run(const void* x, const void* w, const float* w_s, void* y, int64_t M, int64_t N, int64_t K,
                      int scale_fmt, cudaStream_t stream, bool* used) {
   *used = false;
   if (!scale_fmt_ok(scale_fmt)) return FP8BLK_ERR_ARG;
-  if (M < 1 || M > 16 || N < 1 || K < kBlock || K % kBlock || N > (int64_t{1} << 31) - 1 || K > (int64_t{1} << 24))
-    return FP8BLK_OK;
+  const int variant = linear_fused_variant(M, N, K);
+  if (variant < 0) return FP8BLK_OK;
   if (!x || !w || !w_s || !y) return FP8BLK_ERR_NULL;
   if (!is_aligned(x, 16) || !is_aligned(w, 16) || !is_aligned(w_s, 4) || !is_aligned(y, 2)) return FP8BLK_ERR_ALIGN;
   const DevInfo* d;
   if (int st = current_device(&d)) return st;
   const int Kb = static_cast<int>(K / kBlock);
   const size_t extra = fused_extra_bytes(Kb, 16);
-  const int variant = CfgF16S8::kSmemBytes + extra <= kMaxDynSmem   ? 0   // 8 weight stages
-                      : CfgF16S4::kSmemBytes + extra <= kMaxDynSmem ? 1   // 4 weight stages
-                                                                    : -1;
-  if (variant < 0) return FP8BLK_OK;
   GemmParams prm{};
   prm.w_s = w_s;
   prm.c = static_cast<__nv_bfloat16*>(y);

@@ -178,6 +178,18 @@ FP8BLK_API int fp8blk_linear(const void *x_bf16, const void *w_e4m3, const float
                   int64_t K, int scale_fmt, void *workspace, size_t workspace_bytes, fp8blk_stream_t stream);
 
 /*
+ * How many kernels one fp8blk_linear call of shape (M, N, K) launches on the
+ * current device, written to *kernels: 1 where act_quant runs inside the GEMM
+ * kernel (M <= 2, the quantised x fits that kernel's shared memory, and the
+ * slice-per-SM decode GEMM does not take the shape), 2 where act_quant and
+ * fp8_gemm are kernels of their own, 0 for an empty problem (M, N or K zero).
+ * Returns FP8BLK_ERR_NULL for a null kernels, FP8BLK_ERR_SHAPE for a shape
+ * fp8blk_linear refuses, FP8BLK_ERR_ARCH / FP8BLK_ERR_CUDA as the device
+ * check gives them.
+ */
+FP8BLK_API int fp8blk_linear_kernels(int64_t M, int64_t N, int64_t K, int *kernels);
+
+/*
  * The same layer with the activation and the result in HOST memory
  * (x_host bf16 [M, K], y_host bf16 [M, N]), enqueued on `stream`; y_host is
  * valid once the stream has been synchronised. The weight stays on the device.

@@ -58,6 +58,10 @@ def test_host_side_argument_checks_without_gpu(L):
     assert L.fp8blk_weight_dequant(None, None, 0, 5, None, None) == 0
     assert L.fp8blk_weight_dequant(None, None, 3, 5, None, None) == 1
     assert L.fp8blk_gemm(None, None, None, None, None, 2, 2, 100, 0, None, 0, None) == 2
+    n = ctypes.c_int(-1)
+    assert L.fp8blk_linear_kernels(4, 8, 100, ctypes.byref(n)) == 2       # K % 128
+    assert L.fp8blk_linear_kernels(4, 8, 128, None) == 1                  # null
+    assert L.fp8blk_linear_kernels(0, 8, 128, ctypes.byref(n)) == 0 and n.value == 0   # empty
     assert L.fp8blk_gemm(None, None, None, None, None, 0, 2, 128, 0, None, 0, None) == 0
     assert L.fp8blk_linear(None, None, None, None, 2, 2, 100, 0, None, 0, None) == 2
     assert L.fp8blk_linear_host(None, None, None, None, 2, 2, 128, 0, None, 0, None) == 1

@@ -347,3 +347,96 @@ def test_dense_plans_prefer_whole_tiles():
     for M, N, K in streamk:
         p = make_plan(M, N, K, 152)
         assert not p.get("whole") and p["sk_tiles"] > 0, (M, N, K)
+
+
+# ---- the slice-per-SM decode kernel (M <= 16) -------------------------------------
+
+DECODE_SMEM_LIMIT = 232448
+
+
+def decode_plan(M, N, K, sms, boxes=4, target_warps=16):
+    """Mirror of the decode kernel's plan: one CTA per slice of R weight rows
+    (ceil(N / SMs) rounded up to 8), the slice in `boxes` TMA boxes of kbb K
+    blocks, warps = K slices x row-group parts (at most 5 groups of 16 rows
+    per warp with one token fragment, 3 with two). None where the kernel does
+    not take the shape (then the tcgen05 swapped kernel runs)."""
+    if not 1 <= M <= 16 or N < 1 or K < 128 or K % 128:
+        return None
+    Kb = K // 128
+    R = -(-N // sms)
+    R = -(-R // 8) * 8
+    if R > 256:
+        return None
+    nbox = min(Kb, boxes)
+    kbb = -(-Kb // nbox)
+    if kbb > 256:
+        return None
+    nbox = -(-Kb // kbb)
+    groups = -(-R // 16)
+    nt = 1 if M <= 8 else 2
+    gpw = 5 if nt == 1 else 3
+    gparts = -(-groups // gpw)
+    ks = min(max(1, target_warps // gparts), Kb)
+    more = target_warps // ks
+    if more > gparts:
+        gparts = min(more, groups)
+    tok = 8 * nt
+    wbytes = nbox * kbb * R * 128
+    pbytes = ks * tok * (groups * 16 + 4) * 4
+    area = -(-max(wbytes, pbytes) // 16) * 16
+    wblk = (R + 127) // 128 + 1
+    off_bar = -(-(area + wblk * Kb * 4) // 8) * 8
+    smem = 1024 + off_bar + nbox * 8 + 8
+    if smem > DECODE_SMEM_LIMIT or ks * gparts > 16:
+        return None
+    return dict(R=R, ctas=-(-N // R), groups=groups, ks=ks, gparts=gparts, gpw=gpw, warps=ks * gparts, nbox=nbox,
+                kbb=kbb, Kb=Kb, tok=tok, wbytes=wbytes, pbytes=pbytes, area=area, wblk=wblk, smem=smem)
+
+
+def test_decode_plan_of_the_decode_workload():
+    p = decode_plan(8, 10944, 2048, 152)
+    assert (p["R"], p["ctas"], p["groups"], p["ks"], p["gparts"], p["nbox"], p["kbb"], p["tok"]) == \
+        (72, 152, 5, 16, 1, 4, 4, 8)
+    assert p["smem"] <= DECODE_SMEM_LIMIT
+    assert decode_plan(1, 10944, 2048, 152)["ctas"] == 152
+    big = decode_plan(16, 38912, 256, 152)   # the widest slices a box holds: 256 rows, 16 row groups
+    assert (big["R"], big["groups"], big["ks"], big["gparts"], big["tok"]) == (256, 16, 2, 8, 16)
+    assert decode_plan(16, 38912, 256, 148) is None
+    # slices too large for shared memory, or more than 16 tokens: the tcgen05 kernels
+    for shape in ((8, 24576, 1536), (16, 10944, 7168), (2, 10944, 7168), (17, 576, 7168), (64, 10944, 2048)):
+        assert decode_plan(*shape, 152) is None, shape
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 10944, 2048), (9, 10944, 2048), (16, 33000, 256), (4, 7, 128),
+                                   (1, 1217, 640), (7, 3600, 384), (12, 640, 7168), (16, 320, 256),
+                                   (5, 2999, 1024), (16, 11000, 384), (2, 32768, 512), (1, 129, 4096)])
+@pytest.mark.parametrize("sms", [152, 148, 132])
+def test_decode_plan_covers_every_weight_row_and_k_block_once(M, N, K, sms):
+    """Every (weight row < N, K block) goes to exactly one warp of one CTA;
+    no warp holds more row groups than its accumulators; every box holds at
+    least one K block; the staged weight scales cover the slice's 128-row
+    blocks; the partials fit in the weight area."""
+    p = decode_plan(M, N, K, sms)
+    assert p is not None
+    R, Kb, G = p["R"], p["Kb"], p["groups"]
+    assert R % 8 == 0 and p["ctas"] <= sms and p["warps"] <= 16
+    assert (p["nbox"] - 1) * p["kbb"] < Kb <= p["nbox"] * p["kbb"]
+    seen = {}
+    for c in range(p["ctas"]):
+        r0 = c * R
+        assert r0 < N
+        blocks = min(r0 + R - 1, N - 1) // 128 - r0 // 128 + 1
+        assert blocks <= p["wblk"]
+        for ks in range(p["ks"]):
+            kb0, kb1 = ks * Kb // p["ks"], (ks + 1) * Kb // p["ks"]
+            assert kb0 < kb1
+            for gp in range(p["gparts"]):
+                g0, g1 = gp * G // p["gparts"], (gp + 1) * G // p["gparts"]
+                assert 1 <= g1 - g0 <= p["gpw"]
+                for r in range(g0 * 16, g1 * 16):
+                    if r >= R or r0 + r >= N:
+                        continue
+                    for kb in range(kb0, kb1):
+                        seen[(r0 + r, kb)] = seen.get((r0 + r, kb), 0) + 1
+    assert len(seen) == N * Kb and set(seen.values()) == {1}
+    assert p["pbytes"] <= p["area"]

@@ -58,6 +58,16 @@ SHAPES = [
     (3, 12160, 1024, 0.01),   # weight slices of exactly 80 rows
     (16, 11000, 384, 0.0),    # slices of 80 rows, the last one 40
     (33, 10944, 1024, 0.0),   # slices of 72 rows with BN 64
+    # The slice-per-SM decode kernel (M <= 16, a CTA's weight slice in shared memory):
+    (9, 10944, 2048, 0.01),   # two token fragments, seven of them padding; 72-row slices (a half row group)
+    (16, 38912, 256, 0.0),    # 256-row slices: 16 row groups, one K slice each, one K block per box
+    (4, 7, 128, 0.0),         # one CTA, one K block, weight rows past N read as zeros
+    (1, 1217, 640, 0.01),     # 16-row slices, the last one a single row; 5 K blocks in boxes of 3 (one past K)
+    (7, 3600, 384, 0.0),      # 24-row slices, some across 128-row scale blocks; 3 K slices of one K block
+    (12, 640, 7168, 0.0),     # 8-row slices, 20 K slices of 2-3 K blocks
+    # M <= 16 where the slice does not fit: the tcgen05 swapped kernel
+    (8, 24576, 1536, 0.0),
+    (16, 10944, 7168, 0.01),
 ]
 
 
@@ -316,6 +326,19 @@ def test_linear_matches_quant_then_gemm():
     c = fb.fp8_gemm(a, a_s, q, s)
     assert torch.equal(y.view(torch.int16), c.view(torch.int16))
     assert_gemm_close(dev_to_bits(y), oracle.gemm(xq, xs, wq, ws))
+
+
+def test_linear_kernel_count():
+    """fp8blk_linear_kernels names the launches of fp8blk_linear: act_quant
+    fused into the GEMM (1) only for M <= 2 where the decode GEMM does not
+    take the shape."""
+    assert fb.linear_kernels(1, 10944, 2048) == 2    # act_quant + the slice-per-SM decode GEMM
+    assert fb.linear_kernels(8, 10944, 2048) == 2
+    assert fb.linear_kernels(2, 10944, 7168) == 1    # slices too large: the fused kernel
+    assert fb.linear_kernels(64, 10944, 2048) == 2
+    assert fb.linear_kernels(3, 0, 2048) == 0
+    with pytest.raises(fb.Fp8BlkError):
+        fb.linear_kernels(1, 10, 100)
 
 
 @pytest.mark.parametrize("M", [1, 8, 64])

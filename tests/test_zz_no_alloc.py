@@ -22,7 +22,7 @@ import torch
 
 import fp8_block_scaled_quant_gb300 as fb
 import synthetic
-from test_gemm_schedule import make_plan, units
+from test_gemm_schedule import decode_plan, make_plan, units
 
 pytestmark = pytest.mark.gpu
 
@@ -63,17 +63,20 @@ def test_stream_k_shape_writes_partials():
     """The first problem below really runs stream-K with split tiles (plan
     mirror at this GPU's SM count), within the scratch."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    p = make_plan(16, 320, 256, sms)
-    assert p["swap"] and p["ksplit"] == 1 and not p.get("whole") and p["sk_tiles"] > 0
-    assert any(u[4] > 1 for c in range(p["grid"]) for u in units(p, c)), "no tile is split"
-    assert fb.gemm_workspace_bytes(16, 320, 256) <= SCRATCH
+    for M, N, K in ((24, 320, 256), (20, 640, 384)):
+        assert decode_plan(M, N, K, sms) is None   # more than 16 tokens: the tcgen05 swapped kernel
+        p = make_plan(M, N, K, sms)
+        assert p["swap"] and p["ksplit"] == 1 and not p.get("whole") and p["sk_tiles"] > 0
+        assert any(u[4] > 1 for c in range(p["grid"]) for u in units(p, c)), "no tile is split"
+        assert fb.gemm_workspace_bytes(M, N, K) <= SCRATCH
 
 
 def test_noalloc_matches_gemm_on_calls_in_a_row():
     f = noalloc_fn()
-    # stream-K with split tiles; whole tiles round-robin past one per SM; one
-    # CTA per whole tile (BN 16, BN 64); stream-K again with another split.
-    shapes = [(16, 320, 256), (8, 24576, 1536), (8, 10944, 2048), (64, 10944, 2048), (12, 640, 384)]
+    # stream-K with split tiles; whole tiles round-robin past one per SM; the
+    # slice-per-SM decode kernel; one CTA per whole tile (BN 64); stream-K
+    # again with another split.
+    shapes = [(24, 320, 256), (8, 24576, 1536), (8, 10944, 2048), (64, 10944, 2048), (20, 640, 384)]
     probs = [problem(M, N, K, 31 + i) for i, (M, N, K) in enumerate(shapes)]
     refs = [fb.fp8_gemm(*p) for p in probs]
     outs = [torch.empty_like(r) for r in refs]
