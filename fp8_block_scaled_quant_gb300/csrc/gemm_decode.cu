@@ -11,8 +11,9 @@
 //     R rows x K, in a few large TMA boxes (a 3-D map: 128 bytes of a K block
 //     x R rows x K blocks, 128-byte swizzle), so the weight stream runs while
 //     the previous kernel finishes.
-//   - Warps = K slices x row-group parts (16-row groups, at most five per
-//     warp). Right after the wait every warp loads its tokens' operand
+//   - Warps = K slices x row-group parts (at most five 16-row groups per warp
+//     with one token fragment, three with two; at most 16 warps). Right after
+//     the wait every warp loads its tokens' operand
 //     fragments and a_s for its K blocks straight from global memory into
 //     registers (the next K block's while it multiplies the current one), so
 //     no CTA-wide staging stands between the wait and the first product.
