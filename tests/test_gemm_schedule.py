@@ -8,6 +8,11 @@ stream-K range is non-empty, the parts of each split tile are numbered
 0..nparts-1 by consecutive CTAs, and the partial slots they use are
 distinct. A mistake here would leave an output tile unwritten or let two
 CTAs race on one slot."""
+import itertools
+import os
+import shutil
+import subprocess
+
 import pytest
 
 
@@ -440,3 +445,42 @@ def test_decode_plan_covers_every_weight_row_and_k_block_once(M, N, K, sms):
                         seen[(r0 + r, kb)] = seen.get((r0 + r, kb), 0) + 1
     assert len(seen) == N * Kb and set(seen.values()) == {1}
     assert p["pbytes"] <= p["area"]
+
+
+def test_decode_plan_mirror_matches_the_library_plan(tmp_path):
+    """The mirror above against the plan the library computes: the plan
+    function compiled from the kernel's own source (tests/cuda/
+    decode_plan_dump.cu, host code only), over a grid of shapes and SM counts
+    that includes every refusal (too many tokens, slices past 256 rows or past
+    shared memory, K not a multiple of 128)."""
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    exe = str(tmp_path / "decode_plan_dump")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O1", "-std=c++17",
+                    "-I", os.path.join(root, "include"), "-I", os.path.join(root, "fp8_block_scaled_quant_gb300", "csrc"),
+                    "-o", exe, os.path.join(here, "cuda", "decode_plan_dump.cu")],
+                   check=True, capture_output=True, timeout=300)
+    shapes = list(itertools.product((1, 2, 7, 8, 9, 16, 17, 64),
+                                    (1, 7, 8, 129, 320, 1217, 2999, 10944, 24576, 32768, 38912, 50000),
+                                    (100, 128, 256, 384, 640, 2048, 7168, 12288),
+                                    (152, 148, 132, 2, 1)))
+    res = subprocess.run([exe], input="\n".join(f"{M} {N} {K} {s}" for M, N, K, s in shapes) + "\n",
+                         capture_output=True, text=True, timeout=120)
+    lines = res.stdout.splitlines()
+    assert res.returncode == 0 and len(lines) == len(shapes)
+    taken = 0
+    for (M, N, K, sms), line in zip(shapes, lines):
+        got = [int(v) for v in line.split()]
+        p = decode_plan(M, N, K, sms)
+        if p is None:
+            assert got[0] == 0, (M, N, K, sms, got)
+            continue
+        taken += 1
+        want = [1, p["R"], p["ctas"], p["groups"], p["ks"], p["gparts"], p["warps"], p["nbox"], p["kbb"], p["wblk"],
+                p["smem"]]
+        assert got == want, (M, N, K, sms, got, want)
+    assert 500 < taken < len(shapes)
+
